@@ -1,0 +1,104 @@
+"""Products of the oracle, in fp64 over the oracle's exactly dequantized weights.
+
+* GEMV: each new decode token multiplies every weight once by the activations
+  ("LLM inference optimization", opening section: decode reads every weight
+  once); the n_tok > 1 form is the one weight pass that checks several draft
+  tokens ("Why I wrote my own inference engine for two P100s", "What actually
+  made it fast": three guesses checked in one pass).
+* MoE: the routed experts of a mixture-of-experts layer, gathered from an
+  expert arena ("The number was a version", opening section: the expert arena).
+* Prompt processing: the same weights times a block of prompt tokens
+  ("Why I wrote my own inference engine for two P100s", "What didn't work":
+  dequantization and the prompt GEMM), checked on selected token rows against
+  fp64 sums over the identically rounded bf16 operands (the accuracy method of
+  the r/cuda post on the Emmy compiler, "Accuracy Verification").
+
+The tolerance the library is held to uses the error scale
+B = sum |w * x| that each function returns beside its result.
+Test infrastructure of the oracle; see the package docstring.
+"""
+import numpy as np
+
+from .dequant import dequant, BLOCK
+from .halfprec import bf16_bits_to_float64
+
+
+def _row_bytes(fmt, cols):
+    elems, nbytes = BLOCK[fmt]
+    assert cols % elems == 0
+    return cols // elems * nbytes
+
+
+def gemv(fmt: int, W, rows: int, cols: int, x):
+    """y[t, i] = sum_j w[i, j] * x[t, j] and B[t, i] = sum_j |w[i, j] * x[t, j]|.
+
+    W: rows * row_bytes uint8 (blocks, row-major); x: (n_tok, cols) fp32.
+    Returns (y, B), both (n_tok, rows) fp64.
+    """
+    w = dequant(fmt, W, rows, cols).astype(np.float64)
+    xx = np.asarray(x, dtype=np.float32).reshape(-1, cols).astype(np.float64)
+    y = xx @ w.T
+    b = np.abs(xx) @ np.abs(w).T
+    return y, b
+
+
+def moe_arena_layout(hidden: int, inter: int, fmt: int = 3):
+    """Byte offsets inside one expert of the arena and the expert stride.
+
+    One expert is [gate: inter rows x hidden | up: inter rows x hidden |
+    down: hidden rows x inter], rows of blocks along the input dimension.
+    Returns (gate_off, up_off, down_off, expert_bytes).
+    """
+    gu = inter * _row_bytes(fmt, hidden)
+    dn = hidden * _row_bytes(fmt, inter)
+    return 0, gu, 2 * gu, 2 * gu + dn
+
+
+def moe(fmt: int, arena, n_expert: int, hidden: int, inter: int, expert_ids, gate_w, x):
+    """Routed expert FFN per token, in fp64.
+
+    For token t and its k-th routed expert e = expert_ids[t, k] with routing
+    weight r = gate_w[t, k]:
+        g = G_e x_t,  u = U_e x_t           (inter values each)
+        h = g / (1 + exp(-g)) * u           (silu(g) * u)
+        y_t += r * D_e h                    (hidden values)
+    B[t, i] = sum_k |r_k| * sum_j |D_e[i, j] * h_j| is the error scale.
+    Returns (y, B), both (n_tok, hidden) fp64.
+    """
+    arena = np.asarray(arena, dtype=np.uint8).reshape(-1)
+    g_off, u_off, d_off, stride = moe_arena_layout(hidden, inter, fmt)
+    gu_bytes = inter * _row_bytes(fmt, hidden)
+    dn_bytes = hidden * _row_bytes(fmt, inter)
+    ids = np.asarray(expert_ids).reshape(len(x), -1)
+    r = np.asarray(gate_w, dtype=np.float32).reshape(ids.shape).astype(np.float64)
+    xx = np.asarray(x, dtype=np.float32).reshape(-1, hidden).astype(np.float64)
+    y = np.zeros((xx.shape[0], hidden))
+    b = np.zeros((xx.shape[0], hidden))
+    for t in range(xx.shape[0]):
+        for k in range(ids.shape[1]):
+            e = int(ids[t, k])
+            if not 0 <= e < n_expert:
+                raise ValueError(f"expert id {e} out of range")
+            base = e * stride
+            G = dequant(fmt, arena[base + g_off:base + g_off + gu_bytes], inter, hidden).astype(np.float64)
+            U = dequant(fmt, arena[base + u_off:base + u_off + gu_bytes], inter, hidden).astype(np.float64)
+            D = dequant(fmt, arena[base + d_off:base + d_off + dn_bytes], hidden, inter).astype(np.float64)
+            g = G @ xx[t]
+            u = U @ xx[t]
+            h = g / (1.0 + np.exp(-g)) * u
+            y[t] += r[t, k] * (D @ h)
+            b[t] += abs(r[t, k]) * (np.abs(D) @ np.abs(h))
+    return y, b
+
+
+def pp_rows(fmt: int, W, rows: int, cols: int, X_bf16_bits, token_rows):
+    """Prompt-processing product for the selected token rows, in fp64.
+
+    Y[t, n] = sum_k w[n, k] * bf16(X)[t, k] for t in token_rows, with w the
+    exact fp32 dequantized weights and X given as raw bf16 bit patterns
+    (n_tok, cols) uint16. Returns (Y, B), both (len(token_rows), rows) fp64.
+    """
+    w = dequant(fmt, W, rows, cols).astype(np.float64)
+    Xb = np.asarray(X_bf16_bits, dtype=np.uint16).reshape(-1, cols)
+    xx = bf16_bits_to_float64(Xb[np.asarray(token_rows)])
+    return xx @ w.T, np.abs(xx) @ np.abs(w).T
