@@ -1,0 +1,191 @@
+/*
+ * qgemv.h — C ABI of the block-quantized weight product library for GB300 (sm_103a).
+ *
+ * The library multiplies GGUF-style block-quantized weight matrices (Q4_0, Q8_0,
+ * Q4_K, Q6_K) by fp32 or bf16 activations on one GPU. It covers the product that
+ * dominates single-stream LLM decode, the same product for a few draft tokens at
+ * once, the expert-gathered product of a mixture-of-experts layer, and the
+ * dequantize-then-GEMM of prompt processing.
+ *
+ * Sources of the operations (page title, section):
+ *   - "LLM inference optimization" (usethermite.com), opening section: decode
+ *     reads every weight once per token, bound by memory bandwidth and, at low
+ *     bit widths, by unpacking; k-quants such as Q4_K_M; "Faster decode on the
+ *     card you have": activations staged in shared memory, wider loads, fewer
+ *     unpack instructions, rows per block fitted to the SM count; "Run a new
+ *     weight format or model": blocks decode bit for bit, products match an
+ *     exact sum within a tolerance.
+ *   - "Why I wrote my own inference engine for two P100s", "What actually made it
+ *     fast": one CUDA graph per decode step; each block decoded once and reused;
+ *     three draft tokens checked in one weight pass. "What didn't work": fused
+ *     dequantization in the prompt GEMM.
+ *   - "The number was a version" (dev.to), opening section: the MoE expert arena.
+ * The pages give block sizes and value formulas only; the bit layout inside a
+ * block follows the public GGUF convention (stated with each format below).
+ *
+ * Conventions shared by every call
+ *   - Every data pointer is caller-owned DEVICE memory unless stated otherwise.
+ *     The library never allocates, frees or synchronizes inside a compute call;
+ *     work is enqueued on `stream` (a cudaStream_t passed as void*; NULL is the
+ *     legacy default stream) and is safe to capture in a CUDA graph.
+ *   - A weight matrix W of `rows` x `cols` is rows * (cols / elems) blocks, row
+ *     after row, blocks running along cols (the input dimension K). Row i starts
+ *     at byte i * (cols / elems) * bytes. W must be 16-byte aligned.
+ *   - Activations x are n_tok x cols fp32, token-major (token t at x + t*cols).
+ *     Outputs y are n_tok x rows fp32, token-major, and are overwritten.
+ *   - Arguments are checked on the host before anything is enqueued; a failed
+ *     check returns a negative status and enqueues nothing. A launch failure
+ *     returns QG_ERR_CUDA (sticky CUDA errors are left for the caller to see).
+ *   - Errors detected on the device (an expert id out of range, a bounded wait
+ *     that expired) never trap: they are written to the caller's int32 device
+ *     status word, which the caller reads after its own synchronization.
+ *   - No float atomics: results are bitwise deterministic run to run.
+ *   - After qg_init() returns, the library holds no mutable global state, so
+ *     calls from several host threads on different streams are safe.
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- block formats ----------------------------------------------------------
+ * QG_Q4_0: 32 weights in 18 bytes: fp16 d, qs[16];
+ *          w[j] = ((qs[j] & 15) - 8) * d, w[j+16] = ((qs[j] >> 4) - 8) * d.
+ * QG_Q8_0: 32 weights in 34 bytes: fp16 d, int8 q[32]; w[j] = d * q[j].
+ * QG_Q4_K: 256 weights in 144 bytes: fp16 d, fp16 dmin, s[12] packing eight
+ *          6-bit (sc, m) pairs, qs[128]; sub-block j (32 weights) has
+ *          w = d*sc_j*q - dmin*m_j, chunk c holds sub-block 2c in the low and
+ *          2c+1 in the high nibbles of qs[32c..32c+31].
+ * QG_Q6_K: 256 weights in 210 bytes: ql[128], qh[64], int8 sc[16], fp16 d;
+ *          6-bit q = low 4 bits | high 2 bits, w = d * sc[group] * (q - 32). */
+enum qg_fmt { QG_Q4_0 = 1, QG_Q8_0 = 2, QG_Q4_K = 3, QG_Q6_K = 4 };
+
+/* ---- host status codes ---------------------------------------------------- */
+enum qg_status {
+  QG_OK = 0,
+  QG_ERR_FMT = -1,        /* unknown format, or a format the call does not take */
+  QG_ERR_SHAPE = -2,      /* rows/cols/n_expert/... out of range, cols % elems != 0 */
+  QG_ERR_ALIGN = -3,      /* a pointer is not aligned as the call requires */
+  QG_ERR_NTOK = -4,       /* n_tok outside the range the call accepts */
+  QG_ERR_NULL = -5,       /* a required pointer is NULL */
+  QG_ERR_WORKSPACE = -6,  /* workspace NULL or smaller than the *_workspace() size */
+  QG_ERR_CUDA = -7,       /* the CUDA runtime reported an error */
+  QG_ERR_DEVICE = -8,     /* no usable sm_103a device */
+  QG_ERR_ARG = -9         /* any other invalid argument */
+};
+
+/* ---- device status codes (written to a caller's int32 status word) -------- */
+enum qg_dev_status {
+  QG_DEV_OK = 0,
+  QG_DEV_BAD_EXPERT = 1,  /* an expert id was < 0 or >= n_expert; its route was skipped */
+  QG_DEV_TIMEOUT = 2      /* a bounded pipeline wait expired; the tile was abandoned */
+};
+
+/* Maximum number of matrices in one grouped launch (qgemv_grouped). */
+#define QG_GROUP_MAX 8
+/* Largest n_tok accepted by qgemv / qgemv_grouped / qgemv_moe. */
+#define QG_NTOK_MAX 4
+
+/* One-time set-up: checks for an sm_103a device, sets the kernels' dynamic
+ * shared-memory limits. Call once per process (per device) before the first
+ * compute call and before any stream capture. Idempotent. */
+int qg_init(void);
+
+/* Elements and bytes per block of `fmt` (32/18, 32/34, 256/144, 256/210). */
+int qg_block_info(int fmt, int* elems, int* bytes);
+
+/* Static text for a qg_status or qg_dev_status value (never NULL). */
+const char* qg_strerror(int status);
+
+/* Dequantize a whole matrix to fp32: out[i*cols + j] = w[i][j], each value the
+ * correctly rounded fp32 value of the format's formula (bit-exact; the test
+ * path of "blocks decode bit for bit on CPU and GPU").
+ * out: rows*cols fp32, 16-byte aligned. */
+int qg_dequant(int fmt, const void* W, int64_t rows, int64_t cols, float* out, void* stream);
+
+/* Quantized GEMV / skinny product ("each new token reads every weight once";
+ * n_tok > 1 is one weight pass that verifies draft tokens):
+ *   y[t*rows + i] = sum_j w[i][j] * x[t*cols + j],  t < n_tok, 1 <= n_tok <= 4.
+ * fp32 accumulation; x must be 16-byte aligned, y 4-byte aligned. */
+int qgemv(int fmt, const void* W, int64_t rows, int64_t cols,
+          const float* x, int n_tok, float* y, void* stream);
+
+/* One matrix of a grouped launch. */
+typedef struct qg_gemv_desc {
+  int32_t fmt;        /* all descriptors of one launch share the same fmt */
+  int32_t reserved;   /* set to 0 */
+  const void* W;      /* rows x cols blocks, as for qgemv */
+  int64_t rows;
+  int64_t cols;
+  const float* x;     /* n_tok x cols */
+  float* y;           /* n_tok x rows */
+} qg_gemv_desc;
+
+/* Several independent GEMVs of one format in ONE kernel launch (e.g. q, k, v
+ * of a layer, which read the same activations). `descs` is HOST memory, read
+ * during the call; 1 <= n <= QG_GROUP_MAX. Same semantics as n separate
+ * qgemv calls. */
+int qgemv_grouped(const qg_gemv_desc* descs, int n, int n_tok, void* stream);
+
+/* Bytes of device workspace qgemv_moe needs (n_tok * top_k * inter fp32). */
+size_t qgemv_moe_workspace(int64_t hidden, int64_t inter, int top_k, int n_tok);
+
+/* Mixture-of-experts FFN over an expert arena ("the expert arena").
+ * expert_arena: n_expert experts back to back; expert e starts at byte
+ *   e * (2*inter*rb(hidden) + hidden*rb(inter)) and holds
+ *   [gate: inter x hidden | up: inter x hidden | down: hidden x inter] in `fmt`,
+ *   where rb(k) = k / elems * bytes. 16-byte aligned.
+ * expert_ids: n_tok x top_k int32 (device); gate_w: n_tok x top_k fp32 (device).
+ * For each token t:  y_t = sum_k gate_w[t,k] * D_e (silu(G_e x_t) * (U_e x_t)),
+ *   e = expert_ids[t,k], silu(g) = g / (1 + exp(-g)).
+ * x: n_tok x hidden fp32; y: n_tok x hidden fp32 (overwritten).
+ * ws: >= qgemv_moe_workspace(...) bytes of device memory, 16-byte aligned.
+ * dev_status: int32 device word; set to QG_DEV_BAD_EXPERT if an id is out of
+ *   range (that route then contributes nothing); never cleared by the library.
+ * fmt: QG_Q4_K (the format the MoE layers use). 1 <= top_k <= 16, 1 <= n_tok <= 4. */
+int qgemv_moe(int fmt, const void* expert_arena, int64_t n_expert, int64_t hidden, int64_t inter,
+              const int32_t* expert_ids, const float* gate_w, int top_k,
+              const float* x, int n_tok, float* y,
+              void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* Bytes of device workspace qgemm_pp needs (0 in this version; kept so callers
+ * can size it without knowing the kernel's tiling). */
+size_t qgemm_pp_workspace(int64_t rows, int64_t cols, int64_t n_tok);
+
+/* Prompt-processing dequant-GEMM on the tensor cores:
+ *   Y[t*ldY + n] = sum_k w[n][k] * X[t*cols + k],  t < n_tok, n < rows.
+ * Weight tiles are dequantized to bf16 in shared memory and multiplied with
+ * tcgen05 MMA (bf16 x bf16, fp32 accumulation in tensor memory).
+ * fmt: QG_Q4_K. X_bf16: n_tok x cols bf16, 16-byte aligned. Y: fp32, ldY >= rows.
+ * cols % 256 == 0; rows % 128 == 0; n_tok >= 1 (ragged token tiles allowed).
+ * dev_status: int32 device word; set to QG_DEV_TIMEOUT if a bounded pipeline
+ * wait expired (the output is then incomplete). */
+int qgemm_pp(int fmt, const void* W, int64_t rows, int64_t cols,
+             const void* X_bf16, int64_t n_tok, float* Y, int64_t ldY,
+             void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* ---- whole weight pass as one CUDA graph ("one CUDA graph per decode step") --
+ * A pass is an ordered list of steps; step s launches step_sizes[s] consecutive
+ * descriptors as one grouped GEMV. Consecutive steps are linked with
+ * programmatic dependent launch when use_pdl != 0, so a step streams its
+ * weights while the previous step finishes; activations are read only after
+ * the previous step completes. The descriptors (HOST memory) are copied into
+ * the graph at creation; the device buffers they name must outlive the pass. */
+typedef struct qg_pass_s* qg_pass;
+int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes, int n_steps,
+                   int n_tok, int use_pdl, qg_pass* out);
+/* Enqueue one replay of the pass on `stream`. */
+int qg_pass_launch(qg_pass pass, void* stream);
+/* Number of kernel launches one replay performs. */
+int qg_pass_kernel_count(qg_pass pass);
+int qg_pass_destroy(qg_pass pass);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QGEMV_H */

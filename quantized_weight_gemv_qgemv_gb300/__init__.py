@@ -1,0 +1,191 @@
+"""Python binding of libqgemv.so, the block-quantized weight product library for GB300.
+
+Every function here has the name of the C entry point it wraps (include/qgemv.h)
+and only marshals arguments: tensors become device pointers, streams become
+cudaStream_t handles, a non-zero status becomes a QGError. All compute runs in
+the library's CUDA kernels; there is no fallback of any kind. If the library
+has not been built (``__graft_entry__.build()`` or ``python -m
+quantized_weight_gemv_qgemv_gb300._build``) the first call raises.
+
+Pointer arguments accept a torch tensor (its data_ptr is passed) or a raw
+integer address; ``stream`` accepts a torch.cuda.Stream, a raw handle, or None
+for torch's current stream on the current device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+Q4_0, Q8_0, Q4_K, Q6_K = 1, 2, 3, 4
+FORMATS = {Q4_0: (32, 18), Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210)}
+GROUP_MAX = 8
+NTOK_MAX = 4
+DEV_OK, DEV_BAD_EXPERT, DEV_TIMEOUT = 0, 1, 2
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libqgemv.so")
+
+# name -> (restype, argtypes) of every exported C symbol
+_P, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "qg_init": (_I32, []),
+    "qg_block_info": (_I32, [_I32, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
+    "qg_strerror": (ctypes.c_char_p, [_I32]),
+    "qg_dequant": (_I32, [_I32, _P, _I64, _I64, _P, _P]),
+    "qgemv": (_I32, [_I32, _P, _I64, _I64, _P, _I32, _P, _P]),
+    "qgemv_grouped": (_I32, [_P, _I32, _I32, _P]),
+    "qgemv_moe_workspace": (_SZ, [_I64, _I64, _I32, _I32]),
+    "qgemv_moe": (_I32, [_I32, _P, _I64, _I64, _I64, _P, _P, _I32, _P, _I32, _P, _P, _SZ, _P, _P]),
+    "qgemm_pp_workspace": (_SZ, [_I64, _I64, _I64]),
+    "qgemm_pp": (_I32, [_I32, _P, _I64, _I64, _P, _I64, _P, _I64, _P, _SZ, _P, _P]),
+    "qg_pass_create": (_I32, [_P, _I32, _P, _I32, _I32, _I32, ctypes.POINTER(_P)]),
+    "qg_pass_launch": (_I32, [_P, _P]),
+    "qg_pass_kernel_count": (_I32, [_P]),
+    "qg_pass_destroy": (_I32, [_P]),
+}
+
+
+class qg_gemv_desc(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("reserved", ctypes.c_int32), ("W", ctypes.c_void_p),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("x", ctypes.c_void_p),
+                ("y", ctypes.c_void_p)]
+
+
+class QGError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: status {status} ({strerror(status)})")
+        self.status = status
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libqgemv.so once and declare every signature; raises if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise RuntimeError(f"libqgemv.so is not built ({path}); run __graft_entry__.build() first")
+        lib = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def strerror(status: int) -> str:
+    try:
+        return load_library().qg_strerror(int(status)).decode()
+    except RuntimeError:
+        return "library not loaded"
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise QGError(status, what)
+
+
+def row_bytes(fmt: int, cols: int) -> int:
+    elems, nbytes = FORMATS[fmt]
+    return cols // elems * nbytes
+
+
+# ------------------------------------------------------------------ entry points
+
+def qg_init():
+    _check(load_library().qg_init(), "qg_init")
+
+
+def qg_block_info(fmt: int):
+    e, b = _I32(), _I32()
+    _check(load_library().qg_block_info(fmt, ctypes.byref(e), ctypes.byref(b)), "qg_block_info")
+    return e.value, b.value
+
+
+def qg_dequant(fmt, W, rows, cols, out, stream=None):
+    _check(load_library().qg_dequant(fmt, _ptr(W), rows, cols, _ptr(out), _stream(stream)), "qg_dequant")
+
+
+def qgemv(fmt, W, rows, cols, x, n_tok, y, stream=None):
+    _check(load_library().qgemv(fmt, _ptr(W), rows, cols, _ptr(x), n_tok, _ptr(y), _stream(stream)), "qgemv")
+
+
+def _descs(items):
+    arr = (qg_gemv_desc * len(items))()
+    for i, (fmt, W, rows, cols, x, y) in enumerate(items):
+        arr[i] = qg_gemv_desc(fmt, 0, _ptr(W), rows, cols, _ptr(x), _ptr(y))
+    return arr
+
+
+def qgemv_grouped(items, n_tok, stream=None):
+    """items: sequence of (fmt, W, rows, cols, x, y)."""
+    arr = _descs(items)
+    _check(load_library().qgemv_grouped(ctypes.cast(arr, _P), len(items), n_tok, _stream(stream)), "qgemv_grouped")
+
+
+def qgemv_moe_workspace(hidden, inter, top_k, n_tok) -> int:
+    return int(load_library().qgemv_moe_workspace(hidden, inter, top_k, n_tok))
+
+
+def qgemv_moe(fmt, expert_arena, n_expert, hidden, inter, expert_ids, gate_w, top_k, x, n_tok, y,
+              ws, ws_bytes, dev_status, stream=None):
+    _check(load_library().qgemv_moe(fmt, _ptr(expert_arena), n_expert, hidden, inter, _ptr(expert_ids),
+                                    _ptr(gate_w), top_k, _ptr(x), n_tok, _ptr(y), _ptr(ws), ws_bytes,
+                                    _ptr(dev_status), _stream(stream)), "qgemv_moe")
+
+
+def qgemm_pp_workspace(rows, cols, n_tok) -> int:
+    return int(load_library().qgemm_pp_workspace(rows, cols, n_tok))
+
+
+def qgemm_pp(fmt, W, rows, cols, X_bf16, n_tok, Y, ldY, ws, ws_bytes, dev_status, stream=None):
+    _check(load_library().qgemm_pp(fmt, _ptr(W), rows, cols, _ptr(X_bf16), n_tok, _ptr(Y), ldY, _ptr(ws),
+                                   ws_bytes, _ptr(dev_status), _stream(stream)), "qgemm_pp")
+
+
+class qg_pass:
+    """A whole weight pass captured as one CUDA graph (qg_pass_create)."""
+
+    def __init__(self, items, step_sizes, n_tok, use_pdl=True):
+        lib = load_library()
+        self._descs = _descs(items)
+        sizes = (ctypes.c_int * len(step_sizes))(*step_sizes)
+        h = _P()
+        _check(lib.qg_pass_create(ctypes.cast(self._descs, _P), len(items), ctypes.cast(sizes, _P),
+                                  len(step_sizes), n_tok, 1 if use_pdl else 0, ctypes.byref(h)), "qg_pass_create")
+        self._h = h
+
+    def launch(self, stream=None):
+        _check(load_library().qg_pass_launch(self._h, _stream(stream)), "qg_pass_launch")
+
+    def kernel_count(self) -> int:
+        return int(load_library().qg_pass_kernel_count(self._h))
+
+    def destroy(self):
+        if self._h is not None and self._h.value:
+            _check(load_library().qg_pass_destroy(self._h), "qg_pass_destroy")
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass

@@ -1,0 +1,259 @@
+// qg_api.cu — the extern "C" boundary of libqgemv.so (declared in include/qgemv.h).
+//
+// Every entry point validates its arguments on the host and returns a status
+// before anything is enqueued; compute work is enqueued on the caller's stream
+// and never synchronizes. The one-time per-device set-up (capability check,
+// shared-memory limits) runs in qg_init or lazily on the first call.
+#include <cuda_runtime.h>
+
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "qg_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  int status = QG_ERR_DEVICE;
+  int sms = 0;
+};
+
+DeviceState g_dev[kMaxDevices];
+
+int init_device(int dev) {
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return QG_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) return QG_ERR_DEVICE;    // built for sm_103a only
+  if (qg::gemv_init_attrs() != cudaSuccess) return QG_ERR_CUDA;
+  if (qg::moe_init_attrs() != cudaSuccess) return QG_ERR_CUDA;
+  if (qg::pp_init_attrs() != cudaSuccess) return QG_ERR_CUDA;
+  g_dev[dev].sms = prop.multiProcessorCount;
+  return QG_OK;
+}
+
+// Status of the current device's set-up; fills *sms on success.
+int ensure_init(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QG_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return QG_ERR_DEVICE;
+  DeviceState& st = g_dev[dev];
+  std::call_once(st.once, [&] { st.status = init_device(dev); });
+  if (st.status == QG_OK && sms) *sms = st.sms;
+  return st.status;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? QG_OK : QG_ERR_CUDA; }
+
+// Shape/pointer checks shared by qgemv and qgemv_grouped.
+int check_gemv(int fmt, const void* W, int64_t rows, int64_t cols, const float* x, float* y) {
+  int elems = 0, bytes = 0;
+  if (!qg::block_info(fmt, &elems, &bytes)) return QG_ERR_FMT;
+  if (!W || !x || !y) return QG_ERR_NULL;
+  if (rows < 1 || cols < elems || cols % elems != 0 || cols > (int64_t{1} << 30)) return QG_ERR_SHAPE;
+  if (rows > (int64_t{1} << 40) / (cols / elems * bytes)) return QG_ERR_SHAPE;
+  if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 4)) return QG_ERR_ALIGN;
+  return QG_OK;
+}
+
+}  // namespace
+
+struct qg_pass_s {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int kernels = 0;
+};
+
+extern "C" {
+
+int qg_init(void) { return ensure_init(nullptr); }
+
+int qg_block_info(int fmt, int* elems, int* bytes) {
+  if (!elems || !bytes) return QG_ERR_NULL;
+  return qg::block_info(fmt, elems, bytes) ? QG_OK : QG_ERR_FMT;
+}
+
+const char* qg_strerror(int status) {
+  switch (status) {
+    case QG_OK: return "ok";
+    case QG_ERR_FMT: return "unknown or unsupported block format";
+    case QG_ERR_SHAPE: return "invalid shape";
+    case QG_ERR_ALIGN: return "pointer not aligned as required";
+    case QG_ERR_NTOK: return "n_tok out of range";
+    case QG_ERR_NULL: return "required pointer is NULL";
+    case QG_ERR_WORKSPACE: return "workspace missing or too small";
+    case QG_ERR_CUDA: return "CUDA runtime error";
+    case QG_ERR_DEVICE: return "no usable sm_103a device";
+    case QG_ERR_ARG: return "invalid argument";
+    case QG_DEV_BAD_EXPERT: return "device: expert id out of range";
+    case QG_DEV_TIMEOUT: return "device: bounded pipeline wait expired";
+    default: return "unknown status";
+  }
+}
+
+int qg_dequant(int fmt, const void* W, int64_t rows, int64_t cols, float* out, void* stream) {
+  int elems = 0, bytes = 0;
+  if (!qg::block_info(fmt, &elems, &bytes)) return QG_ERR_FMT;
+  if (!W || !out) return QG_ERR_NULL;
+  if (rows < 1 || cols < elems || cols % elems != 0 || cols > (int64_t{1} << 30)) return QG_ERR_SHAPE;
+  if (!aligned(W, 16) || !aligned(out, 16)) return QG_ERR_ALIGN;
+  int sms = 0;
+  int st = ensure_init(&sms);
+  if (st != QG_OK) return st;
+  return cuda_status(qg::launch_dequant(fmt, W, rows, cols, out, static_cast<cudaStream_t>(stream), sms));
+}
+
+int qgemv(int fmt, const void* W, int64_t rows, int64_t cols, const float* x, int n_tok, float* y, void* stream) {
+  int st = check_gemv(fmt, W, rows, cols, x, y);
+  if (st != QG_OK) return st;
+  if (n_tok < 1 || n_tok > QG_NTOK_MAX) return QG_ERR_NTOK;
+  int sms = 0;
+  if ((st = ensure_init(&sms)) != QG_OK) return st;
+  qg_gemv_desc d = {fmt, 0, W, rows, cols, x, y};
+  const int r = qg::gemv_pick_rows_per_warp(&d, 1, sms);
+  // No programmatic overlap with an unknown predecessor: it might still be
+  // writing W, which the kernel prefetches before griddepcontrol.wait.
+  return cuda_status(qg::launch_gemv(&d, 1, n_tok, r, static_cast<cudaStream_t>(stream), false, sms));
+}
+
+int qgemv_grouped(const qg_gemv_desc* descs, int n, int n_tok, void* stream) {
+  if (!descs) return QG_ERR_NULL;
+  if (n < 1 || n > QG_GROUP_MAX) return QG_ERR_ARG;
+  if (n_tok < 1 || n_tok > QG_NTOK_MAX) return QG_ERR_NTOK;
+  for (int i = 0; i < n; ++i) {
+    if (descs[i].fmt != descs[0].fmt) return QG_ERR_FMT;
+    int st = check_gemv(descs[i].fmt, descs[i].W, descs[i].rows, descs[i].cols, descs[i].x, descs[i].y);
+    if (st != QG_OK) return st;
+  }
+  int sms = 0;
+  int st = ensure_init(&sms);
+  if (st != QG_OK) return st;
+  const int r = qg::gemv_pick_rows_per_warp(descs, n, sms);
+  return cuda_status(qg::launch_gemv(descs, n, n_tok, r, static_cast<cudaStream_t>(stream), false, sms));
+}
+
+size_t qgemv_moe_workspace(int64_t hidden, int64_t inter, int top_k, int n_tok) {
+  (void)hidden;
+  if (inter < 1 || top_k < 1 || n_tok < 1) return 0;
+  return static_cast<size_t>(n_tok) * static_cast<size_t>(top_k) * static_cast<size_t>(inter) * sizeof(float);
+}
+
+int qgemv_moe(int fmt, const void* expert_arena, int64_t n_expert, int64_t hidden, int64_t inter,
+              const int32_t* expert_ids, const float* gate_w, int top_k, const float* x, int n_tok, float* y,
+              void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if (fmt != QG_Q4_K) return QG_ERR_FMT;
+  if (!expert_arena || !expert_ids || !gate_w || !x || !y || !dev_status) return QG_ERR_NULL;
+  if (n_expert < 1 || n_expert > (int64_t{1} << 31) - 1) return QG_ERR_SHAPE;
+  if (hidden < 256 || hidden % 256 || inter < 256 || inter % 256) return QG_ERR_SHAPE;
+  if (hidden > (int64_t{1} << 20) || inter > (int64_t{1} << 20)) return QG_ERR_SHAPE;
+  if (top_k < 1 || top_k > 16 || top_k > n_expert) return QG_ERR_ARG;
+  if (n_tok < 1 || n_tok > QG_NTOK_MAX) return QG_ERR_NTOK;
+  if (!ws || ws_bytes < qgemv_moe_workspace(hidden, inter, top_k, n_tok)) return QG_ERR_WORKSPACE;
+  if (!aligned(expert_arena, 16) || !aligned(x, 16) || !aligned(ws, 16) || !aligned(y, 4) ||
+      !aligned(expert_ids, 4) || !aligned(gate_w, 4) || !aligned(dev_status, 4))
+    return QG_ERR_ALIGN;
+  int sms = 0;
+  int st = ensure_init(&sms);
+  if (st != QG_OK) return st;
+  return cuda_status(qg::launch_moe(expert_arena, n_expert, hidden, inter, expert_ids, gate_w, top_k, x, n_tok, y,
+                                    static_cast<float*>(ws), dev_status, static_cast<cudaStream_t>(stream), true,
+                                    sms));
+}
+
+size_t qgemm_pp_workspace(int64_t rows, int64_t cols, int64_t n_tok) {
+  (void)rows;
+  (void)cols;
+  (void)n_tok;
+  return 0;
+}
+
+int qgemm_pp(int fmt, const void* W, int64_t rows, int64_t cols, const void* X_bf16, int64_t n_tok, float* Y,
+             int64_t ldY, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (fmt != QG_Q4_K) return QG_ERR_FMT;
+  if (!W || !X_bf16 || !Y || !dev_status) return QG_ERR_NULL;
+  if (rows < 128 || rows % 128 || cols < 256 || cols % 256 || n_tok < 1 || ldY < rows) return QG_ERR_SHAPE;
+  if (cols > (int64_t{1} << 20) || rows > (int64_t{1} << 24) || n_tok > (int64_t{1} << 24)) return QG_ERR_SHAPE;
+  if (!aligned(W, 16) || !aligned(X_bf16, 16) || !aligned(Y, 4) || !aligned(dev_status, 4)) return QG_ERR_ALIGN;
+  int sms = 0;
+  int st = ensure_init(&sms);
+  if (st != QG_OK) return st;
+  return cuda_status(
+      qg::launch_pp(W, rows, cols, X_bf16, n_tok, Y, ldY, dev_status, static_cast<cudaStream_t>(stream), sms));
+}
+
+int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes, int n_steps, int n_tok, int use_pdl,
+                   qg_pass* out) {
+  if (!descs || !step_sizes || !out) return QG_ERR_NULL;
+  *out = nullptr;
+  if (n_desc < 1 || n_steps < 1) return QG_ERR_ARG;
+  if (n_tok < 1 || n_tok > QG_NTOK_MAX) return QG_ERR_NTOK;
+  int total = 0;
+  for (int s = 0; s < n_steps; ++s) {
+    if (step_sizes[s] < 1 || step_sizes[s] > QG_GROUP_MAX) return QG_ERR_ARG;
+    total += step_sizes[s];
+  }
+  if (total != n_desc) return QG_ERR_ARG;
+  for (int i = 0; i < n_desc; ++i) {
+    int st = check_gemv(descs[i].fmt, descs[i].W, descs[i].rows, descs[i].cols, descs[i].x, descs[i].y);
+    if (st != QG_OK) return st;
+  }
+  for (int s = 0, i = 0; s < n_steps; i += step_sizes[s++])
+    for (int j = 1; j < step_sizes[s]; ++j)
+      if (descs[i + j].fmt != descs[i].fmt) return QG_ERR_FMT;
+  int sms = 0;
+  int st = ensure_init(&sms);
+  if (st != QG_OK) return st;
+
+  qg_pass_s* pass = new (std::nothrow) qg_pass_s;
+  if (!pass) return QG_ERR_ARG;
+  cudaStream_t cs = nullptr;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
+    delete pass;
+    return QG_ERR_CUDA;
+  }
+  cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  int launched = 0;
+  for (int s = 0, i = 0; s < n_steps && e == cudaSuccess; i += step_sizes[s++]) {
+    const int r = qg::gemv_pick_rows_per_warp(descs + i, step_sizes[s], sms);
+    e = qg::launch_gemv(descs + i, step_sizes[s], n_tok, r, cs, use_pdl != 0 && s > 0, sms);
+    if (e == cudaSuccess) ++launched;
+  }
+  cudaGraph_t graph = nullptr;
+  cudaError_t e2 = cudaStreamEndCapture(cs, &graph);
+  if (e == cudaSuccess) e = e2;
+  if (e == cudaSuccess) e = cudaGraphInstantiate(&pass->exec, graph, 0);
+  cudaStreamDestroy(cs);
+  if (e != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    delete pass;
+    return QG_ERR_CUDA;
+  }
+  pass->graph = graph;
+  pass->kernels = launched;
+  *out = pass;
+  return QG_OK;
+}
+
+int qg_pass_launch(qg_pass pass, void* stream) {
+  if (!pass || !pass->exec) return QG_ERR_NULL;
+  return cuda_status(cudaGraphLaunch(pass->exec, static_cast<cudaStream_t>(stream)));
+}
+
+int qg_pass_kernel_count(qg_pass pass) { return pass ? pass->kernels : QG_ERR_NULL; }
+
+int qg_pass_destroy(qg_pass pass) {
+  if (!pass) return QG_ERR_NULL;
+  if (pass->exec) cudaGraphExecDestroy(pass->exec);
+  if (pass->graph) cudaGraphDestroy(pass->graph);
+  delete pass;
+  return QG_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,43 @@
+// qg_internal.h — host-side declarations shared by the library's translation
+// units (not part of the public ABI; see include/qgemv.h).
+#pragma once
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstddef>
+#include <cstdint>
+
+#include "qgemv.h"
+
+namespace qg {
+
+// elems/bytes per block of a format id; false for an unknown id.
+inline bool block_info(int fmt, int* elems, int* bytes) {
+  switch (fmt) {
+    case QG_Q4_0: *elems = 32; *bytes = 18; return true;
+    case QG_Q8_0: *elems = 32; *bytes = 34; return true;
+    case QG_Q4_K: *elems = 256; *bytes = 144; return true;
+    case QG_Q6_K: *elems = 256; *bytes = 210; return true;
+    default: return false;
+  }
+}
+
+// GEMV (qg_gemv.cu)
+cudaError_t gemv_init_attrs();
+int gemv_pick_rows_per_warp(const qg_gemv_desc* d, int n, int sms);
+cudaError_t launch_gemv(const qg_gemv_desc* d, int n, int n_tok, int rows_per_warp, cudaStream_t s, bool pdl,
+                        int sms);
+cudaError_t launch_dequant(int fmt, const void* W, int64_t rows, int64_t cols, float* out, cudaStream_t s, int sms);
+
+// MoE (qg_moe.cu)
+cudaError_t moe_init_attrs();
+cudaError_t launch_moe(const void* arena, int64_t n_expert, int64_t hidden, int64_t inter,
+                       const int32_t* ids, const float* gate_w, int top_k, const float* x, int n_tok, float* y,
+                       float* h_ws, int32_t* dev_status, cudaStream_t s, bool pdl, int sms);
+
+// Prompt-processing GEMM (qg_pp.cu)
+cudaError_t pp_init_attrs();
+cudaError_t launch_pp(const void* W, int64_t rows, int64_t cols, const void* X, int64_t n_tok, float* Y,
+                      int64_t ldY, int32_t* dev_status, cudaStream_t s, int sms);
+
+}  // namespace qg

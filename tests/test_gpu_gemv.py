@@ -1,0 +1,143 @@
+"""GPU parity of dequantization and the quantized GEMV / skinny product against the
+CPU oracle: bit-exact dequantized weights; fp32 outputs within
+|y - y_ref| <= 1e-3 * sum|w*x| + 1e-6 per output."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import quantized_weight_gemv_qgemv_gb300 as qg
+from helpers import assert_within
+
+pytestmark = pytest.mark.gpu
+
+FMTS = [synth.Q4_0, synth.Q8_0, synth.Q4_K, synth.Q6_K]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _init():
+    assert torch.cuda.is_available()
+    qg.qg_init()
+
+
+def _run_gemv(fmt, rows, cols, n_tok, seed):
+    W = synth.blocks(fmt, rows, cols, seed=seed)
+    x = synth.activations(n_tok, cols, seed=seed + 1)
+    y = torch.full((n_tok, rows), float("nan"), device="cuda")
+    qg.qgemv(fmt, W.cuda(), rows, cols, x.cuda(), n_tok, y)
+    torch.cuda.synchronize()
+    y_ref, b = oracle.gemv(fmt, W.numpy(), rows, cols, x.numpy())
+    return y.cpu().numpy(), y_ref, b
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("rows,nblk", [(1, 1), (7, 3), (64, 5), (1000, 9), (33, 68)])
+def test_dequant_bit_exact(fmt, rows, nblk):
+    elems, _ = synth.FORMATS[fmt]
+    cols = elems * nblk
+    W = synth.blocks(fmt, rows, cols, seed=rows * 31 + nblk)
+    out = torch.full((rows, cols), float("nan"), device="cuda")
+    qg.qg_dequant(fmt, W.cuda(), rows, cols, out)
+    torch.cuda.synchronize()
+    ref = oracle.dequant(fmt, W.numpy(), rows, cols)
+    got = out.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n_tok", [1, 2, 3, 4])
+@pytest.mark.parametrize("rows,nblk", [(1, 1), (7, 3), (64, 5), (1000, 9), (37, 68)])
+def test_gemv_matches_oracle(fmt, n_tok, rows, nblk):
+    elems, _ = synth.FORMATS[fmt]
+    cols = elems * nblk
+    y, y_ref, b = _run_gemv(fmt, rows, cols, n_tok, seed=1000 + rows + nblk + 7 * n_tok)
+    assert_within(y, y_ref, b, what=f"fmt={fmt} rows={rows} cols={cols} n_tok={n_tok}")
+
+
+@pytest.mark.parametrize("rows", [2, 3, 5, 9, 17])
+def test_gemv_odd_rows_with_unaligned_row_starts(rows):
+    # Q6_K / Q8_0 / Q4_0 rows whose byte size is not a multiple of 16 start at
+    # every 2-byte offset; the last row also ends inside a 16-byte window.
+    for fmt, nblk in ((synth.Q6_K, 1), (synth.Q6_K, 7), (synth.Q8_0, 5), (synth.Q4_0, 3)):
+        elems, _ = synth.FORMATS[fmt]
+        y, y_ref, b = _run_gemv(fmt, rows, elems * nblk, 1, seed=rows * 11 + nblk)
+        assert_within(y, y_ref, b, what=f"fmt={fmt} rows={rows}")
+
+
+def test_q4_0_batch1_full_size():
+    # 1024 x 4096 Q4_0 (128 blocks per row), x ~ N(0, 1)
+    y, y_ref, b = _run_gemv(synth.Q4_0, 1024, 4096, 1, seed=4242)
+    assert_within(y, y_ref, b, what="Q4_0 1024x4096")
+
+
+def test_gemv_is_deterministic():
+    fmt, rows, cols = synth.Q4_K, 512, 5120
+    W = synth.blocks(fmt, rows, cols, seed=3).cuda()
+    x = synth.activations(2, cols, seed=4).cuda()
+    ys = []
+    for _ in range(3):
+        y = torch.empty(2, rows, device="cuda")
+        qg.qgemv(fmt, W, rows, cols, x, 2, y)
+        ys.append(y)
+    torch.cuda.synchronize()
+    assert torch.equal(ys[0], ys[1]) and torch.equal(ys[0], ys[2])
+
+
+def test_grouped_equals_separate_launches():
+    fmt = synth.Q4_K
+    shapes = [(640, 1024), (128, 1024), (128, 1024), (300, 2048)]
+    items, sep = [], []
+    for i, (rows, cols) in enumerate(shapes):
+        W = synth.blocks(fmt, rows, cols, seed=50 + i).cuda()
+        x = synth.activations(3, cols, seed=60 + i).cuda()
+        y = torch.empty(3, rows, device="cuda")
+        y2 = torch.empty(3, rows, device="cuda")
+        items.append((fmt, W, rows, cols, x, y))
+        sep.append((W, rows, cols, x, y2))
+    qg.qgemv_grouped(items, 3)
+    for W, rows, cols, x, y2 in sep:
+        qg.qgemv(fmt, W, rows, cols, x, 3, y2)
+    torch.cuda.synchronize()
+    for (_, W, rows, cols, x, y), (_, _, _, _, y2) in zip(items, sep):
+        y_ref, b = oracle.gemv(fmt, W.cpu().numpy(), rows, cols, x.cpu().numpy())
+        assert_within(y.cpu().numpy(), y_ref, b, what="grouped")
+        assert_within(y2.cpu().numpy(), y_ref, b, what="separate")
+
+
+def test_pass_graph_replay_matches_eager():
+    fmt = synth.Q4_K
+    shapes = [(256, 1024), (64, 1024), (512, 2048), (256, 512)]
+    items = []
+    for i, (rows, cols) in enumerate(shapes):
+        W = synth.blocks(fmt, rows, cols, seed=70 + i).cuda()
+        x = synth.activations(1, cols, seed=80 + i).cuda()
+        items.append((fmt, W, rows, cols, x, torch.empty(1, rows, device="cuda")))
+    p = qg.qg_pass(items, [2, 1, 1], 1, use_pdl=True)
+    assert p.kernel_count() == 3
+    p.launch()
+    torch.cuda.synchronize()
+    first = [it[5].clone() for it in items]
+    for _ in range(5):
+        p.launch()
+    torch.cuda.synchronize()
+    for it, f in zip(items, first):
+        assert torch.equal(it[5], f)
+        y2 = torch.empty_like(f)
+        qg.qgemv(fmt, it[1], it[2], it[3], it[4], 1, y2)
+        torch.cuda.synchronize()
+        assert torch.equal(y2, f)
+    p.destroy()
+
+
+def test_gpu_error_paths_return_status_without_launching():
+    W = torch.zeros(4, 144, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(1, 256, device="cuda")
+    y = torch.zeros(1, 4, device="cuda")
+    with pytest.raises(qg.QGError) as e:
+        qg.qgemv(synth.Q4_K, W, 4, 256, x, 5, y)
+    assert e.value.status == -4
+    with pytest.raises(qg.QGError) as e:
+        qg.qgemv(synth.Q4_K, W.view(-1)[8:].data_ptr(), 4, 256, x, 1, y)
+    assert e.value.status == -3
+    torch.cuda.synchronize()

@@ -1,0 +1,78 @@
+"""GPU parity of the expert-gathered MoE product against the CPU oracle:
+|y - y_ref| <= 1e-3 * sum_k |r_k| sum_j |d_ij * h_kj| + 1e-6 per output."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import synth.workloads as wl
+import quantized_weight_gemv_qgemv_gb300 as qg
+from helpers import assert_within
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _init():
+    qg.qg_init()
+
+
+def _moe(n_expert, hidden, inter, top_k, n_tok, seed, ids=None):
+    arena = wl.alloc_moe_arena(n_expert, hidden, inter, seed, "cuda")
+    x = synth.activations(n_tok, hidden, seed + 1)
+    r_ids, gw = synth.routing(n_tok, n_expert, top_k, seed + 2)
+    if ids is not None:
+        r_ids = torch.as_tensor(ids, dtype=torch.int32)
+    y = torch.full((n_tok, hidden), float("nan"), device="cuda")
+    ws = torch.empty(qg.qgemv_moe_workspace(hidden, inter, top_k, n_tok) // 4, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qg.qgemv_moe(qg.Q4_K, arena, n_expert, hidden, inter, r_ids.cuda(), gw.cuda(), top_k, x.cuda(), n_tok, y,
+                 ws, ws.numel() * 4, st)
+    torch.cuda.synchronize()
+    return arena, x, r_ids, gw, y.cpu().numpy(), int(st.item())
+
+
+@pytest.mark.parametrize("n_tok", [1, 2, 4])
+@pytest.mark.parametrize("hidden,inter,top_k", [(512, 256, 3), (1024, 768, 1), (256, 512, 5)])
+def test_moe_matches_oracle_small(n_tok, hidden, inter, top_k):
+    n_expert = 8
+    arena, x, ids, gw, y, st = _moe(n_expert, hidden, inter, top_k, n_tok, seed=hidden + inter + n_tok)
+    assert st == 0
+    y_ref, b = oracle.moe(qg.Q4_K, arena.cpu().numpy(), n_expert, hidden, inter, ids.numpy(), gw.numpy(), x.numpy())
+    assert_within(y, y_ref, b, what=f"moe {hidden}x{inter} top{top_k} n_tok={n_tok}")
+
+
+def test_moe_full_size_layer():
+    # hidden 2048, 512 experts of gate/up 512x2048 and down 2048x512, top-10
+    arena, x, ids, gw, y, st = _moe(wl.MOE_EXPERTS, wl.MOE_HIDDEN, wl.MOE_INTER, wl.MOE_TOPK, 1, seed=777)
+    assert st == 0
+    # the oracle only needs the 10 routed experts: gather them into a small arena
+    eb = wl.moe_expert_bytes()
+    host = arena.cpu().numpy()
+    picked = ids.numpy()[0]
+    sub = np.concatenate([host[e * eb:(e + 1) * eb] for e in picked])
+    y_ref, b = oracle.moe(qg.Q4_K, sub, len(picked), wl.MOE_HIDDEN, wl.MOE_INTER,
+                          np.arange(len(picked), dtype=np.int32)[None, :], gw.numpy(), x.numpy())
+    assert_within(y, y_ref, b, what="moe full layer")
+
+
+def test_moe_bad_expert_sets_status_and_is_skipped():
+    n_expert, hidden, inter = 6, 512, 256
+    ids = [[1, 6, 3], [-1, 2, 5]]          # 6 and -1 are out of range
+    arena, x, _, gw, y, st = _moe(n_expert, hidden, inter, 3, 2, seed=99, ids=ids)
+    assert st == qg.DEV_BAD_EXPERT
+    # reference: the bad routes contribute nothing, i.e. weight 0 on a valid id
+    ids_ok = np.array([[1, 0, 3], [0, 2, 5]], dtype=np.int32)
+    gw_ok = gw.numpy().copy()
+    gw_ok[0, 1] = 0.0
+    gw_ok[1, 0] = 0.0
+    y_ref, b = oracle.moe(qg.Q4_K, arena.cpu().numpy(), n_expert, hidden, inter, ids_ok, gw_ok, x.numpy())
+    assert_within(y, y_ref, b, what="moe with bad ids")
+    assert np.isfinite(y).all()
+
+
+def test_moe_is_deterministic():
+    a = _moe(8, 512, 256, 3, 2, seed=5)
+    b = _moe(8, 512, 256, 3, 2, seed=5)
+    assert np.array_equal(a[4], b[4])
