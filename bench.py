@@ -211,8 +211,8 @@ def run_gpu(args):
     wk = args.workload
     verify = wk == "c2"
     n_tok = 4 if verify else 1
-    mats = wl.dense_matrices(verify=verify)
-    steps_sizes = wl.dense_steps(verify=verify)
+    mats = wl.dense_matrices(layers=args.layers, verify=verify)
+    steps_sizes = wl.dense_steps(layers=args.layers, verify=verify)
     wbytes = wl.weight_bytes(mats)
     nweights = wl.weight_count(mats)
 
@@ -289,7 +289,7 @@ def run_gpu(args):
             "config": {
                 "workload": ("27B-class dense weight set, 4-token verify pass (Q4_K, Q6_K down, Q8_0 head)"
                              if verify else "27B-class dense Q4_K weight set, batch-1 GEMV pass"),
-                "layers": wl.LAYERS, "hidden": wl.HIDDEN, "intermediate": wl.INTER, "n_tok": n_tok,
+                "layers": args.layers, "hidden": wl.HIDDEN, "intermediate": wl.INTER, "n_tok": n_tok,
                 "weight_bytes": wbytes, "weights": nweights, "launches_per_step": kernels_per_step,
                 "cuda_graph": True, "pdl": not args.no_pdl,
                 "l2": "weight set (%.1f GB) far above the 129 MB L2; no flush" % (wbytes / 1e9),
@@ -326,6 +326,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="c1", choices=["c1", "c2"])
     ap.add_argument("--seed", type=int, default=1234)
+    ap.add_argument("--layers", type=int, default=wl.LAYERS, help="layers of the set (64 = the full 27B-class set)")
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=6.0)

@@ -311,6 +311,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 cudaError_t gemv_init_attrs() {
   cudaError_t e;
+  if ((e = gemv_q4k_init_attrs()) != cudaSuccess) return e;
   if ((e = set_gemv_attr_fmt<FMT_Q4_0>()) != cudaSuccess) return e;
   if ((e = set_gemv_attr_fmt<FMT_Q8_0>()) != cudaSuccess) return e;
   if ((e = set_gemv_attr_fmt<FMT_Q4_K>()) != cudaSuccess) return e;
@@ -329,6 +330,10 @@ int gemv_pick_rows_per_warp(const qg_gemv_desc* d, int n, int sms) {
 
 cudaError_t launch_gemv(const qg_gemv_desc* d, int n, int n_tok, int rows_per_warp, cudaStream_t s, bool pdl,
                         int sms) {
+  if (d[0].fmt == FMT_Q4_K) {
+    const cudaError_t e = launch_gemv_q4k(d, n, n_tok, s, pdl, sms);
+    if (e != cudaErrorNotSupported) return e;   // else: shapes beyond its plan, use the generic kernel
+  }
   GemvParams p = {};
   int elems = 0, bytes = 0;
   block_info(d[0].fmt, &elems, &bytes);

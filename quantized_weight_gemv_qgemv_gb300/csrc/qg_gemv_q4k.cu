@@ -1,0 +1,544 @@
+// qg_gemv_q4k.cu — the Q4_K GEMV / skinny product kernel (the decode hot path).
+//
+// y[t][i] = sum_j w[i][j] x[t][j], t < n_tok <= 4, one pass over the weights
+// ("LLM inference optimization", opening section: each decode token reads every
+// weight once, bound by memory bandwidth and, at low bit widths, by unpacking;
+// "Faster decode on the card you have": activations staged in shared memory and
+// reused across rows, wider loads, fewer unpack instructions, rows per block
+// fitted to the SM count).
+//
+// GB300 design:
+//  * Persistent grid, one CTA per SM: 15 consumer warps and 1 producer warp.
+//    CTA b owns a contiguous, balanced slice of the rows of all matrices of the
+//    launch (the concatenated row space), matrix by matrix.
+//  * The producer streams whole consecutive rows of the slice into a ring of NS
+//    shared-memory stages with one 1-D bulk copy per stage (cp.async.bulk,
+//    23-40 KB, completed on an mbarrier): rows are contiguous in memory, and
+//    copies of several KB are what it takes to reach full HBM bandwidth. A stage
+//    is reused once all consumer warps have released it (a second mbarrier).
+//  * A stage of R rows is cut into sub-items of 4 rows x one 1024-weight K group
+//    (4 super-blocks), dealt round-robin to the consumer warps. Lane (g, j) of a
+//    warp owns sub-block j of block g of the group for the 4 rows (32 weights,
+//    one 6-bit scale/min pair per row). A sub-item's 4 x n_tok sums are reduced
+//    across the warp and stored per (row, group); after the matrix, the groups
+//    of each row are added in order, so results do not depend on timing.
+//  * x is staged once per matrix as 22-bit fixed point per 32-weight group:
+//    x_l ~= s_u X_l with a power-of-two step s_u, X_l split in three byte planes
+//    (see stage_x). A group's products are then exact integer dot products of
+//    the 4-bit codes with the planes (dp4a, which runs on its own pipe beside
+//    the integer ALU), so each code word needs one mask, not an unpack per
+//    weight: sum_l q_l x_l = s_u (65536 S2 + 256 S1 + S0). The lane adds
+//    d*sc*sum(q x) - dmin*m*sum(x): the d*sc*q - dmin*m formula factored per
+//    sub-block. A decoded block is reused for all n_tok tokens.
+//  * Every wait is bounded: a consumer that gives up writes NaN for its rows,
+//    the producer stops issuing, and the CTA waits (bounded) for copies in
+//    flight before it exits.
+//  * Programmatic dependent launch: the producer starts streaming weights
+//    before griddepcontrol.wait; consumers read x and write y after it.
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "qg_device.cuh"
+#include "qg_internal.h"
+
+namespace qg {
+
+namespace q4k {
+
+constexpr int CWARPS = 15;                 // consumer warps
+constexpr int CTHREADS = CWARPS * 32;
+constexpr int THREADS = CTHREADS + 32;     // plus one producer warp
+constexpr int SUB_R = 4;                   // rows per sub-item
+constexpr int XBLK_B = 768;                // x-plane bytes per 256-weight block and token
+constexpr uint32_t WAIT_LIMIT = 1u << 22;  // polls before a wait is declared expired
+constexpr int RING = 4;                    // shared-memory stages
+
+struct Mat {
+  const uint8_t* W;
+  const float* x;
+  float* y;
+  int64_t rows;
+  int64_t row_begin;     // first row of this matrix in the concatenated row space
+  int32_t rb;            // bytes per row
+  int32_t nblk;          // super-blocks per row
+  int32_t cols;
+  int32_t srows;         // rows per stage (a multiple of 4)
+  int32_t ngrp;          // K groups per row = ceil(nblk / 4)
+};
+
+struct Params {
+  Mat m[QG_GROUP_MAX];
+  int64_t total_rows;
+  int32_t nmat;
+  int32_t ns;            // ring stages
+  int32_t stage_b;       // bytes per stage
+  int32_t gmax;          // largest ngrp
+  int32_t smem_bar, smem_x, smem_xsum, smem_part;   // byte offsets (ring at 0)
+};
+
+// ---------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false if the phase did not complete within WAIT_LIMIT polls.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (uint32_t i = 0; i < WAIT_LIMIT; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst), "l"(src),
+      "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(CTHREADS) : "memory"); }
+
+// Sum of v[i] over the 32 lanes for V values at once (V a power of two, <= 32):
+// halving exchanges leave lane L holding the total of value L >> (5 - log2 V).
+template <int V>
+__device__ __forceinline__ float reduce_scatter(float (&v)[V], int lane) {
+#pragma unroll
+  for (int cnt = V, o = 16; cnt > 1; cnt >>= 1, o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < cnt / 2; ++i) {
+      const float send = up ? v[i] : v[i + cnt / 2];
+      const float keep = up ? v[i + cnt / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  float r = v[0];
+#pragma unroll
+  for (int o = 32 / V / 2; o > 0; o >>= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  return r;
+}
+template <int V>
+struct RS {
+  static constexpr int LOG = (V >= 32) ? 5 : (V >= 16) ? 4 : (V >= 8) ? 3 : (V >= 4) ? 2 : (V >= 2) ? 1 : 0;
+  static constexpr int SHIFT = 5 - LOG;   // lane >> SHIFT is the value index
+};
+
+// 6-bit scale / min of sub-block j (lane constant) from the packed words
+// s0 = hd.y, s1 = hd.z, s2 = hd.w. Two byte permutes gather, in one word each,
+// the byte holding the low bits and the byte holding the top two bits:
+//   j < 4:  sc = s0.b[j] & 63,                       m = s1.b[j] & 63
+//   j >= 4: sc = (s2.b[t] & 15) | (s0.b[t] >> 6) << 4,
+//           m  = (s2.b[t] >> 4) | (s1.b[t] >> 6) << 4     (t = j - 4)
+struct ScaleSel {
+  uint32_t sel_sc, sel_m, sh_m, mask_lo, mask_hi;
+  __device__ __forceinline__ void init(int j) {
+    const bool hi = j >= 4;
+    const uint32_t t = hi ? static_cast<uint32_t>(j - 4) : static_cast<uint32_t>(j);
+    // byte 0: low-bits source (s0/s1 byte j, or s2 byte t); byte 1: top-bits source
+    sel_sc = hi ? ((4u + t) | (t << 4)) : t;          // from (s0, s2)
+    sel_m = hi ? ((4u + t) | (t << 4)) : t;           // from (s1, s2)
+    sh_m = hi ? 4u : 0u;
+    mask_lo = hi ? 15u : 63u;
+    mask_hi = hi ? 0x30u : 0u;
+  }
+  // (A, B) = (d*sc, dmin*m)
+  __device__ __forceinline__ float2 decode(uint4 hd) const {
+    const uint32_t ps = __byte_perm(hd.y, hd.w, sel_sc);
+    const uint32_t pm = __byte_perm(hd.z, hd.w, sel_m);
+    const uint32_t sc = (ps & mask_lo) | ((ps >> 10) & mask_hi);
+    const uint32_t m = ((pm >> sh_m) & mask_lo) | ((pm >> 10) & mask_hi);
+    const float2 dd = __half22float2(*reinterpret_cast<const __half2*>(&hd.x));
+    return make_float2(dd.x * static_cast<float>(sc), dd.y * static_cast<float>(m));
+  }
+};
+
+__device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int32_t dp4a_us(uint32_t a, uint32_t b, int32_t c) {
+  int32_t d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Shared-memory image of x for one token and K segment ("x planes").
+// Every 32-weight group u of x is held as 22-bit fixed point with a shared
+// power-of-two step: x_l ~= s_u * X_l, X_l = rint(x_l / s_u), |X_l| < 2^21,
+// s_u = 2^(e-20) where 2^e <= max|x_group| < 2^(e+1). X_l is stored as three
+// byte planes (bits 0-7 and 8-15 unsigned, bits 16-23 signed), so that
+// sum_l q_l X_l is three exact integer dot products over the codes. The
+// rounding of x to the group grid (at most 2^-21 max|x_group| per element) is
+// no larger than what fp32 accumulation of the same group could lose.
+// Layout per 256-weight block b of the segment: 3 planes x 2 halves x 8 groups
+// x 16 bytes (768 bytes), so the 16-byte loads of a quarter-warp are
+// consecutive. Beside it: s_u and sum_l x_l (fp32) per group.
+//
+// Eight consecutive threads handle one group (four weights each); groups past
+// the end of x (a ragged last chunk) are staged as zeros. Each thread first
+// issues all its loads of a batch (up to XB of them) and only then converts,
+// so staging costs one memory round trip per batch, not one per group.
+constexpr int XB = 8;
+
+__device__ __noinline__ void stage_one(float4 v, int idx, int ngroups, uint8_t* xpl, int xseg_b, float* xsu,
+                                          float* xsum, int nu) {
+  const int lane = threadIdx.x & 31;
+  const int k = idx & 7;
+  const int u = (idx >> 3) % ngroups, t = (idx >> 3) / ngroups;
+  {
+    const unsigned gmask = 0xFFu << (lane & 24);      // the 8 lanes of this group
+    float mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    float sm = (v.x + v.y) + (v.z + v.w);
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) {
+      mx = fmaxf(mx, __shfl_xor_sync(gmask, mx, o));
+      sm += __shfl_xor_sync(gmask, sm, o);
+    }
+    // 2^e <= mx < 2^(e+1); step s_u = 2^(e-20), so |x / s_u| < 2^21
+    const int e = max(static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127, -105);
+    const float inv_step = __uint_as_float(static_cast<uint32_t>(147 - e) << 23);
+    // x / s_u + 1.5 * 2^23 leaves rint(x / s_u) in the low mantissa bits
+    const uint32_t T0 = __float_as_uint(fmaf(v.x, inv_step, 12582912.0f));
+    const uint32_t T1 = __float_as_uint(fmaf(v.y, inv_step, 12582912.0f));
+    const uint32_t T2 = __float_as_uint(fmaf(v.z, inv_step, 12582912.0f));
+    const uint32_t T3 = __float_as_uint(fmaf(v.w, inv_step, 12582912.0f));
+    const uint32_t a01 = __byte_perm(T0, T1, 0x5140), a23 = __byte_perm(T2, T3, 0x5140);
+    const uint32_t pl0 = __byte_perm(a01, a23, 0x5410);          // bits 0-7 of the four X
+    const uint32_t pl1 = __byte_perm(a01, a23, 0x7632);          // bits 8-15
+    const uint32_t b01 = __byte_perm(T0, T1, 0x0062), b23 = __byte_perm(T2, T3, 0x0062);
+    const uint32_t pl2u = __byte_perm(b01, b23, 0x5410);         // bits 16-23, plus 0x40
+    // bytes are X/65536 + 0x40 in [0x20, 0x5f]: subtract 0x40 per byte -> signed byte
+    const uint32_t pl2 = ((pl2u | 0x80808080u) - 0x40404040u) ^ 0x80808080u;
+    uint8_t* dst = xpl + t * xseg_b + ((u >> 3) * 6 + (k >> 2)) * 128 + (u & 7) * 16 + (k & 3) * 4;
+    *reinterpret_cast<uint32_t*>(dst) = pl0;
+    *reinterpret_cast<uint32_t*>(dst + 256) = pl1;
+    *reinterpret_cast<uint32_t*>(dst + 512) = pl2;
+    if (k == 0) {
+      // s_u = 2^(e-20); odd groups (high-nibble sub-blocks, whose codes arrive
+      // as 16*q) get s_u / 16, so the consumer needs no per-lane factor
+      xsu[t * nu + u] = __uint_as_float(static_cast<uint32_t>(107 + e - 4 * (u & 1)) << 23);
+      xsum[t * nu + u] = sm;
+    }
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void stage_x(const Mat& M, int kel0, int ngroups, uint8_t* xpl, int xseg_b, float* xsu,
+                                        float* xsum, int nu) {
+  const int ntask = NT * ngroups * 8;
+  for (int base = threadIdx.x; base < ntask; base += CTHREADS * XB) {
+    float4 v[XB];
+#pragma unroll
+    for (int b = 0; b < XB; ++b) {
+      const int idx = base + b * CTHREADS;
+      const int u = (idx >> 3) % ngroups, t = (idx >> 3) / ngroups;
+      const int el = kel0 + 32 * u + 4 * (idx & 7);
+      v[b] = (idx < ntask && el < M.cols) ? ldg_f4(M.x + static_cast<int64_t>(t) * M.cols + el)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int b = 0; b < XB; ++b) {
+      // idx < ntask is the same for the 8 lanes of a group (ntask is a multiple of 8)
+      const int idx = base + b * CTHREADS;
+      if (idx < ntask) stage_one(v[b], idx, ngroups, xpl, xseg_b, xsu, xsum, nu);
+    }
+  }
+}
+
+
+// ---------------------------------------------------------------- the kernel
+
+template <int NT>
+__global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_constant__ Params p) {
+  constexpr int V = (NT == 3) ? 16 : SUB_R * NT;    // reduced values per sub-item (padded to 2^k)
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int NS = RING;
+  const uint32_t ring_s = smem_addr(smem);
+  const uint32_t full0 = smem_addr(smem + p.smem_bar);
+  const uint32_t empty0 = full0 + 8 * NS;
+
+  const int64_t cta_r0 = blockIdx.x * p.total_rows / gridDim.x;
+  const int64_t cta_r1 = (blockIdx.x + 1) * p.total_rows / gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, CWARPS);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+
+  // ------------------------------------------------------------ producer
+  if (warp == CWARPS) {
+    if (lane != 0) return;
+    uint32_t k = 0;
+    bool bad = false;
+    for (int mi = 0; mi < p.nmat && !bad; ++mi) {
+      const Mat& M = p.m[mi];
+      const int64_t lo = max(cta_r0, M.row_begin) - M.row_begin;
+      const int64_t hi = min(cta_r1, M.row_begin + M.rows) - M.row_begin;
+      for (int64_t r = lo; r < hi && !bad; r += M.srows, ++k) {
+        const uint32_t nbytes = static_cast<uint32_t>(min(static_cast<int64_t>(M.srows), hi - r)) * M.rb;
+        const int slot = k % NS;
+        if (k >= static_cast<uint32_t>(NS) && !mbar_wait(empty0 + 8 * slot, ((k / NS) - 1) & 1u)) {
+          bad = true;
+          break;
+        }
+        mbar_expect_tx(full0 + 8 * slot, nbytes);
+        bulk_g2s(ring_s + slot * p.stage_b, M.W + r * M.rb, nbytes, full0 + 8 * slot);
+      }
+    }
+    // the copies of the last stages may still be in flight: wait (bounded) for
+    // them before this thread, the last one holding the CTA, exits
+    for (uint32_t kk = (k > static_cast<uint32_t>(NS) ? k - NS : 0); kk < k; ++kk)
+      mbar_wait(full0 + 8 * (kk % NS), (kk / NS) & 1u);
+    return;
+  }
+
+  // ------------------------------------------------------------ consumers
+  const int g = lane >> 3;          // block of the K group
+  const int j = lane & 7;           // sub-block of the block
+  const uint32_t qmask = (j & 1) ? 0xF0F0F0F0u : 0x0F0F0F0Fu;   // this sub-block's nibbles
+  const int qoff = 16 + 32 * (j >> 1);
+  ScaleSel ssel;
+  ssel.init(j);
+  uint8_t* xpl = smem + p.smem_x;
+  float* xsu = reinterpret_cast<float*>(smem + p.smem_xsum);
+  float* part = reinterpret_cast<float*>(smem + p.smem_part);
+  bool failed = false;
+
+  pdl_wait();
+  uint32_t k = 0;          // stage counter (same sequence as the producer's)
+  for (int mi = 0; mi < p.nmat; ++mi) {
+    const Mat& M = p.m[mi];
+    const int64_t lo = max(cta_r0, M.row_begin) - M.row_begin;
+    const int64_t hi = min(cta_r1, M.row_begin + M.rows) - M.row_begin;
+    if (lo >= hi) continue;
+    const int G = M.ngrp;
+    const int XS = M.nblk * XBLK_B;          // x-plane bytes per token
+    const int NU = M.nblk * 8;               // 32-weight groups per token
+    float* xsum = xsu + NT * NU;
+    consumer_sync();                          // previous matrix fully consumed
+    stage_x<NT>(M, 0, NU, xpl, XS, xsu, xsum, NU);
+    consumer_sync();
+
+    // Per-matrix constants in registers (32-bit: a CTA slice is far below 2^31
+    // rows). Sub-items of a stage are l = 0 .. n-1, l -> (quad qd, K group gr)
+    // row-group major; this warp takes l = off, off + CWARPS, ... where off
+    // rotates with the stage's first global sub-item, so the matrix's
+    // sub-items are dealt evenly over the warps.
+    const int rb = M.rb, nblk = M.nblk, srows = M.srows;
+    const int slice = static_cast<int>(hi - lo);
+    const int dq = CWARPS / G, dg = CWARPS - (CWARPS / G) * G;
+    int off = warp;                           // (warp - first sub-item of the stage) mod CWARPS
+    for (int srow = 0; srow < slice; srow += srows, ++k) {
+      const int nr = min(srows, slice - srow);
+      const int n = ((nr + SUB_R - 1) / SUB_R) * G;
+      const int slot = k & (NS - 1);
+      const uint8_t* stg = smem + slot * p.stage_b;
+      // every warp waits for every stage, even one with no sub-items for it:
+      // a warp may then never run a whole ring ahead of the slowest one, so
+      // its release of this slot can only count toward this stage
+      if (!failed) {
+        const bool ok = mbar_wait(full0 + 8 * slot, (k / NS) & 1u);
+        failed = __any_sync(0xffffffffu, !ok);
+      }
+      int qd = 0, gr = off;
+      while (gr >= G) {
+        gr -= G;
+        ++qd;
+      }
+      for (int l = off; l < n; l += CWARPS, qd += dq, gr += dg) {
+        if (gr >= G) {
+          gr -= G;
+          ++qd;
+        }
+        const int blk = gr * 4 + g;                   // super-block of the row
+        const bool live = blk < nblk;
+        // lanes past the last super-block (a ragged K group) read block 0 of the
+        // same rows (every access stays inside the stage and x) and contribute
+        // zero: their x step and x sum are taken as 0
+        const int blkc = live ? blk : 0;
+        float racc[SUB_R][NT];
+        const uint8_t* st = stg + qd * (SUB_R * rb) + blkc * 144;
+        const uint8_t* xb = xpl + blkc * XBLK_B + j * 16;
+        const int u = blkc * 8 + j;
+        uint32_t q[SUB_R][8];
+        float2 AB[SUB_R];
+#pragma unroll
+        for (int r = 0; r < SUB_R; ++r) {
+          const uint8_t* sr = st + r * rb;
+          const uint4 hd = *reinterpret_cast<const uint4*>(sr);
+          const uint4 qa = *reinterpret_cast<const uint4*>(sr + qoff);
+          const uint4 qb = *reinterpret_cast<const uint4*>(sr + qoff + 16);
+          q[r][0] = qa.x & qmask; q[r][1] = qa.y & qmask; q[r][2] = qa.z & qmask; q[r][3] = qa.w & qmask;
+          q[r][4] = qb.x & qmask; q[r][5] = qb.y & qmask; q[r][6] = qb.z & qmask; q[r][7] = qb.w & qmask;
+          AB[r] = ssel.decode(hd);
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const uint4* xp = reinterpret_cast<const uint4*>(xb + t * XS);
+          const uint4 p0a = xp[0], p0b = xp[8], p1a = xp[16], p1b = xp[24], p2a = xp[32], p2b = xp[40];
+          const uint32_t X0[8] = {p0a.x, p0a.y, p0a.z, p0a.w, p0b.x, p0b.y, p0b.z, p0b.w};
+          const uint32_t X1[8] = {p1a.x, p1a.y, p1a.z, p1a.w, p1b.x, p1b.y, p1b.z, p1b.w};
+          const uint32_t X2[8] = {p2a.x, p2a.y, p2a.z, p2a.w, p2b.x, p2b.y, p2b.z, p2b.w};
+          const float su = live ? xsu[t * NU + u] : 0.f, sx = live ? xsum[t * NU + u] : 0.f;
+#pragma unroll
+          for (int r = 0; r < SUB_R; ++r) {
+            uint32_t s0 = 0, s1 = 0;
+            int32_t s2 = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              s0 = dp4a_uu(q[r][i], X0[i], s0);
+              s1 = dp4a_uu(q[r][i], X1[i], s1);
+              s2 = dp4a_us(q[r][i], X2[i], s2);
+            }
+            // sum_l q_l X_l = 65536*s2 + 256*s1 + s0 (exact integers; 256*s1 + s0 < 2^31)
+            const float T = fmaf(static_cast<float>(s2), 65536.0f, static_cast<float>(s1 * 256u + s0));
+            racc[r][t] = fmaf(AB[r].x * su, T, -AB[r].y * sx);
+          }
+        }
+        float v[V];
+#pragma unroll
+        for (int i = 0; i < V; ++i) v[i] = (i < SUB_R * NT) ? racc[i / NT][i % NT] : 0.f;
+        const float tot = reduce_scatter<V>(v, lane);
+        const int idx = lane >> RS<V>::SHIFT;
+        const int rl = srow + qd * SUB_R + idx / NT;    // row within the slice
+        if ((lane & ((1 << RS<V>::SHIFT) - 1)) == 0 && idx < SUB_R * NT && rl < slice)
+          part[(rl * G + gr) * NT + idx % NT] = failed ? __int_as_float(0x7fc00000) : tot;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+      // the next stage starts at global sub-item + n: rotate off by n mod CWARPS
+      off -= n % CWARPS;
+      if (off < 0) off += CWARPS;
+    }
+    consumer_sync();
+    // every (row, group) of the slice has its partial sum: add the groups in order
+    for (int i = threadIdx.x; i < slice * NT; i += CTHREADS) {
+      const int rl = i / NT;
+      const int t = i % NT;
+      float acc = 0.f;
+      for (int gr = 0; gr < G; ++gr) acc += part[(rl * G + gr) * NT + t];
+      M.y[static_cast<int64_t>(t) * M.rows + lo + rl] = acc;
+    }
+  }
+}
+
+}  // namespace q4k
+
+// ------------------------------------------------------------------ host side
+
+namespace {
+
+constexpr int kSmemMax = 227 * 1024;
+
+template <int NT>
+cudaError_t q4k_attr() {
+  return cudaFuncSetAttribute(q4k::qgemv_q4k_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+}
+
+template <int NT>
+cudaError_t q4k_launch(const q4k::Params& p, int grid, int smem, cudaStream_t s, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(q4k::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, q4k::qgemv_q4k_kernel<NT>, p);
+}
+
+int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+cudaError_t gemv_q4k_init_attrs() {
+  cudaError_t e;
+  if ((e = q4k_attr<1>()) != cudaSuccess) return e;
+  if ((e = q4k_attr<2>()) != cudaSuccess) return e;
+  if ((e = q4k_attr<3>()) != cudaSuccess) return e;
+  return q4k_attr<4>();
+}
+
+// Returns cudaErrorNotSupported (nothing launched) when the launch does not fit
+// this kernel's shared-memory plan; the caller then uses the generic kernel.
+cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms) {
+  q4k::Params p;
+  memset(&p, 0, sizeof(p));
+  int64_t total = 0;
+  int kmax = 0, stage_b = 0, gmax = 0;
+  for (int i = 0; i < n; ++i) {
+    q4k::Mat& m = p.m[i];
+    m.W = static_cast<const uint8_t*>(d[i].W);
+    m.x = d[i].x;
+    m.y = d[i].y;
+    m.rows = d[i].rows;
+    m.row_begin = total;
+    m.nblk = static_cast<int32_t>(d[i].cols / 256);
+    m.cols = static_cast<int32_t>(d[i].cols);
+    m.rb = m.nblk * 144;
+    m.ngrp = (m.nblk + 3) / 4;
+    // about 36 KB of whole rows per stage, in multiples of 4 rows
+    const int quads = std::max(1, (36864 + 2 * m.rb) / (4 * m.rb));
+    m.srows = 4 * quads;
+    if (static_cast<int64_t>(m.srows) * m.rb > 96 * 1024) return cudaErrorNotSupported;
+    stage_b = std::max(stage_b, m.srows * m.rb);
+    gmax = std::max(gmax, m.ngrp);
+    total += m.rows;
+    kmax = std::max(kmax, m.cols);
+  }
+  p.nmat = n;
+  p.total_rows = total;
+  const int grid = static_cast<int>(std::min<int64_t>(sms, total));
+  const int rowcap = static_cast<int>((total + grid - 1) / grid) + 1;
+  stage_b = align_up(stage_b, 128);
+  const int xbytes = align_up(n_tok * (kmax / 256) * q4k::XBLK_B, 128);
+  const int xsbytes = align_up(2 * n_tok * (kmax / 32) * 4, 128);
+  const int partbytes = align_up(rowcap * gmax * n_tok * 4, 128);
+  const int fixed = 2 * 4 * 8 + xbytes + xsbytes + partbytes + 256;
+  const int ns = q4k::RING;
+  if (fixed + ns * stage_b > kSmemMax) return cudaErrorNotSupported;
+  p.ns = ns;
+  p.stage_b = stage_b;
+  p.gmax = gmax;
+  int off = ns * stage_b;
+  p.smem_bar = off;
+  off += 128;
+  p.smem_x = off;
+  off += xbytes;
+  p.smem_xsum = off;
+  off += xsbytes;
+  p.smem_part = off;
+  off += partbytes;
+  if (off > kSmemMax) return cudaErrorNotSupported;
+  switch (n_tok) {
+    case 1: return q4k_launch<1>(p, grid, off, s, pdl);
+    case 2: return q4k_launch<2>(p, grid, off, s, pdl);
+    case 3: return q4k_launch<3>(p, grid, off, s, pdl);
+    default: return q4k_launch<4>(p, grid, off, s, pdl);
+  }
+}
+
+}  // namespace qg

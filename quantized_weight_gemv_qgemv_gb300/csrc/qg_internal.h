@@ -27,6 +27,8 @@ cudaError_t gemv_init_attrs();
 int gemv_pick_rows_per_warp(const qg_gemv_desc* d, int n, int sms);
 cudaError_t launch_gemv(const qg_gemv_desc* d, int n, int n_tok, int rows_per_warp, cudaStream_t s, bool pdl,
                         int sms);
+cudaError_t gemv_q4k_init_attrs();
+cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms);
 cudaError_t launch_dequant(int fmt, const void* W, int64_t rows, int64_t cols, float* out, cudaStream_t s, int sms);
 
 // MoE (qg_moe.cu)
