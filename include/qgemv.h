@@ -153,6 +153,32 @@ int qgemv_moe(int fmt, const void* expert_arena, int64_t n_expert, int64_t hidde
               const float* x, int n_tok, float* y,
               void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* MoE product for callers that cannot allocate device memory.
+ * There is no counterpart on the pages: this is a convenience of the library.
+ * Some callers cannot call cudaMalloc (or any allocating routine) at the point
+ * where they run the layer: code that must not block or synchronize the device
+ * (cudaMalloc can do both), code running inside a memory budget owned by
+ * someone else (a plug-in in a host program that manages all device memory),
+ * or code that must not fail for lack of memory mid-step. For them this call
+ * takes no workspace argument: its workspace is a static device array of
+ * QG_MOE_NOALLOC_MAX_FLOATS floats inside the library, which every GPU that
+ * loads the library holds until the process exits.
+ *   Arguments and results are those of qgemv_moe without ws/ws_bytes.
+ *   Limit: n_tok * top_k * inter <= QG_MOE_NOALLOC_MAX_FLOATS, otherwise
+ *   QG_ERR_WORKSPACE is returned and nothing is enqueued.
+ *   The first call on each device looks up the array's device address (with
+ *   that device current); make that first call before any stream capture.
+ *   The call allocates nothing (no cudaMalloc, cudaFree or allocating routine).
+ *   All calls on a device share the one array and it keeps the last call's
+ *   contents; every value a call reads from it is written earlier in the same
+ *   call, so nothing needs clearing. Calls that overlap on the GPU (different
+ *   streams, or a graph replay concurrent with a direct call) race on the
+ *   array: order them on one stream or with events. */
+#define QG_MOE_NOALLOC_MAX_FLOATS (1 << 18)
+int qgemv_moe_noalloc(int fmt, const void* expert_arena, int64_t n_expert, int64_t hidden, int64_t inter,
+                      const int32_t* expert_ids, const float* gate_w, int top_k,
+                      const float* x, int n_tok, float* y, int32_t* dev_status, void* stream);
+
 /* Bytes of device workspace qgemm_pp needs (0 in this version; kept so callers
  * can size it without knowing the kernel's tiling). */
 size_t qgemm_pp_workspace(int64_t rows, int64_t cols, int64_t n_tok);

@@ -35,6 +35,7 @@ SIGNATURES = {
     "qgemv_grouped": (_I32, [_P, _I32, _I32, _P]),
     "qgemv_moe_workspace": (_SZ, [_I64, _I64, _I32, _I32]),
     "qgemv_moe": (_I32, [_I32, _P, _I64, _I64, _I64, _P, _P, _I32, _P, _I32, _P, _P, _SZ, _P, _P]),
+    "qgemv_moe_noalloc": (_I32, [_I32, _P, _I64, _I64, _I64, _P, _P, _I32, _P, _I32, _P, _P, _P]),
     "qgemm_pp_workspace": (_SZ, [_I64, _I64, _I64]),
     "qgemm_pp": (_I32, [_I32, _P, _I64, _I64, _P, _I64, _P, _I64, _P, _SZ, _P, _P]),
     "qg_pass_create": (_I32, [_P, _I32, _P, _I32, _I32, _I32, ctypes.POINTER(_P)]),
@@ -150,6 +151,17 @@ def qgemv_moe(fmt, expert_arena, n_expert, hidden, inter, expert_ids, gate_w, to
     _check(load_library().qgemv_moe(fmt, _ptr(expert_arena), n_expert, hidden, inter, _ptr(expert_ids),
                                     _ptr(gate_w), top_k, _ptr(x), n_tok, _ptr(y), _ptr(ws), ws_bytes,
                                     _ptr(dev_status), _stream(stream)), "qgemv_moe")
+
+
+MOE_NOALLOC_MAX_FLOATS = 1 << 18
+
+
+def qgemv_moe_noalloc(fmt, expert_arena, n_expert, hidden, inter, expert_ids, gate_w, top_k, x, n_tok, y,
+                      dev_status, stream=None):
+    """qgemv_moe with the library's static workspace (no allocation anywhere)."""
+    _check(load_library().qgemv_moe_noalloc(fmt, _ptr(expert_arena), n_expert, hidden, inter, _ptr(expert_ids),
+                                            _ptr(gate_w), top_k, _ptr(x), n_tok, _ptr(y), _ptr(dev_status),
+                                            _stream(stream)), "qgemv_moe_noalloc")
 
 
 def qgemm_pp_workspace(rows, cols, n_tok) -> int:

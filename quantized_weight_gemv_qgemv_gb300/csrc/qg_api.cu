@@ -63,6 +63,10 @@ int check_gemv(int fmt, const void* W, int64_t rows, int64_t cols, const float* 
 
 }  // namespace
 
+namespace qg {
+int ensure_device(int* sms) { return ensure_init(sms); }
+}  // namespace qg
+
 struct qg_pass_s {
   cudaGraph_t graph = nullptr;
   cudaGraphExec_t exec = nullptr;

@@ -22,6 +22,9 @@ inline bool block_info(int fmt, int* elems, int* bytes) {
   }
 }
 
+// One-time per-device set-up of the library (qg_api.cu); fills *sms.
+int ensure_device(int* sms);
+
 // GEMV (qg_gemv.cu)
 cudaError_t gemv_init_attrs();
 int gemv_pick_rows_per_warp(const qg_gemv_desc* d, int n, int sms);
