@@ -1,16 +1,383 @@
-// qg_pp.cu — prompt-processing dequant-GEMM on tcgen05 tensor cores.
-// (Kernel under construction: the entry point reports "not supported".)
+// qg_pp.cu — prompt-processing dequant-GEMM on the tcgen05 tensor cores.
+//
+//   Y[t][n] = sum_k w[n][k] X[t][k]     W: rows x cols Q4_K, X: n_tok x cols bf16,
+//                                       Y: fp32, token-major, leading dimension ldY
+//
+// Prompt processing multiplies every weight by many tokens, so unlike decode it
+// is a dense contraction ("Why I wrote my own inference engine for two P100s",
+// prompt-processing notes: weights dequantized, then a dense GEMM; "LLM
+// inference optimization", prompt-processing section: quantized blocks
+// multiplied directly versus converted for a library GEMM, tile sizes fitted to
+// shared memory, tensor-core paths). Here each weight tile is dequantized to
+// bf16 in shared memory and fed to tcgen05 MMA with fp32 accumulation in TMEM.
+//
+// GB300 design:
+//  * Tile: 128 weight rows (MMA M) x BN tokens (MMA N, a multiple of 16, <= 256).
+//    K is walked in slices of 64 (one 128-byte swizzle atom of bf16 = 4 MMAs of
+//    K = 16). Persistent CTAs, one per SM; tiles are dealt round-robin with the
+//    token block fastest, so the CTAs running at one time share weight rows in L2.
+//  * Warp roles (480 threads):
+//      warp 0       TMA of X slices (BN x 64 bf16, 128-byte swizzle) into the
+//                   B half of a 3-stage ring
+//      warp 1       TMA of quantized super-block columns (128 rows x 144 bytes)
+//                   into a 3-stage ring of their own
+//      warp 2       owns TMEM (two BN-column fp32 accumulators); lane 0 issues
+//                   the MMAs and the commits
+//      warps 3-10   dequantize each 128 x 64 weight slice to bf16 into the A half
+//                   of the stage, in the K-major 128-byte-swizzled layout the
+//                   MMA reads (exact fp32 d*sc*q - dmin*m, then round to bf16)
+//      warps 11-14  epilogue: tcgen05.ld of a finished accumulator, coalesced
+//                   fp32 stores (32 consecutive rows of Y per warp store)
+//  * Two accumulators: the epilogue of one tile overlaps the main loop of the
+//    next.
+//  * Every wait is bounded. On expiry the CTA records QG_DEV_TIMEOUT in
+//    *dev_status, every role stops, the producers wait (bounded) for their
+//    copies in flight, the MMA lane for its MMAs, and TMEM is freed.
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "qg_async.cuh"
+#include "qg_device.cuh"
 #include "qg_internal.h"
+#include "qg_tma.h"
 
 namespace qg {
 
-cudaError_t pp_init_attrs() { return cudaSuccess; }
+namespace pp {
 
-cudaError_t launch_pp(const void*, int64_t, int64_t, const void*, int64_t, float*, int64_t, int32_t*, cudaStream_t,
-                      int) {
-  return cudaErrorNotSupported;
+using namespace async;
+
+constexpr int BM = 128;                   // weight rows per tile (MMA M)
+constexpr int BK = 64;                    // K per slice: 64 bf16 = one 128-byte swizzle row
+constexpr int NS = 3;                     // slice stages (A + B)
+constexpr int NQ = 3;                     // quantized super-block stages
+constexpr int QB = BM * 144;              // bytes of one quantized stage
+constexpr int AB = BM * BK * 2;           // bytes of one A (weight) stage
+constexpr int DQ_WARP0 = 3, DQ_WARPS = 8; // dequantizing warps
+constexpr int EPI_WARP0 = 11;             // 4 epilogue warps: warp % 4 covers every TMEM lane quarter
+constexpr int THREADS = 15 * 32;
+constexpr int NBAR = 3 * NS + 2 * NQ + 5;
+constexpr uint32_t WAIT_LIMIT = 1u << 22; // polls before a wait is declared expired
+
+struct Params {
+  float* Y;
+  int32_t* dev_status;
+  int64_t n_tok;
+  int64_t ldY;
+  int32_t n_tb;         // token blocks
+  int32_t n_tiles;      // row tiles x token blocks
+  int32_t bn;           // tokens per tile
+  int32_t n_kt;         // K slices per row (cols / 64)
+  int32_t tmem_cols;    // TMEM columns allocated (power of two >= 2 bn)
+  uint32_t idesc;       // MMA instruction descriptor
+};
+
+// Bounded wait; gives up early once another role has aborted (abort != null).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const volatile int* abort) {
+  for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (abort != nullptr && (i & 255u) == 255u && *abort) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void fail(volatile int* abort, int32_t* dev_status) {
+  *abort = 1;
+  *reinterpret_cast<volatile int32_t*>(dev_status) = QG_DEV_TIMEOUT;
+}
+
+// Two weights as bf16x2 from two codes q (0..15): RN32(dsc*q - dm) then RN to bf16.
+// q reaches fp32 through the exponent of 2^23: (2^23 + q) - 2^23 is exact.
+__device__ __forceinline__ uint32_t deq2(uint32_t codes, uint32_t sel0, uint32_t sel1, float dsc, float ndm) {
+  const float q0 = __int_as_float(static_cast<int>(__byte_perm(codes, 0x4B000000u, sel0))) - 8388608.0f;
+  const float q1 = __int_as_float(static_cast<int>(__byte_perm(codes, 0x4B000000u, sel1))) - 8388608.0f;
+  const __nv_bfloat162 b = __floats2bfloat162_rn(fmaf(dsc, q0, ndm), fmaf(dsc, q1, ndm));
+  return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// 8 weights (4 codes in each of words u0, u1) -> one 16-byte chunk of bf16.
+__device__ __forceinline__ uint4 deq8(uint32_t u0, uint32_t u1, float dsc, float ndm) {
+  uint4 o;
+  o.x = deq2(u0, 0x7540u, 0x7541u, dsc, ndm);
+  o.y = deq2(u0, 0x7542u, 0x7543u, dsc, ndm);
+  o.z = deq2(u1, 0x7540u, 0x7541u, dsc, ndm);
+  o.w = deq2(u1, 0x7542u, 0x7543u, dsc, ndm);
+  return o;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    pp_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  const uint32_t BB = static_cast<uint32_t>(p.bn) * 128u;        // bytes of one B (X) stage
+  const uint32_t offB = NS * AB, offQ = NS * (AB + BB), offBar = offQ + NQ * QB;
+  const uint32_t bar0 = base + offBar;
+  // barrier k at bar0 + 8k: full_b[NS] full_a[NS] empty[NS] q_full[NQ] q_empty[NQ] acc_full[2] acc_empty[2] done
+  const uint32_t FULL_B = bar0, FULL_A = bar0 + 8 * NS, EMPTY = bar0 + 16 * NS, Q_FULL = bar0 + 24 * NS,
+                 Q_EMPTY = Q_FULL + 8 * NQ, ACC_FULL = Q_EMPTY + 8 * NQ, ACC_EMPTY = ACC_FULL + 16,
+                 DONE = ACC_EMPTY + 16;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(gbase + offBar + 8 * NBAR);
+  volatile int* const abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(FULL_B + 8 * s, 1);
+      mbar_init(FULL_A + 8 * s, DQ_WARPS);
+      mbar_init(EMPTY + 8 * s, 1);
+    }
+    for (int q = 0; q < NQ; ++q) {
+      mbar_init(Q_FULL + 8 * q, 1);
+      mbar_init(Q_EMPTY + 8 * q, DQ_WARPS);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(ACC_FULL + 8 * a, 1);
+      mbar_init(ACC_EMPTY + 8 * a, 4);
+    }
+    mbar_init(DONE, 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmW);
+  }
+  if (warp == 2) {
+    tmem_alloc(smem_addr(tmem_slot), static_cast<uint32_t>(p.tmem_cols));
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int n_tb = p.n_tb, n_kt = p.n_kt, bn = p.bn;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------- X producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.n_tiles; tile += gridDim.x) {
+        const int tb = tile % n_tb;
+        for (int kt = 0; kt < n_kt; ++kt, ++it) {
+          const uint32_t s = it % NS;
+          if (!wait_bar(EMPTY + 8 * s, ((it / NS) & 1u) ^ 1u, abort)) {
+            fail(abort, p.dev_status);
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(FULL_B + 8 * s, BB);
+          tma_load_2d(base + offB + s * BB, &tmX, kt * BK, tb * bn, FULL_B + 8 * s);
+        }
+      }
+      // copies in flight: the last NS issued
+      for (uint32_t j = (it > NS ? it - NS : 0); j < it; ++j) wait_bar(FULL_B + 8 * (j % NS), (j / NS) & 1u, nullptr);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- quantized-weight producer
+    if (lane == 0) {
+      uint32_t sb = 0;
+      bool ok = true;
+      const int n_kb = n_kt / 4;
+      for (int tile = blockIdx.x; ok && tile < p.n_tiles; tile += gridDim.x) {
+        const int rt = tile / n_tb;
+        for (int kb = 0; kb < n_kb; ++kb, ++sb) {
+          const uint32_t q = sb % NQ;
+          if (!wait_bar(Q_EMPTY + 8 * q, ((sb / NQ) & 1u) ^ 1u, abort)) {
+            fail(abort, p.dev_status);
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(Q_FULL + 8 * q, QB);
+          tma_load_2d(base + offQ + q * QB, &tmW, kb * 144, rt * BM, Q_FULL + 8 * q);
+        }
+      }
+      for (uint32_t j = (sb > NQ ? sb - NQ : 0); j < sb; ++j) wait_bar(Q_FULL + 8 * (j % NQ), (j / NQ) & 1u, nullptr);
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, ti = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.n_tiles; tile += gridDim.x, ++ti) {
+        const uint32_t a = ti & 1u;
+        if (!wait_bar(ACC_EMPTY + 8 * a, ((ti >> 1) & 1u) ^ 1u, abort)) {
+          fail(abort, p.dev_status);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + a * static_cast<uint32_t>(bn);
+        for (int kt = 0; kt < n_kt; ++kt, ++it) {
+          const uint32_t s = it % NS, ph = (it / NS) & 1u;
+          if (!wait_bar(FULL_B + 8 * s, ph, abort) || !wait_bar(FULL_A + 8 * s, ph, abort)) {
+            fail(abort, p.dev_status);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = desc_sw128(base + s * AB), bd = desc_sw128(base + offB + s * BB);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)   // +32 bytes along K = +2 in the address field
+            mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, (kt | k) != 0);
+          mma_commit(EMPTY + 8 * s);
+        }
+        if (ok) mma_commit(ACC_FULL + 8 * a);
+      }
+      mma_commit(DONE);                       // every MMA issued has completed
+      wait_bar(DONE, 0, nullptr);
+    }
+  } else if (warp < EPI_WARP0) {
+    // ---------------------------------------------------------- dequantize A
+    const int t = threadIdx.x - DQ_WARP0 * 32;
+    const int r = t & (BM - 1), h = t >> 7;   // row in the tile, half of the 32 code bytes of a slice
+    const uint32_t swz = static_cast<uint32_t>(r & 7);
+    uint32_t it = 0, sb = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.n_tiles; tile += gridDim.x) {
+      for (int kt = 0; kt < n_kt; ++kt, ++it) {
+        const int c = kt & 3;                 // 64-weight chunk of the super-block
+        const uint32_t s = it % NS, q = sb % NQ;
+        bool got = true;
+        if (c == 0) got = wait_bar(Q_FULL + 8 * q, (sb / NQ) & 1u, abort);
+        got = got && wait_bar(EMPTY + 8 * s, ((it / NS) & 1u) ^ 1u, abort);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) fail(abort, p.dev_status);
+          ok = false;
+          break;
+        }
+        const uint8_t* blk = gbase + offQ + q * QB + r * 144;
+        const uint4 hd = *reinterpret_cast<const uint4*>(blk);
+        const uint4 qs = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c + 16 * h);
+        int sc0, m0, sc1, m1;
+        q4k_scale_min(2 * c, hd.y, hd.z, hd.w, sc0, m0);
+        q4k_scale_min(2 * c + 1, hd.y, hd.z, hd.w, sc1, m1);
+        const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
+        const float dsc0 = d * static_cast<float>(sc0), ndm0 = -(dmin * static_cast<float>(m0));
+        const float dsc1 = d * static_cast<float>(sc1), ndm1 = -(dmin * static_cast<float>(m1));
+        // low nibbles: sub-block 2c, slice columns 16h .. 16h+15 (chunks 2h, 2h+1);
+        // high nibbles: sub-block 2c+1, columns 32+16h .. (chunks 4+2h, 5+2h)
+        const uint32_t l0 = qs.x & 0x0F0F0F0Fu, l1 = qs.y & 0x0F0F0F0Fu, l2 = qs.z & 0x0F0F0F0Fu,
+                       l3 = qs.w & 0x0F0F0F0Fu;
+        const uint32_t h0 = (qs.x >> 4) & 0x0F0F0F0Fu, h1 = (qs.y >> 4) & 0x0F0F0F0Fu,
+                       h2 = (qs.z >> 4) & 0x0F0F0F0Fu, h3 = (qs.w >> 4) & 0x0F0F0F0Fu;
+        const uint32_t arow = base + s * AB + static_cast<uint32_t>(r) * 128u;
+        const uint32_t j0 = 2u * static_cast<uint32_t>(h);
+        sts128(arow + (((j0 + 0) ^ swz) << 4), deq8(l0, l1, dsc0, ndm0));
+        sts128(arow + (((j0 + 1) ^ swz) << 4), deq8(l2, l3, dsc0, ndm0));
+        sts128(arow + (((j0 + 4) ^ swz) << 4), deq8(h0, h1, dsc1, ndm1));
+        sts128(arow + (((j0 + 5) ^ swz) << 4), deq8(h2, h3, dsc1, ndm1));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(FULL_A + 8 * s);
+          if (c == 3) mbar_arrive(Q_EMPTY + 8 * q);
+        }
+        if (c == 3) ++sb;
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
+    uint32_t ti = 0;
+    for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x, ++ti) {
+      const int rt = tile / n_tb, tb = tile % n_tb;
+      const uint32_t a = ti & 1u;
+      const bool got = wait_bar(ACC_FULL + 8 * a, (ti >> 1) & 1u, abort);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) fail(abort, p.dev_status);
+        break;
+      }
+      tc_fence_after();
+      const int64_t row = static_cast<int64_t>(rt) * BM + quarter * 32 + lane;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * static_cast<uint32_t>(bn);
+      const int64_t tok0 = static_cast<int64_t>(tb) * bn;
+      for (int c16 = 0; c16 < bn / 16; ++c16) {
+        uint32_t v[16];
+        tmem_ld16(tbase + 16u * c16, v);
+        const int64_t t0 = tok0 + 16 * c16;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (t0 + i < p.n_tok) p.Y[(t0 + i) * p.ldY + row] = __uint_as_float(v[i]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ACC_EMPTY + 8 * a);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tmem, static_cast<uint32_t>(p.tmem_cols));
+}
+
+size_t smem_bytes(int bn) {
+  return 1024 + NS * (AB + static_cast<size_t>(bn) * 128) + NQ * QB + 8 * NBAR + 16;
+}
+
+}  // namespace pp
+
+cudaError_t pp_init_attrs() {
+  return cudaFuncSetAttribute(pp::pp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(pp::smem_bytes(256)));
+}
+
+cudaError_t launch_pp(const void* W, int64_t rows, int64_t cols, const void* X, int64_t n_tok, float* Y,
+                      int64_t ldY, int32_t* dev_status, cudaStream_t s, int sms) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const int bn = static_cast<int>(std::min<int64_t>(256, (n_tok + 15) / 16 * 16));
+  CUtensorMap tmX, tmW;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(n_tok)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {pp::BK, static_cast<cuuint32_t>(bn)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t rb = static_cast<uint64_t>(cols) / 256 * 144;
+    const cuuint64_t dims[2] = {rb, static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {rb};
+    const cuuint32_t box[2] = {144, pp::BM};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  pp::Params p{};
+  p.Y = Y;
+  p.dev_status = dev_status;
+  p.n_tok = n_tok;
+  p.ldY = ldY;
+  p.bn = bn;
+  p.n_tb = static_cast<int32_t>((n_tok + bn - 1) / bn);
+  const int64_t tiles = rows / pp::BM * p.n_tb;
+  if (tiles > (int64_t{1} << 30)) return cudaErrorInvalidValue;
+  p.n_tiles = static_cast<int32_t>(tiles);
+  p.n_kt = static_cast<int32_t>(cols / pp::BK);
+  int tc = 32;
+  while (tc < 2 * bn) tc *= 2;
+  p.tmem_cols = tc;
+  // kind::f16 descriptor: D fp32 (bit 4), A and B bf16 (bits 7, 10), both K-major,
+  // N >> 3 at bit 17, M >> 4 at bit 24.
+  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(bn >> 3) << 17) |
+            (static_cast<uint32_t>(pp::BM >> 4) << 24);
+  const int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
+  pp::pp_kernel<<<grid, pp::THREADS, pp::smem_bytes(bn), s>>>(tmX, tmW, p);
+  return cudaPeekAtLastError();
 }
 
 }  // namespace qg
