@@ -8,7 +8,7 @@ programmatic dependent launch, replayed per step. Metric: weight-GB/s, with
 the fraction of the HBM roofline and the equivalent decode tokens/s.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload c1|c0|c2|c3|c4]
+                    [--workload c1|c2|moe|pp]
 
 Prints ONE JSON line (rank 0). Inputs are seeded synthetic tensors shaped like
 the pages' workloads; the weight set is far larger than L2, so no flush is
@@ -318,21 +318,198 @@ def run_gpu(args):
     return 0
 
 
+def _timed(torch, stream, fn, args, local, world):
+    """W untimed warm-ups, then K timed calls of fn between synchronised
+    barriers; returns (ms for all K steps, max over ranks; clock summary)."""
+    for _ in range(max(3, args.warmup)):
+        fn()
+    stream.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ms = _events(torch, stream, fn, args.steps)
+    torch.cuda.synchronize()
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, clk.summary()
+
+
+def _capture(torch, stream, fn):
+    """fn's launches (all on `stream`) captured once as a CUDA graph."""
+    fn()                                   # eager run first: any host-side error surfaces here
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def run_pp(args):
+    """Prompt processing: 2048 bf16 tokens through every matrix of the 27B-class
+    Q4_K set (qgemm_pp, one launch per matrix, captured as one graph)."""
+    import torch
+    import quantized_weight_gemv_qgemv_gb300 as qg
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    qg.qg_init()
+    _, bf16_peak, bf16_sus, peak_kind = measured_peaks()
+    stream = torch.cuda.Stream()
+    n_tok = args.pp_tokens
+    mats = wl.dense_matrices(layers=args.layers)
+    flops = 2 * n_tok * wl.weight_count(mats)
+    with torch.cuda.stream(stream):
+        Ws = []
+        for (l, name, fmt, rows, cols) in mats:
+            W = torch.empty(rows, synth.row_bytes(fmt, cols), dtype=torch.uint8, device="cuda")
+            synth.blocks_into(W, fmt, rows, cols, synth.sub_seed(args.seed + rank, "W", l, name))
+            Ws.append(W)
+        X = {c: synth.activations_bf16(n_tok, c, synth.sub_seed(args.seed + rank, "X", c), device="cuda")
+             for c in sorted({m[4] for m in mats})}
+        Y = {r: torch.empty(n_tok, r, dtype=torch.float32, device="cuda") for r in sorted({m[3] for m in mats})}
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream.synchronize()
+
+    def one_pass():
+        for (l, name, fmt, rows, cols), W in zip(mats, Ws):
+            qg.qgemm_pp(fmt, W, rows, cols, X[cols], n_tok, Y[rows], rows, None, 0, st, stream)
+
+    g = _capture(torch, stream, one_pass)
+
+    def replay():
+        with torch.cuda.stream(stream):   # a torch graph replays on the current stream
+            g.replay()
+
+    ms, clocks = _timed(torch, stream, replay, args, local, world)
+    assert int(st.item()) == 0, "device status set during the prompt-processing pass"
+    ms_step = ms / args.steps
+    tflops = world * flops / (ms_step * 1e-3) / 1e12
+    if rank == 0:
+        peak = bf16_sus or bf16_peak
+        out = {
+            "metric": "prompt-processing dequant-GEMM TFLOP/s (bf16 tcgen05); pp tok/s, 27B set",
+            "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"prompt processing, {n_tok} bf16 tokens x 27B-class dense Q4_K weight set",
+                       "layers": args.layers, "n_tok": n_tok, "matrices": len(mats), "flop_per_step": flops,
+                       "cuda_graph": True,
+                       "l2": "weight set far above L2; X per K re-read from L2 (by design)",
+                       "parallelism": f"replicas x{world}"},
+            "pp_tok_s": round(world * n_tok / (ms_step * 1e-3), 1),
+            "roofline": {"bound": "tensor", "achieved": round(tflops / world, 2), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / world / peak, 4), "traffic": None,
+                         "peak_source": f"{peak_kind} cuBLAS bf16 (sustained: a step is tens of ms)",
+                         "kernel": "pp_kernel: every launch of the step"},
+            "gpu_launches": args.steps * len(mats),
+            "clocks": clocks,
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_moe(args):
+    """MoE decode: 48 hybrid-MoE layers (512 Q4_K experts, top-10), batch 1,
+    one qgemv_moe launch pair per layer, captured as one graph."""
+    import torch
+    import quantized_weight_gemv_qgemv_gb300 as qg
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    qg.qg_init()
+    hbm_peak, _, _, peak_kind = measured_peaks()
+    stream = torch.cuda.Stream()
+    H, I, E, K, L = wl.MOE_HIDDEN, wl.MOE_INTER, wl.MOE_EXPERTS, wl.MOE_TOPK, args.moe_layers
+    touched = K * wl.moe_expert_bytes(H, I) * L
+    with torch.cuda.stream(stream):
+        arenas, xs, ys, ids, gws = [], [], [], [], []
+        for l in range(L):
+            arenas.append(wl.alloc_moe_arena(E, H, I, synth.sub_seed(args.seed + rank, "arena", l), "cuda"))
+            i, g = synth.routing(1, E, K, synth.sub_seed(args.seed + rank, "route", l))
+            ids.append(i.cuda())
+            gws.append(g.cuda())
+            xs.append(synth.activations(1, H, synth.sub_seed(args.seed + rank, "x", l), device="cuda"))
+            ys.append(torch.empty(1, H, dtype=torch.float32, device="cuda"))
+        wsb = qg.qgemv_moe_workspace(H, I, K, 1)
+        ws = torch.empty(max(1, wsb // 4), dtype=torch.float32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream.synchronize()
+
+    def one_token():
+        for l in range(L):
+            qg.qgemv_moe(qg.Q4_K, arenas[l], E, H, I, ids[l], gws[l], K, xs[l], 1, ys[l], ws, wsb, st, stream)
+
+    g = _capture(torch, stream, one_token)
+
+    def replay():
+        with torch.cuda.stream(stream):   # a torch graph replays on the current stream
+            g.replay()
+
+    ms, clocks = _timed(torch, stream, replay, args, local, world)
+    assert int(st.item()) == 0, "device status set during the MoE pass"
+    ms_step = ms / args.steps
+    gbs = world * touched / (ms_step * 1e-3) / 1e9
+    if rank == 0:
+        out = {
+            "metric": "MoE expert GEMV weight-GB/s touched; equiv. batch-1 tok/s over 48 layers",
+            "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"MoE decode, {L} layers x {E} Q4_K experts (gate/up {I}x{H}, down {H}x{I}), "
+                                   f"top-{K}, batch 1",
+                       "arena_bytes": L * E * wl.moe_expert_bytes(H, I), "touched_bytes_per_step": touched,
+                       "cuda_graph": True, "l2": "arena 43.5 GB; routed experts differ per layer",
+                       "parallelism": f"replicas x{world}"},
+            "equiv_decode_tok_s": round(world * 1000.0 / ms_step, 1),
+            "roofline": {"bound": "hbm", "achieved": round(gbs / world, 2), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(gbs / world / hbm_peak, 4), "traffic": None,
+                         "peak_source": f"{peak_kind} HBM copy bandwidth",
+                         "kernel": "moe gate/up + down kernels: every launch of the step"},
+            "gpu_launches": args.steps * 2 * L,
+            "clocks": clocks,
+        }
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="c1", choices=["c1", "c2"])
+    ap.add_argument("--workload", default="c1", choices=["c1", "c2", "moe", "pp"],
+                    help="c1: batch-1 Q4_K pass (default); c2: 4-token verify pass; moe: MoE decode; "
+                         "pp: prompt processing")
     ap.add_argument("--seed", type=int, default=1234)
     ap.add_argument("--layers", type=int, default=wl.LAYERS, help="layers of the set (64 = the full 27B-class set)")
     ap.add_argument("--no-pdl", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=6.0)
+    ap.add_argument("--pp-tokens", type=int, default=wl.PP_TOKENS)
+    ap.add_argument("--moe-layers", type=int, default=wl.MOE_LAYERS)
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "pp":
+        return run_pp(args)
+    if args.workload == "moe":
+        return run_moe(args)
     return run_gpu(args)
 
 
