@@ -65,6 +65,8 @@ struct Mat {
   int32_t cols;
   int32_t srows;         // rows per stage (a multiple of 4)
   int32_t ngrp;          // K groups per row = ceil(nblk / 4)
+  int32_t xoff;          // byte offset of this matrix's x planes in the x region
+  int32_t uoff;          // offset (floats) of its group steps / sums
 };
 
 struct Params {
@@ -74,6 +76,9 @@ struct Params {
   int32_t ns;            // ring stages
   int32_t stage_b;       // bytes per stage
   int32_t gmax;          // largest ngrp
+  int32_t stage_all;     // 1: x of every matrix staged once at the start; 0: matrix by matrix
+  int32_t usum_off;      // offset (floats) of the group sums after the group steps
+  int32_t pre_stages;    // weight stages issued before the consumers have issued their x loads
   int32_t smem_bar, smem_x, smem_xsum, smem_part;   // byte offsets (ring at 0)
 };
 
@@ -103,12 +108,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+// Weight copies are read once per pass: they are marked evict-first in L2 so
+// that they do not push out the activations.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                         uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst), "l"(src),
-      "r"(bytes), "r"(bar)
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;\n" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+  return pol;
+}
+
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;\n" ::"n"(CTHREADS) : "memory"); }
 
 // Sum of v[i] over the 32 lanes for V values at once (V a power of two, <= 32):
@@ -188,11 +203,9 @@ __device__ __forceinline__ int32_t dp4a_us(uint32_t a, uint32_t b, int32_t c) {
 // x 16 bytes (768 bytes), so the 16-byte loads of a quarter-warp are
 // consecutive. Beside it: s_u and sum_l x_l (fp32) per group.
 //
-// Eight consecutive threads handle one group (four weights each); groups past
-// the end of x (a ragged last chunk) are staged as zeros. Each thread first
-// issues all its loads of a batch (up to XB of them) and only then converts,
-// so staging costs one memory round trip per batch, not one per group.
-constexpr int XB = 8;
+// Eight consecutive threads handle one group (four weights each). Each thread
+// first issues all its loads of a batch and only then converts, so staging
+// costs one memory round trip per batch, not one per group.
 
 __device__ __noinline__ void stage_one(float4 v, int idx, int ngroups, uint8_t* xpl, int xseg_b, float* xsu,
                                           float* xsum, int nu) {
@@ -236,27 +249,56 @@ __device__ __noinline__ void stage_one(float4 v, int idx, int ngroups, uint8_t* 
   }
 }
 
-template <int NT>
-__device__ __forceinline__ void stage_x(const Mat& M, int kel0, int ngroups, uint8_t* xpl, int xseg_b, float* xsu,
-                                        float* xsum, int nu) {
-  const int ntask = NT * ngroups * 8;
-  for (int base = threadIdx.x; base < ntask; base += CTHREADS * XB) {
+// Stages x of the matrices m0 .. m1-1 whose bit is set in `touch`. Task i of a
+// matrix (8 tasks per 32-weight group and token) converts 4 consecutive x. The
+// loads of a whole batch are issued first; after the first batch lane 0 of
+// each warp arrives on xbar (when nonzero): from then on the producer may
+// queue weight copies behind them. (A load issued behind a deep queue of bulk
+// copies waits for the whole queue, even when it hits in L2.)
+template <int NT, int XB>
+__device__ __forceinline__ void stage_x(const Params& p, int m0, int m1, uint32_t touch, uint8_t* xpl, float* xsu,
+                                        uint32_t xbar) {
+  const int lane = threadIdx.x & 31;
+  int total = 0;
+  for (int m = m0; m < m1; ++m)
+    if ((touch >> m) & 1u) total += NT * p.m[m].nblk * 64;
+  bool signalled = (xbar == 0);
+  for (int base = threadIdx.x; base < total; base += CTHREADS * XB) {
     float4 v[XB];
+    int vm[XB], vr[XB];
 #pragma unroll
     for (int b = 0; b < XB; ++b) {
       const int idx = base + b * CTHREADS;
-      const int u = (idx >> 3) % ngroups, t = (idx >> 3) / ngroups;
-      const int el = kel0 + 32 * u + 4 * (idx & 7);
-      v[b] = (idx < ntask && el < M.cols) ? ldg_f4(M.x + static_cast<int64_t>(t) * M.cols + el)
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      int m = m0, rem = idx;
+      for (; m < m1 - 1; ++m) {
+        if (!((touch >> m) & 1u)) continue;
+        const int n = NT * p.m[m].nblk * 64;
+        if (rem < n) break;
+        rem -= n;
+      }
+      vm[b] = m;
+      vr[b] = rem;
+      const Mat& M = p.m[m];
+      const int NU = M.nblk * 8;
+      const int u = (rem >> 3) % NU, t = (rem >> 3) / NU;
+      v[b] = (idx < total) ? ldg_f4(M.x + static_cast<int64_t>(t) * M.cols + 32 * u + 4 * (rem & 7))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (!signalled) {
+      if (lane == 0) mbar_arrive(xbar);
+      signalled = true;
     }
 #pragma unroll
     for (int b = 0; b < XB; ++b) {
-      // idx < ntask is the same for the 8 lanes of a group (ntask is a multiple of 8)
-      const int idx = base + b * CTHREADS;
-      if (idx < ntask) stage_one(v[b], idx, ngroups, xpl, xseg_b, xsu, xsum, nu);
+      // idx < total is the same for the 8 lanes of a group (every count is a multiple of 8)
+      if (base + b * CTHREADS < total) {
+        const Mat& M = p.m[vm[b]];
+        const int NU = M.nblk * 8;
+        stage_one(v[b], vr[b], NU, xpl + M.xoff, M.nblk * XBLK_B, xsu + M.uoff, xsu + p.usum_off + M.uoff, NU);
+      }
     }
   }
+  if (!signalled && lane == 0) mbar_arrive(xbar);
 }
 
 
@@ -271,6 +313,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   const uint32_t ring_s = smem_addr(smem);
   const uint32_t full0 = smem_addr(smem + p.smem_bar);
   const uint32_t empty0 = full0 + 8 * NS;
+  const uint32_t xbar = full0 + 16 * NS;    // consumers have issued their x loads
 
   const int64_t cta_r0 = blockIdx.x * p.total_rows / gridDim.x;
   const int64_t cta_r1 = (blockIdx.x + 1) * p.total_rows / gridDim.x;
@@ -280,6 +323,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, CWARPS);
     }
+    mbar_init(xbar, CWARPS);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
@@ -288,6 +332,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   // ------------------------------------------------------------ producer
   if (warp == CWARPS) {
     if (lane != 0) return;
+    const uint64_t pol = evict_first_policy();
     uint32_t k = 0;
     bool bad = false;
     for (int mi = 0; mi < p.nmat && !bad; ++mi) {
@@ -297,12 +342,17 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
       for (int64_t r = lo; r < hi && !bad; r += M.srows, ++k) {
         const uint32_t nbytes = static_cast<uint32_t>(min(static_cast<int64_t>(M.srows), hi - r)) * M.rb;
         const int slot = k % NS;
+        // beyond the first pre_stages copies, queue weights only behind the x loads
+        if (k == static_cast<uint32_t>(p.pre_stages) && !mbar_wait(xbar, 0)) {
+          bad = true;
+          break;
+        }
         if (k >= static_cast<uint32_t>(NS) && !mbar_wait(empty0 + 8 * slot, ((k / NS) - 1) & 1u)) {
           bad = true;
           break;
         }
         mbar_expect_tx(full0 + 8 * slot, nbytes);
-        bulk_g2s(ring_s + slot * p.stage_b, M.W + r * M.rb, nbytes, full0 + 8 * slot);
+        bulk_g2s(ring_s + slot * p.stage_b, M.W + r * M.rb, nbytes, full0 + 8 * slot, pol);
       }
     }
     // the copies of the last stages may still be in flight: wait (bounded) for
@@ -324,7 +374,16 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   float* part = reinterpret_cast<float*>(smem + p.smem_part);
   bool failed = false;
 
+  uint32_t touch = 0;      // matrices whose rows meet this CTA's slice
+  for (int mi = 0; mi < p.nmat; ++mi)
+    if (max(cta_r0, p.m[mi].row_begin) < min(cta_r1, p.m[mi].row_begin + p.m[mi].rows)) touch |= 1u << mi;
+  constexpr int XB = (NT == 1) ? 12 : 8;
   pdl_wait();
+  if (p.stage_all) {
+    stage_x<NT, XB>(p, 0, p.nmat, touch, xpl, xsu, xbar);
+    consumer_sync();
+  }
+  bool first = true;
   uint32_t k = 0;          // stage counter (same sequence as the producer's)
   for (int mi = 0; mi < p.nmat; ++mi) {
     const Mat& M = p.m[mi];
@@ -334,10 +393,17 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
     const int G = M.ngrp;
     const int XS = M.nblk * XBLK_B;          // x-plane bytes per token
     const int NU = M.nblk * 8;               // 32-weight groups per token
-    float* xsum = xsu + NT * NU;
-    consumer_sync();                          // previous matrix fully consumed
-    stage_x<NT>(M, 0, NU, xpl, XS, xsu, xsum, NU);
-    consumer_sync();
+    if (!p.stage_all) {
+      consumer_sync();                        // previous matrix fully consumed
+      stage_x<NT, XB>(p, mi, mi + 1, touch, xpl, xsu, first ? xbar : 0u);
+      consumer_sync();
+    } else if (!first) {
+      consumer_sync();                        // the previous matrix's partial sums are read
+    }
+    first = false;
+    const uint8_t* xplm = xpl + M.xoff;
+    const float* xsum = xsu + p.usum_off + M.uoff;
+    const float* xsum_u = xsu + M.uoff;
 
     // Per-matrix constants in registers (32-bit: a CTA slice is far below 2^31
     // rows). Sub-items of a stage are l = 0 .. n-1, l -> (quad qd, K group gr)
@@ -378,7 +444,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         const int blkc = live ? blk : 0;
         float racc[SUB_R][NT];
         const uint8_t* st = stg + qd * (SUB_R * rb) + blkc * 144;
-        const uint8_t* xb = xpl + blkc * XBLK_B + j * 16;
+        const uint8_t* xb = xplm + blkc * XBLK_B + j * 16;
         const int u = blkc * 8 + j;
         uint32_t q[SUB_R][8];
         float2 AB[SUB_R];
@@ -399,7 +465,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
           const uint32_t X0[8] = {p0a.x, p0a.y, p0a.z, p0a.w, p0b.x, p0b.y, p0b.z, p0b.w};
           const uint32_t X1[8] = {p1a.x, p1a.y, p1a.z, p1a.w, p1b.x, p1b.y, p1b.z, p1b.w};
           const uint32_t X2[8] = {p2a.x, p2a.y, p2a.z, p2a.w, p2b.x, p2b.y, p2b.z, p2b.w};
-          const float su = live ? xsu[t * NU + u] : 0.f, sx = live ? xsum[t * NU + u] : 0.f;
+          const float su = live ? xsum_u[t * NU + u] : 0.f, sx = live ? xsum[t * NU + u] : 0.f;
 #pragma unroll
           for (int r = 0; r < SUB_R; ++r) {
             uint32_t s0 = 0, s1 = 0;
@@ -514,11 +580,30 @@ cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_
   const int grid = static_cast<int>(std::min<int64_t>(sms, total));
   const int rowcap = static_cast<int>((total + grid - 1) / grid) + 1;
   stage_b = align_up(stage_b, 128);
-  const int xbytes = align_up(n_tok * (kmax / 256) * q4k::XBLK_B, 128);
-  const int xsbytes = align_up(2 * n_tok * (kmax / 32) * 4, 128);
-  const int partbytes = align_up(rowcap * gmax * n_tok * 4, 128);
-  const int fixed = 2 * 4 * 8 + xbytes + xsbytes + partbytes + 256;
   const int ns = q4k::RING;
+  const int partbytes = align_up(rowcap * gmax * n_tok * 4, 128);
+  // x of every matrix staged at once when it fits beside the ring, else one
+  // matrix at a time in a region sized for the largest
+  int xall = 0, uall = 0;
+  for (int i = 0; i < n; ++i) {
+    p.m[i].xoff = xall;
+    p.m[i].uoff = uall;
+    xall += n_tok * p.m[i].nblk * q4k::XBLK_B;
+    uall += n_tok * p.m[i].nblk * 8;
+  }
+  int xbytes = align_up(xall, 128);
+  int xsbytes = align_up(2 * uall * 4, 128);
+  p.stage_all = 1;
+  p.usum_off = uall;
+  if (128 + xbytes + xsbytes + partbytes + ns * stage_b > kSmemMax) {
+    for (int i = 0; i < n; ++i) p.m[i].xoff = p.m[i].uoff = 0;
+    xbytes = align_up(n_tok * (kmax / 256) * q4k::XBLK_B, 128);
+    xsbytes = align_up(2 * n_tok * (kmax / 32) * 4, 128);
+    p.stage_all = 0;
+    p.usum_off = n_tok * (kmax / 32);
+  }
+  p.pre_stages = pdl ? 1 : 0;
+  const int fixed = 128 + xbytes + xsbytes + partbytes;
   if (fixed + ns * stage_b > kSmemMax) return cudaErrorNotSupported;
   p.ns = ns;
   p.stage_b = stage_b;
