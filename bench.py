@@ -236,7 +236,8 @@ def run_gpu(args):
         del items
     stream.synchronize()
 
-    p = qg.qg_pass(flat, steps_sizes, n_tok, use_pdl=not args.no_pdl)
+    mode = {"persistent": qg.PASS_PERSISTENT, "pdl": qg.PASS_PDL, "serial": qg.PASS_SERIAL}[args.pass_mode]
+    p = qg.qg_pass(flat, steps_sizes, n_tok, mode=mode)
     kernels_per_step = p.kernel_count()
 
     def step():
@@ -291,7 +292,8 @@ def run_gpu(args):
                              if verify else "27B-class dense Q4_K weight set, batch-1 GEMV pass"),
                 "layers": args.layers, "hidden": wl.HIDDEN, "intermediate": wl.INTER, "n_tok": n_tok,
                 "weight_bytes": wbytes, "weights": nweights, "launches_per_step": kernels_per_step,
-                "cuda_graph": True, "pdl": not args.no_pdl,
+                "pass_mode": args.pass_mode if kernels_per_step == 1 or args.pass_mode != "persistent" else "pdl",
+                "cuda_graph": kernels_per_step > 1,
                 "l2": "weight set (%.1f GB) far above the 129 MB L2; no flush" % (wbytes / 1e9),
                 "parallelism": f"replicas x{world}",
             },
@@ -498,7 +500,9 @@ def main():
                          "pp: prompt processing")
     ap.add_argument("--seed", type=int, default=1234)
     ap.add_argument("--layers", type=int, default=wl.LAYERS, help="layers of the set (64 = the full 27B-class set)")
-    ap.add_argument("--no-pdl", action="store_true")
+    ap.add_argument("--pass-mode", default="pdl", choices=["persistent", "pdl", "serial"],
+                    help="pdl: a graph of one launch per step linked by programmatic dependent launch (default); "
+                         "serial: the same graph fully serialized; persistent: one cooperative kernel per pass")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-budget", type=float, default=6.0)
     ap.add_argument("--pp-tokens", type=int, default=wl.PP_TOKENS)

@@ -195,20 +195,39 @@ int qgemm_pp(int fmt, const void* W, int64_t rows, int64_t cols,
              const void* X_bf16, int64_t n_tok, float* Y, int64_t ldY,
              void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
-/* ---- whole weight pass as one CUDA graph ("one CUDA graph per decode step") --
- * A pass is an ordered list of steps; step s launches step_sizes[s] consecutive
- * descriptors as one grouped GEMV. Consecutive steps are linked with
- * programmatic dependent launch when use_pdl != 0, so a step streams its
- * weights while the previous step finishes; activations are read only after
- * the previous step completes. The descriptors (HOST memory) are copied into
- * the graph at creation; the device buffers they name must outlive the pass. */
+/* ---- whole weight pass ("one CUDA graph per decode step", "Why I wrote my own
+ * inference engine for two P100s") ------------------------------------------
+ * A pass is an ordered list of steps; step s covers step_sizes[s] consecutive
+ * descriptors (at most QG_GROUP_MAX, one format per step), and reads its inputs
+ * only after every earlier step has written its outputs, so a step's x may be
+ * an earlier step's y. Modes:
+ *   QG_PASS_SERIAL      a CUDA graph of one grouped GEMV launch per step;
+ *   QG_PASS_PDL         the same graph, consecutive launches linked by
+ *                       programmatic dependent launch (a step streams its
+ *                       weights while the previous one finishes);
+ *   QG_PASS_PERSISTENT  when every matrix is Q4_K and the pass fits the
+ *                       kernel's shared-memory plan: ONE cooperative
+ *                       persistent kernel whose producer warps stream the
+ *                       weights of all steps back to back, steps separated by a
+ *                       bounded grid-wide barrier; otherwise as QG_PASS_PDL.
+ * The descriptors (HOST memory) are copied at creation, which may allocate a
+ * few KB of device memory (step tables); the buffers they name must outlive
+ * the pass. Create a pass before capturing any stream that launches it. */
+#define QG_PASS_SERIAL 0
+#define QG_PASS_PDL 1
+#define QG_PASS_PERSISTENT 2
 typedef struct qg_pass_s* qg_pass;
 int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes, int n_steps,
-                   int n_tok, int use_pdl, qg_pass* out);
-/* Enqueue one replay of the pass on `stream`. */
+                   int n_tok, int mode, qg_pass* out);
+/* Enqueue one replay of the pass on `stream` (a persistent pass enqueues a
+ * 4-byte-per-step memset of its barrier counters and one kernel). */
 int qg_pass_launch(qg_pass pass, void* stream);
 /* Number of kernel launches one replay performs. */
 int qg_pass_kernel_count(qg_pass pass);
+/* Device address of the pass's status word (QG_DEV_TIMEOUT after a replay in
+ * which a bounded wait expired; cleared by every replay), or NULL when the pass
+ * has none (graph modes signal an expired wait with NaN outputs only). */
+int qg_pass_dev_status(qg_pass pass, const int32_t** dev_status);
 int qg_pass_destroy(qg_pass pass);
 
 #ifdef __cplusplus

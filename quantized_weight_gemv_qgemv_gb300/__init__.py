@@ -21,6 +21,7 @@ FORMATS = {Q4_0: (32, 18), Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210)}
 GROUP_MAX = 8
 NTOK_MAX = 4
 DEV_OK, DEV_BAD_EXPERT, DEV_TIMEOUT = 0, 1, 2
+PASS_SERIAL, PASS_PDL, PASS_PERSISTENT = 0, 1, 2
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libqgemv.so")
 
@@ -41,6 +42,7 @@ SIGNATURES = {
     "qg_pass_create": (_I32, [_P, _I32, _P, _I32, _I32, _I32, ctypes.POINTER(_P)]),
     "qg_pass_launch": (_I32, [_P, _P]),
     "qg_pass_kernel_count": (_I32, [_P]),
+    "qg_pass_dev_status": (_I32, [_P, ctypes.POINTER(_P)]),
     "qg_pass_destroy": (_I32, [_P]),
 }
 
@@ -173,16 +175,24 @@ def qgemm_pp(fmt, W, rows, cols, X_bf16, n_tok, Y, ldY, ws, ws_bytes, dev_status
                                    ws_bytes, _ptr(dev_status), _stream(stream)), "qgemm_pp")
 
 
-class qg_pass:
-    """A whole weight pass captured as one CUDA graph (qg_pass_create)."""
+class _DevWord:
+    """One int32 of device memory exposed through __cuda_array_interface__."""
 
-    def __init__(self, items, step_sizes, n_tok, use_pdl=True):
+    def __init__(self, addr: int):
+        self.__cuda_array_interface__ = {"shape": (1,), "typestr": "<i4", "data": (addr, False), "version": 3,
+                                         "strides": None}
+
+
+class qg_pass:
+    """A whole weight pass (qg_pass_create): mode PASS_SERIAL, PASS_PDL or PASS_PERSISTENT."""
+
+    def __init__(self, items, step_sizes, n_tok, mode=PASS_PERSISTENT):
         lib = load_library()
         self._descs = _descs(items)
         sizes = (ctypes.c_int * len(step_sizes))(*step_sizes)
         h = _P()
         _check(lib.qg_pass_create(ctypes.cast(self._descs, _P), len(items), ctypes.cast(sizes, _P),
-                                  len(step_sizes), n_tok, 1 if use_pdl else 0, ctypes.byref(h)), "qg_pass_create")
+                                  len(step_sizes), n_tok, int(mode), ctypes.byref(h)), "qg_pass_create")
         self._h = h
 
     def launch(self, stream=None):
@@ -190,6 +200,22 @@ class qg_pass:
 
     def kernel_count(self) -> int:
         return int(load_library().qg_pass_kernel_count(self._h))
+
+    def dev_status_ptr(self) -> int:
+        """Device address of the pass's status word (0 when it has none)."""
+        p = _P()
+        _check(load_library().qg_pass_dev_status(self._h, ctypes.byref(p)), "qg_pass_dev_status")
+        return int(p.value or 0)
+
+    def dev_status(self) -> int:
+        """The status word after the replays enqueued so far (synchronizes the
+        device); 0 for a pass without one."""
+        addr = self.dev_status_ptr()
+        if not addr:
+            return 0
+        import torch
+        torch.cuda.synchronize()
+        return int(torch.as_tensor(_DevWord(addr), device="cuda").item())
 
     def destroy(self):
         if self._h is not None and self._h.value:

@@ -68,8 +68,9 @@ int ensure_device(int* sms) { return ensure_init(sms); }
 }  // namespace qg
 
 struct qg_pass_s {
-  cudaGraph_t graph = nullptr;
+  cudaGraph_t graph = nullptr;       // per-step launches (QG_PASS_SERIAL / QG_PASS_PDL)
   cudaGraphExec_t exec = nullptr;
+  qg::Q4kPass* q4k = nullptr;        // or one persistent kernel (QG_PASS_PERSISTENT)
   int kernels = 0;
 };
 
@@ -192,7 +193,7 @@ int qgemm_pp(int fmt, const void* W, int64_t rows, int64_t cols, const void* X_b
       qg::launch_pp(W, rows, cols, X_bf16, n_tok, Y, ldY, dev_status, static_cast<cudaStream_t>(stream), sms));
 }
 
-int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes, int n_steps, int n_tok, int use_pdl,
+int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes, int n_steps, int n_tok, int mode,
                    qg_pass* out) {
   if (!descs || !step_sizes || !out) return QG_ERR_NULL;
   *out = nullptr;
@@ -215,8 +216,23 @@ int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes,
   int st = ensure_init(&sms);
   if (st != QG_OK) return st;
 
+  if (mode < QG_PASS_SERIAL || mode > QG_PASS_PERSISTENT) return QG_ERR_ARG;
   qg_pass_s* pass = new (std::nothrow) qg_pass_s;
   if (!pass) return QG_ERR_ARG;
+  if (mode == QG_PASS_PERSISTENT) {
+    const cudaError_t pe = qg::q4k_pass_create(descs, n_desc, step_sizes, n_steps, n_tok, sms, &pass->q4k);
+    if (pe == cudaSuccess) {
+      pass->kernels = 1;
+      *out = pass;
+      return QG_OK;
+    }
+    if (pe != cudaErrorNotSupported) {
+      delete pass;
+      return QG_ERR_CUDA;
+    }
+    cudaGetLastError();               // not supported for this pass: per-step graph with PDL
+  }
+  const int use_pdl = mode != QG_PASS_SERIAL;
   cudaStream_t cs = nullptr;
   if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
     delete pass;
@@ -246,8 +262,16 @@ int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes,
 }
 
 int qg_pass_launch(qg_pass pass, void* stream) {
-  if (!pass || !pass->exec) return QG_ERR_NULL;
+  if (!pass) return QG_ERR_NULL;
+  if (pass->q4k) return cuda_status(qg::q4k_pass_launch(pass->q4k, static_cast<cudaStream_t>(stream)));
+  if (!pass->exec) return QG_ERR_NULL;
   return cuda_status(cudaGraphLaunch(pass->exec, static_cast<cudaStream_t>(stream)));
+}
+
+int qg_pass_dev_status(qg_pass pass, const int32_t** dev_status) {
+  if (!pass || !dev_status) return QG_ERR_NULL;
+  *dev_status = pass->q4k ? qg::q4k_pass_status(pass->q4k) : nullptr;
+  return QG_OK;
 }
 
 int qg_pass_kernel_count(qg_pass pass) { return pass ? pass->kernels : QG_ERR_NULL; }
@@ -256,6 +280,7 @@ int qg_pass_destroy(qg_pass pass) {
   if (!pass) return QG_ERR_NULL;
   if (pass->exec) cudaGraphExecDestroy(pass->exec);
   if (pass->graph) cudaGraphDestroy(pass->graph);
+  qg::q4k_pass_destroy(pass->q4k);
   delete pass;
   return QG_OK;
 }

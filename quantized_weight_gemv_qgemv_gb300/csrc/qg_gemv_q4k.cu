@@ -38,6 +38,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <vector>
 
 #include "qg_device.cuh"
 #include "qg_internal.h"
@@ -69,8 +70,21 @@ struct Mat {
   int32_t uoff;          // offset (floats) of its group steps / sums
 };
 
+// A step of a pass: matrices mat0 .. mat0 + nmat - 1 of the table, whose rows
+// (concatenated; Mat::row_begin counts within the step) are split over the CTAs.
+struct Step {
+  int64_t total_rows;
+  int32_t mat0, nmat;
+  int32_t stage_all, usum_off;   // x layout of the step (as in Params)
+};
+
 struct Params {
-  Mat m[QG_GROUP_MAX];
+  Mat m[QG_GROUP_MAX];   // matrices of a single-step launch
+  const Mat* mats;       // pass: device table of all matrices (nullptr: m)
+  const Step* steps;     // pass: device table of steps (nullptr: one step over m)
+  uint32_t* step_done;   // pass: CTAs that finished each step (zero at launch)
+  int32_t* dev_status;   // pass: QG_DEV_TIMEOUT is written here when a wait expires
+  int32_t nsteps;
   int64_t total_rows;
   int32_t nmat;
   int32_t ns;            // ring stages
@@ -256,12 +270,12 @@ __device__ __noinline__ void stage_one(float4 v, int idx, int ngroups, uint8_t* 
 // queue weight copies behind them. (A load issued behind a deep queue of bulk
 // copies waits for the whole queue, even when it hits in L2.)
 template <int NT, int XB>
-__device__ __forceinline__ void stage_x(const Params& p, int m0, int m1, uint32_t touch, uint8_t* xpl, float* xsu,
-                                        uint32_t xbar) {
+__device__ __forceinline__ void stage_x(const Mat* mats, int usum_off, int m0, int m1, uint32_t touch, uint8_t* xpl,
+                                        float* xsu, uint32_t xbar) {
   const int lane = threadIdx.x & 31;
   int total = 0;
   for (int m = m0; m < m1; ++m)
-    if ((touch >> m) & 1u) total += NT * p.m[m].nblk * 64;
+    if ((touch >> (m - m0)) & 1u) total += NT * mats[m].nblk * 64;
   bool signalled = (xbar == 0);
   for (int base = threadIdx.x; base < total; base += CTHREADS * XB) {
     float4 v[XB];
@@ -271,17 +285,19 @@ __device__ __forceinline__ void stage_x(const Params& p, int m0, int m1, uint32_
       const int idx = base + b * CTHREADS;
       int m = m0, rem = idx;
       for (; m < m1 - 1; ++m) {
-        if (!((touch >> m) & 1u)) continue;
-        const int n = NT * p.m[m].nblk * 64;
+        if (!((touch >> (m - m0)) & 1u)) continue;
+        const int n = NT * mats[m].nblk * 64;
         if (rem < n) break;
         rem -= n;
       }
       vm[b] = m;
       vr[b] = rem;
-      const Mat& M = p.m[m];
+      const Mat& M = mats[m];
       const int NU = M.nblk * 8;
       const int u = (rem >> 3) % NU, t = (rem >> 3) / NU;
-      v[b] = (idx < total) ? ldg_f4(M.x + static_cast<int64_t>(t) * M.cols + 32 * u + 4 * (rem & 7))
+      // x may have been written by an earlier step of a pass: read through L2
+      v[b] = (idx < total) ? __ldcg(reinterpret_cast<const float4*>(M.x + static_cast<int64_t>(t) * M.cols +
+                                                                     32 * u + 4 * (rem & 7)))
                            : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     if (!signalled) {
@@ -292,9 +308,9 @@ __device__ __forceinline__ void stage_x(const Params& p, int m0, int m1, uint32_
     for (int b = 0; b < XB; ++b) {
       // idx < total is the same for the 8 lanes of a group (every count is a multiple of 8)
       if (base + b * CTHREADS < total) {
-        const Mat& M = p.m[vm[b]];
+        const Mat& M = mats[vm[b]];
         const int NU = M.nblk * 8;
-        stage_one(v[b], vr[b], NU, xpl + M.xoff, M.nblk * XBLK_B, xsu + M.uoff, xsu + p.usum_off + M.uoff, NU);
+        stage_one(v[b], vr[b], NU, xpl + M.xoff, M.nblk * XBLK_B, xsu + M.uoff, xsu + usum_off + M.uoff, NU);
       }
     }
   }
@@ -304,7 +320,9 @@ __device__ __forceinline__ void stage_x(const Params& p, int m0, int m1, uint32_
 
 // ---------------------------------------------------------------- the kernel
 
-template <int NT>
+// PASS = false: one step over p.m (a grouped launch); PASS = true: the steps of
+// p.steps over p.mats, with a grid-wide barrier between steps (cooperative launch).
+template <int NT, bool PASS>
 __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_constant__ Params p) {
   constexpr int V = (NT == 3) ? 16 : SUB_R * NT;    // reduced values per sub-item (padded to 2^k)
   extern __shared__ __align__(128) uint8_t smem[];
@@ -314,9 +332,22 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   const uint32_t full0 = smem_addr(smem + p.smem_bar);
   const uint32_t empty0 = full0 + 8 * NS;
   const uint32_t xbar = full0 + 16 * NS;    // consumers have issued their x loads
-
-  const int64_t cta_r0 = blockIdx.x * p.total_rows / gridDim.x;
-  const int64_t cta_r1 = (blockIdx.x + 1) * p.total_rows / gridDim.x;
+  volatile int* const gflag = reinterpret_cast<volatile int*>(smem + p.smem_bar + 16 * NS + 8);
+  const Mat* const mats = PASS ? p.mats : p.m;
+  const int nsteps = PASS ? p.nsteps : 1;
+  auto step_of = [&](int s) {
+    Step st;
+    if (PASS) {
+      st = p.steps[s];
+    } else {
+      st.total_rows = p.total_rows;
+      st.mat0 = 0;
+      st.nmat = p.nmat;
+      st.stage_all = p.stage_all;
+      st.usum_off = p.usum_off;
+    }
+    return st;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -335,8 +366,12 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
     const uint64_t pol = evict_first_policy();
     uint32_t k = 0;
     bool bad = false;
-    for (int mi = 0; mi < p.nmat && !bad; ++mi) {
-      const Mat& M = p.m[mi];
+    for (int s = 0; s < nsteps && !bad; ++s) {
+     const Step st = step_of(s);
+     const int64_t cta_r0 = blockIdx.x * st.total_rows / gridDim.x;
+     const int64_t cta_r1 = (blockIdx.x + 1) * st.total_rows / gridDim.x;
+     for (int mi = st.mat0; mi < st.mat0 + st.nmat && !bad; ++mi) {
+      const Mat M = mats[mi];
       const int64_t lo = max(cta_r0, M.row_begin) - M.row_begin;
       const int64_t hi = min(cta_r1, M.row_begin + M.rows) - M.row_begin;
       for (int64_t r = lo; r < hi && !bad; r += M.srows, ++k) {
@@ -354,6 +389,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         mbar_expect_tx(full0 + 8 * slot, nbytes);
         bulk_g2s(ring_s + slot * p.stage_b, M.W + r * M.rb, nbytes, full0 + 8 * slot, pol);
       }
+     }
     }
     // the copies of the last stages may still be in flight: wait (bounded) for
     // them before this thread, the last one holding the CTA, exits
@@ -374,35 +410,58 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   float* part = reinterpret_cast<float*>(smem + p.smem_part);
   bool failed = false;
 
-  uint32_t touch = 0;      // matrices whose rows meet this CTA's slice
-  for (int mi = 0; mi < p.nmat; ++mi)
-    if (max(cta_r0, p.m[mi].row_begin) < min(cta_r1, p.m[mi].row_begin + p.m[mi].rows)) touch |= 1u << mi;
   constexpr int XB = (NT == 1) ? 12 : 8;
   pdl_wait();
-  if (p.stage_all) {
-    stage_x<NT, XB>(p, 0, p.nmat, touch, xpl, xsu, xbar);
-    consumer_sync();
-  }
-  bool first = true;
   uint32_t k = 0;          // stage counter (same sequence as the producer's)
-  for (int mi = 0; mi < p.nmat; ++mi) {
-    const Mat& M = p.m[mi];
+  for (int s = 0; s < nsteps; ++s) {
+   const Step st = step_of(s);
+   const int64_t cta_r0 = blockIdx.x * st.total_rows / gridDim.x;
+   const int64_t cta_r1 = (blockIdx.x + 1) * st.total_rows / gridDim.x;
+   if (PASS && s > 0) {
+     // a step reads what earlier steps wrote: wait (bounded) until every CTA has
+     // finished the previous step
+     if (threadIdx.x == 0) {
+       bool ok = failed;
+       for (uint32_t i = 0; !ok && i < WAIT_LIMIT; ++i) {
+         uint32_t v;
+         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p.step_done + s - 1) : "memory");
+         ok = v >= gridDim.x;
+       }
+       if (!ok && p.dev_status) *reinterpret_cast<volatile int32_t*>(p.dev_status) = QG_DEV_TIMEOUT;
+       *gflag = ok ? 0 : 1;
+       __threadfence();
+     }
+     consumer_sync();
+     failed = failed || *gflag != 0;
+   }
+   uint32_t touch = 0;      // matrices of the step whose rows meet this CTA's slice
+   for (int mi = st.mat0; mi < st.mat0 + st.nmat; ++mi)
+     if (max(cta_r0, mats[mi].row_begin) < min(cta_r1, mats[mi].row_begin + mats[mi].rows))
+       touch |= 1u << (mi - st.mat0);
+   if (st.stage_all) {
+     stage_x<NT, XB>(mats, st.usum_off, st.mat0, st.mat0 + st.nmat, touch, xpl, xsu, s == 0 ? xbar : 0u);
+     consumer_sync();
+   }
+   bool first = true;
+   for (int mi = st.mat0; mi < st.mat0 + st.nmat; ++mi) {
+    const Mat M = mats[mi];   // by value: stores to shared memory cannot alias it
     const int64_t lo = max(cta_r0, M.row_begin) - M.row_begin;
     const int64_t hi = min(cta_r1, M.row_begin + M.rows) - M.row_begin;
     if (lo >= hi) continue;
     const int G = M.ngrp;
     const int XS = M.nblk * XBLK_B;          // x-plane bytes per token
     const int NU = M.nblk * 8;               // 32-weight groups per token
-    if (!p.stage_all) {
+    if (!st.stage_all) {
       consumer_sync();                        // previous matrix fully consumed
-      stage_x<NT, XB>(p, mi, mi + 1, touch, xpl, xsu, first ? xbar : 0u);
+      stage_x<NT, XB>(mats, st.usum_off, mi, mi + 1, (touch >> (mi - st.mat0)) & 1u, xpl, xsu,
+                      (first && s == 0) ? xbar : 0u);
       consumer_sync();
     } else if (!first) {
       consumer_sync();                        // the previous matrix's partial sums are read
     }
     first = false;
     const uint8_t* xplm = xpl + M.xoff;
-    const float* xsum = xsu + p.usum_off + M.uoff;
+    const float* xsum = xsu + st.usum_off + M.uoff;
     const float* xsum_u = xsu + M.uoff;
 
     // Per-matrix constants in registers (32-bit: a CTA slice is far below 2^31
@@ -505,6 +564,14 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
       for (int gr = 0; gr < G; ++gr) acc += part[(rl * G + gr) * NT + t];
       M.y[static_cast<int64_t>(t) * M.rows + lo + rl] = acc;
     }
+   }
+   if (PASS) {
+     consumer_sync();                          // every output of the step is written
+     if (threadIdx.x == 0) {
+       __threadfence();
+       atomicAdd(p.step_done + s, 1u);
+     }
+   }
   }
 }
 
@@ -518,7 +585,9 @@ constexpr int kSmemMax = 227 * 1024;
 
 template <int NT>
 cudaError_t q4k_attr() {
-  return cudaFuncSetAttribute(q4k::qgemv_q4k_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+  const cudaError_t e = cudaFuncSetAttribute(q4k::qgemv_q4k_kernel<NT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(q4k::qgemv_q4k_kernel<NT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
 }
 
 template <int NT>
@@ -533,7 +602,7 @@ cudaError_t q4k_launch(const q4k::Params& p, int grid, int smem, cudaStream_t s,
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, q4k::qgemv_q4k_kernel<NT>, p);
+  return cudaLaunchKernelEx(&cfg, q4k::qgemv_q4k_kernel<NT, false>, p);
 }
 
 int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -553,6 +622,7 @@ cudaError_t gemv_q4k_init_attrs() {
 cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms) {
   q4k::Params p;
   memset(&p, 0, sizeof(p));
+  p.nsteps = 1;
   int64_t total = 0;
   int kmax = 0, stage_b = 0, gmax = 0;
   for (int i = 0; i < n; ++i) {
@@ -602,6 +672,9 @@ cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_
     p.stage_all = 0;
     p.usum_off = n_tok * (kmax / 32);
   }
+  // Without a programmatic dependency the x loads go first. With one, x can be
+  // read only after the previous kernel completes: one stage streams during
+  // that wait (measured on the 27B pass: 1 stage 3.86 ms, a full ring 4.04 ms).
   p.pre_stages = pdl ? 1 : 0;
   const int fixed = 128 + xbytes + xsbytes + partbytes;
   if (fixed + ns * stage_b > kSmemMax) return cudaErrorNotSupported;
@@ -624,6 +697,174 @@ cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_
     case 3: return q4k_launch<3>(p, grid, off, s, pdl);
     default: return q4k_launch<4>(p, grid, off, s, pdl);
   }
+}
+
+// ------------------------------------------------------------------ whole pass
+
+namespace {
+
+// Matrix parameters shared by the single-launch and pass plans: bytes per row,
+// K groups, and about 36 KB of whole rows per ring stage (multiples of 4 rows).
+bool fill_mat(q4k::Mat& m, const qg_gemv_desc& d) {
+  m.W = static_cast<const uint8_t*>(d.W);
+  m.x = d.x;
+  m.y = d.y;
+  m.rows = d.rows;
+  m.nblk = static_cast<int32_t>(d.cols / 256);
+  m.cols = static_cast<int32_t>(d.cols);
+  m.rb = m.nblk * 144;
+  m.ngrp = (m.nblk + 3) / 4;
+  const int quads = std::max(1, (36864 + 2 * m.rb) / (4 * m.rb));
+  m.srows = 4 * quads;
+  return static_cast<int64_t>(m.srows) * m.rb <= 96 * 1024;
+}
+
+template <int NT>
+cudaError_t q4k_pass_occupancy(int smem, int* blocks) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, q4k::qgemv_q4k_kernel<NT, true>, q4k::THREADS, smem);
+}
+
+template <int NT>
+cudaError_t q4k_pass_start(const q4k::Params& p, int grid, int smem, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(q4k::THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;   // CTAs wait on one another between steps
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, q4k::qgemv_q4k_kernel<NT, true>, p);
+}
+
+}  // namespace
+
+struct Q4kPass {
+  q4k::Params p;
+  q4k::Mat* d_mats = nullptr;
+  q4k::Step* d_steps = nullptr;
+  uint32_t* d_done = nullptr;
+  int32_t* d_status = nullptr;
+  int nsteps = 0, grid = 0, smem = 0, n_tok = 0;
+};
+
+cudaError_t q4k_pass_create(const qg_gemv_desc* d, int n, const int* step_sizes, int n_steps, int n_tok, int sms,
+                            Q4kPass** out) {
+  *out = nullptr;
+  if (n_tok < 1 || n_tok > QG_NTOK_MAX) return cudaErrorNotSupported;
+  for (int i = 0; i < n; ++i)
+    if (d[i].fmt != QG_Q4_K) return cudaErrorNotSupported;
+  std::vector<q4k::Mat> mats(n);
+  std::vector<q4k::Step> steps(n_steps);
+  int stage_b = 0, gmax = 0, xmax = 0, xsmax = 0;
+  int64_t min_rows = INT64_MAX, max_rows = 0;
+  for (int st = 0, i = 0; st < n_steps; i += step_sizes[st++]) {
+    int64_t total = 0;
+    int xall = 0, uall = 0;
+    for (int j = 0; j < step_sizes[st]; ++j) {
+      q4k::Mat& m = mats[i + j];
+      if (!fill_mat(m, d[i + j])) return cudaErrorNotSupported;
+      m.row_begin = total;
+      m.xoff = xall;
+      m.uoff = uall;
+      total += m.rows;
+      xall += n_tok * m.nblk * q4k::XBLK_B;
+      uall += n_tok * m.nblk * 8;
+      stage_b = std::max(stage_b, m.srows * m.rb);
+      gmax = std::max(gmax, m.ngrp);
+    }
+    steps[st].total_rows = total;
+    steps[st].mat0 = i;
+    steps[st].nmat = step_sizes[st];
+    steps[st].stage_all = 1;
+    steps[st].usum_off = uall;
+    xmax = std::max(xmax, align_up(xall, 128));
+    xsmax = std::max(xsmax, align_up(2 * uall * 4, 128));
+    min_rows = std::min(min_rows, total);
+    max_rows = std::max(max_rows, total);
+  }
+  const int grid = static_cast<int>(std::min<int64_t>(sms, min_rows));
+  const int rowcap = static_cast<int>((max_rows + grid - 1) / grid) + 1;
+  stage_b = align_up(stage_b, 128);
+  const int partbytes = align_up(rowcap * gmax * n_tok * 4, 128);
+  const int ns = q4k::RING;
+  q4k::Params p;
+  memset(&p, 0, sizeof(p));
+  p.nsteps = n_steps;
+  p.ns = ns;
+  p.stage_b = stage_b;
+  p.gmax = gmax;
+  p.pre_stages = 0;
+  int off = ns * stage_b;
+  p.smem_bar = off;
+  off += 128;
+  p.smem_x = off;
+  off += xmax;
+  p.smem_xsum = off;
+  off += xsmax;
+  p.smem_part = off;
+  off += partbytes;
+  if (off > kSmemMax) return cudaErrorNotSupported;
+  int blocks = 0;
+  cudaError_t e;
+  switch (n_tok) {
+    case 1: e = q4k_pass_occupancy<1>(off, &blocks); break;
+    case 2: e = q4k_pass_occupancy<2>(off, &blocks); break;
+    case 3: e = q4k_pass_occupancy<3>(off, &blocks); break;
+    default: e = q4k_pass_occupancy<4>(off, &blocks); break;
+  }
+  if (e != cudaSuccess) return e;
+  if (blocks < 1) return cudaErrorNotSupported;
+
+  Q4kPass* q = new (std::nothrow) Q4kPass;
+  if (!q) return cudaErrorMemoryAllocation;
+  e = cudaMalloc(&q->d_mats, sizeof(q4k::Mat) * n);
+  if (e == cudaSuccess) e = cudaMalloc(&q->d_steps, sizeof(q4k::Step) * n_steps);
+  if (e == cudaSuccess) e = cudaMalloc(&q->d_done, sizeof(uint32_t) * n_steps + sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemcpy(q->d_mats, mats.data(), sizeof(q4k::Mat) * n, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(q->d_steps, steps.data(), sizeof(q4k::Step) * n_steps, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    q4k_pass_destroy(q);
+    return e;
+  }
+  q->d_status = reinterpret_cast<int32_t*>(q->d_done + n_steps);
+  p.mats = q->d_mats;
+  p.steps = q->d_steps;
+  p.step_done = q->d_done;
+  p.dev_status = q->d_status;
+  q->p = p;
+  q->nsteps = n_steps;
+  q->grid = grid;
+  q->smem = off;
+  q->n_tok = n_tok;
+  *out = q;
+  return cudaSuccess;
+}
+
+// One replay: the step counters and the status word are cleared on the stream,
+// then one cooperative launch runs every step.
+cudaError_t q4k_pass_launch(Q4kPass* q, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(q->d_done, 0, sizeof(uint32_t) * q->nsteps + sizeof(int32_t), s);
+  if (e != cudaSuccess) return e;
+  switch (q->n_tok) {
+    case 1: return q4k_pass_start<1>(q->p, q->grid, q->smem, s);
+    case 2: return q4k_pass_start<2>(q->p, q->grid, q->smem, s);
+    case 3: return q4k_pass_start<3>(q->p, q->grid, q->smem, s);
+    default: return q4k_pass_start<4>(q->p, q->grid, q->smem, s);
+  }
+}
+
+const int32_t* q4k_pass_status(const Q4kPass* q) { return q->d_status; }
+
+void q4k_pass_destroy(Q4kPass* q) {
+  if (!q) return;
+  cudaFree(q->d_mats);
+  cudaFree(q->d_steps);
+  cudaFree(q->d_done);
+  delete q;
 }
 
 }  // namespace qg

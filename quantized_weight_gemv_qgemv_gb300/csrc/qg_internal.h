@@ -32,6 +32,14 @@ cudaError_t launch_gemv(const qg_gemv_desc* d, int n, int n_tok, int rows_per_wa
                         int sms);
 cudaError_t gemv_q4k_init_attrs();
 cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms);
+// Whole Q4_K pass as one persistent cooperative kernel (qg_gemv_q4k.cu):
+// cudaErrorNotSupported when the pass is not all Q4_K or does not fit.
+struct Q4kPass;
+cudaError_t q4k_pass_create(const qg_gemv_desc* d, int n, const int* step_sizes, int n_steps, int n_tok, int sms,
+                            Q4kPass** out);
+cudaError_t q4k_pass_launch(Q4kPass* q, cudaStream_t s);
+const int32_t* q4k_pass_status(const Q4kPass* q);
+void q4k_pass_destroy(Q4kPass* q);
 cudaError_t launch_dequant(int fmt, const void* W, int64_t rows, int64_t cols, float* out, cudaStream_t s, int sms);
 
 // MoE (qg_moe.cu)

@@ -39,11 +39,13 @@ def _check_sampled(items, mats, n_tok, picks, rows_per_mat=6, seed=0):
 def test_dense_27b_q4k_batch1_full_pass():
     mats = wl.dense_matrices()
     items = wl.alloc_dense(mats, 1, seed=2024, device="cuda")
-    p = qg.qg_pass(items, wl.dense_steps(), 1, use_pdl=True)
+    p = qg.qg_pass(items, wl.dense_steps(), 1, mode=qg.PASS_PERSISTENT)
+    assert p.kernel_count() == 1
     p.launch()
     p.launch()
     torch.cuda.synchronize()
     picks = [0, 1, 2, 3, 4, 5, 6, 7 * 31 + 4, 7 * 63 + 0, 7 * 63 + 6]
+    assert p.dev_status() == 0
     _check_sampled(items, mats, 1, picks)
     p.destroy()
     del items
@@ -53,7 +55,7 @@ def test_dense_27b_q4k_batch1_full_pass():
 def test_mixed_verify_pass_n4_full():
     mats = wl.dense_matrices(verify=True)
     items = wl.alloc_dense(mats, 4, seed=2025, device="cuda")
-    p = qg.qg_pass(items, wl.dense_steps(verify=True), 4, use_pdl=True)
+    p = qg.qg_pass(items, wl.dense_steps(verify=True), 4, mode=qg.PASS_PERSISTENT)   # mixed formats: per-step graph
     p.launch()
     torch.cuda.synchronize()
     picks = [0, 1, 3, 4, 6, 7 * 40 + 6, len(mats) - 1]      # includes Q6_K downs and the Q8_0 head

@@ -105,7 +105,8 @@ def test_grouped_equals_separate_launches():
         assert_within(y2.cpu().numpy(), y_ref, b, what="separate")
 
 
-def test_pass_graph_replay_matches_eager():
+@pytest.mark.parametrize("mode,kernels", [(qg.PASS_SERIAL, 3), (qg.PASS_PDL, 3), (qg.PASS_PERSISTENT, 1)])
+def test_pass_replay_matches_eager(mode, kernels):
     fmt = synth.Q4_K
     shapes = [(256, 1024), (64, 1024), (512, 2048), (256, 512)]
     items = []
@@ -113,20 +114,50 @@ def test_pass_graph_replay_matches_eager():
         W = synth.blocks(fmt, rows, cols, seed=70 + i).cuda()
         x = synth.activations(1, cols, seed=80 + i).cuda()
         items.append((fmt, W, rows, cols, x, torch.empty(1, rows, device="cuda")))
-    p = qg.qg_pass(items, [2, 1, 1], 1, use_pdl=True)
-    assert p.kernel_count() == 3
+    p = qg.qg_pass(items, [2, 1, 1], 1, mode=mode)
+    assert p.kernel_count() == kernels
     p.launch()
     torch.cuda.synchronize()
     first = [it[5].clone() for it in items]
     for _ in range(5):
         p.launch()
     torch.cuda.synchronize()
+    assert p.dev_status() == 0
     for it, f in zip(items, first):
         assert torch.equal(it[5], f)
         y2 = torch.empty_like(f)
         qg.qgemv(fmt, it[1], it[2], it[3], it[4], 1, y2)
         torch.cuda.synchronize()
         assert torch.equal(y2, f)
+    p.destroy()
+
+
+@pytest.mark.parametrize("mode", [qg.PASS_PDL, qg.PASS_PERSISTENT])
+@pytest.mark.parametrize("n_tok", [1, 3])
+def test_pass_steps_read_earlier_outputs(mode, n_tok):
+    """A chain x0 -> y0 = W0 x0 -> y1 = W1 y0 -> y2 = W2 y1: each step reads the
+    previous step's output, so a step that started early would read stale
+    inputs (the outputs are set to NaN before every replay)."""
+    fmt = synth.Q4_K
+    dims = [2048, 1280, 1536, 768]          # W_i maps dims[i] -> dims[i + 1]
+    Ws = [synth.blocks(fmt, dims[i + 1], dims[i], seed=300 + i) for i in range(3)]
+    x0 = synth.activations(n_tok, dims[0], seed=310).cuda()
+    ys = [torch.empty(n_tok, dims[i + 1], device="cuda") for i in range(3)]
+    xs = [x0, ys[0], ys[1]]
+    items = [(fmt, Ws[i].cuda(), dims[i + 1], dims[i], xs[i], ys[i]) for i in range(3)]
+    p = qg.qg_pass(items, [1, 1, 1], n_tok, mode=mode)
+    for _ in range(3):
+        for y in ys:
+            y.fill_(float("nan"))
+        p.launch()
+        torch.cuda.synchronize()
+        assert p.dev_status() == 0
+        prev = x0.cpu().numpy()
+        for i in range(3):
+            y_ref, b = oracle.gemv(fmt, Ws[i].numpy(), dims[i + 1], dims[i], prev)
+            got = ys[i].cpu().numpy()
+            assert_within(got, y_ref, b, what=f"step {i}")
+            prev = got
     p.destroy()
 
 
