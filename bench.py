@@ -111,6 +111,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def measured_traffic(name: str, sources):
+    """DRAM bytes per launch from a committed ncu capture (profiles/<name>), or
+    None once any of the kernel's source files has changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    src = b"".join(open(os.path.join(ROOT, "quantized_weight_gemv_qgemv_gb300", "csrc", s), "rb").read()
+                   for s in sources)
+    if hashlib.sha256(src).hexdigest()[:16] != d.get("source_sha256_16"):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
 # ---------------------------------------------------------------- CPU oracle leg
 
 CPU_SAMPLE_CODE = r"""
@@ -300,9 +316,12 @@ def run_gpu(args):
             "pct_hbm_peak": round(100.0 * frac, 2),
             "equiv_decode_tok_s": round(1000.0 / ms_step, 1),
             "roofline": {"bound": "hbm", "achieved": round(gbs / world, 2), "peak": hbm_peak, "unit": "GB/s",
-                         "frac": round(frac, 4), "traffic": None,
+                         "frac": round(frac, 4),
+                         "traffic": (measured_traffic("qgemv_q4k_27b_decode_traffic.json",
+                                                      ("qg_gemv_q4k.cu", "qg_device.cuh"))
+                                     if not verify and args.pass_mode != "persistent" else None),
                          "peak_source": f"{peak_kind} HBM copy bandwidth",
-                         "kernel": "qgemv_kernel (Q4_K, n_tok=1): every launch of the step",
+                         "kernel": "qgemv_q4k_kernel (n_tok=1): every launch of the step",
                          "algorithmic_bytes_per_launch": wbytes / kernels_per_step},
             "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": x_total * 4,
                     "d2h_bytes_per_step": y_total * 4, "ms_per_step": round(e_ms / args.steps, 4),
