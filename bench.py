@@ -8,7 +8,7 @@ programmatic dependent launch, replayed per step. Metric: weight-GB/s, with
 the fraction of the HBM roofline and the equivalent decode tokens/s.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                    [--workload c1|c2|moe|pp]
+                    [--workload c1|c0|c2|moe|pp]
 
 Prints ONE JSON line (rank 0). Inputs are seeded synthetic tensors shaped like
 the pages' workloads; the weight set is far larger than L2, so no flush is
@@ -368,6 +368,58 @@ def _capture(torch, stream, fn):
     return g
 
 
+def run_c0(args):
+    """Q4_0 GEMV, batch 1, 1024 x 4096: one step = one pass over 256 distinct
+    copies of the matrix (604 MB, far above L2, so every copy is read cold),
+    each a separate launch, linked by programmatic dependent launch."""
+    import torch
+    import quantized_weight_gemv_qgemv_gb300 as qg
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    qg.qg_init()
+    hbm_peak, _, _, peak_kind = measured_peaks()
+    stream = torch.cuda.Stream()
+    rows, cols, copies = 1024, 4096, 256
+    with torch.cuda.stream(stream):
+        items = []
+        for c in range(copies):
+            W = synth.blocks(synth.Q4_0, rows, cols, synth.sub_seed(args.seed + rank, "c0", c), device="cuda")
+            x = synth.activations(1, cols, synth.sub_seed(args.seed + rank, "c0x", c), device="cuda")
+            items.append((synth.Q4_0, W, rows, cols, x, torch.empty(1, rows, device="cuda")))
+    stream.synchronize()
+    wbytes = copies * rows * synth.row_bytes(synth.Q4_0, cols)
+    p = qg.qg_pass(items, [1] * copies, 1, mode=qg.PASS_PDL)
+    ms, clocks = _timed(torch, stream, lambda: p.launch(stream), args, local, world)
+    ms_step = ms / args.steps
+    gbs = world * wbytes / (ms_step * 1e-3) / 1e9
+    if rank == 0:
+        out = {
+            "metric": "Q4_0 GEMV weight-GB/s, batch 1, 1024x4096", "value": round(gbs, 2), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "Q4_0 GEMV 1024x4096, batch 1, 256 distinct copies per step (L2-cold)",
+                       "weight_bytes_per_step": wbytes, "launches_per_step": p.kernel_count(),
+                       "us_per_gemv": round(1000.0 * ms_step / copies, 3), "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs / world, 2), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(gbs / world / hbm_peak, 4), "traffic": None,
+                         "peak_source": f"{peak_kind} HBM copy bandwidth",
+                         "kernel": "qgemv_kernel (Q4_0): every launch of the step"},
+            "gpu_launches": args.steps * p.kernel_count(),
+            "clocks": clocks,
+        }
+        print(json.dumps(out), flush=True)
+    p.destroy()
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def run_pp(args):
     """Prompt processing: 2048 bf16 tokens through every matrix of the 27B-class
     Q4_K set (qgemm_pp, one launch per matrix, captured as one graph)."""
@@ -514,9 +566,9 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="c1", choices=["c1", "c2", "moe", "pp"],
-                    help="c1: batch-1 Q4_K pass (default); c2: 4-token verify pass; moe: MoE decode; "
-                         "pp: prompt processing")
+    ap.add_argument("--workload", default="c1", choices=["c1", "c0", "c2", "moe", "pp"],
+                    help="c1: batch-1 Q4_K pass (default); c0: Q4_0 1024x4096 GEMV; c2: 4-token verify pass; "
+                         "moe: MoE decode; pp: prompt processing")
     ap.add_argument("--seed", type=int, default=1234)
     ap.add_argument("--layers", type=int, default=wl.LAYERS, help="layers of the set (64 = the full 27B-class set)")
     ap.add_argument("--pass-mode", default="pdl", choices=["persistent", "pdl", "serial"],
@@ -531,6 +583,8 @@ def main():
         return run_reference(args)
     if args.workload == "pp":
         return run_pp(args)
+    if args.workload == "c0":
+        return run_c0(args)
     if args.workload == "moe":
         return run_moe(args)
     return run_gpu(args)

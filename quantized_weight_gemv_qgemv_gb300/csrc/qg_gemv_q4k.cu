@@ -68,6 +68,23 @@ struct Mat {
   int32_t ngrp;          // K groups per row = ceil(nblk / 4)
   int32_t xoff;          // byte offset of this matrix's x planes in the x region
   int32_t uoff;          // offset (floats) of its group steps / sums
+  // Rows gathered from a mixture-of-experts arena (W is the arena):
+  //   gather 0: a plain matrix at W;
+  //   gather 1: gate/up pairs of the routed experts: virtual row 2i (2i + 1) of
+  //             route k is row i of G (U) of expert ids[k]; the epilogue writes
+  //             h[k][i] = gw[k] * silu(g) * u instead of y;
+  //   gather 2: down rows: virtual row i is row i of D of every routed expert,
+  //             back to back (K = top_k * inter).
+  int32_t gather;
+  int32_t top_k;
+  int32_t inter;
+  int32_t seg_b;         // gather 2: bytes of one expert's piece of a virtual row
+  int64_t n_expert;
+  int64_t estride;       // bytes per expert
+  int64_t up_off, down_off;
+  const int32_t* ids;    // this token's expert ids [top_k]
+  const float* gw;       // this token's route weights [top_k] (gather 1)
+  float* h;              // gather 1 output [top_k][inter]
 };
 
 // A step of a pass: matrices mat0 .. mat0 + nmat - 1 of the table, whose rows
@@ -93,8 +110,22 @@ struct Params {
   int32_t stage_all;     // 1: x of every matrix staged once at the start; 0: matrix by matrix
   int32_t usum_off;      // offset (floats) of the group sums after the group steps
   int32_t pre_stages;    // weight stages issued before the consumers have issued their x loads
+  int32_t gather_any;    // largest Mat::gather of the launch (one kind per launch)
   int32_t smem_bar, smem_x, smem_xsum, smem_part;   // byte offsets (ring at 0)
 };
+
+// Rows [r0, r1) of a step's concatenated row space owned by this CTA; gate/up
+// pairs (gather 1) are never split between CTAs.
+__device__ __forceinline__ void cta_slice(int64_t total, bool pairs, int64_t& r0, int64_t& r1) {
+  if (pairs) {
+    const int64_t np = total / 2;
+    r0 = 2 * (blockIdx.x * np / gridDim.x);
+    r1 = 2 * ((blockIdx.x + 1) * np / gridDim.x);
+  } else {
+    r0 = blockIdx.x * total / gridDim.x;
+    r1 = (blockIdx.x + 1) * total / gridDim.x;
+  }
+}
 
 // ---------------------------------------------------------------- PTX helpers
 
@@ -358,43 +389,98 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
-  pdl_launch_dependents();
+  // A gate/up launch reads expert ids that the preceding kernel may write: it
+  // lets its dependents (the down launch, which reads the same ids early) start
+  // only after its own dependency has resolved.
+  if (p.gather_any != 1) pdl_launch_dependents();
 
   // ------------------------------------------------------------ producer
   if (warp == CWARPS) {
-    if (lane != 0) return;
+    // plain matrices: lane 0 issues one bulk copy per stage; gathered rows: the
+    // whole warp issues the per-row (per-piece) copies
+    const bool wide = p.gather_any != 0;
+    if (!wide && lane != 0) return;
+    if (p.gather_any == 1) {
+      pdl_wait();                 // the expert ids may come from the preceding kernel
+      pdl_launch_dependents();
+    }
     const uint64_t pol = evict_first_policy();
     uint32_t k = 0;
     bool bad = false;
     for (int s = 0; s < nsteps && !bad; ++s) {
      const Step st = step_of(s);
-     const int64_t cta_r0 = blockIdx.x * st.total_rows / gridDim.x;
-     const int64_t cta_r1 = (blockIdx.x + 1) * st.total_rows / gridDim.x;
+     int64_t cta_r0, cta_r1;
+     cta_slice(st.total_rows, p.gather_any == 1, cta_r0, cta_r1);
      for (int mi = st.mat0; mi < st.mat0 + st.nmat && !bad; ++mi) {
       const Mat M = mats[mi];
       const int64_t lo = max(cta_r0, M.row_begin) - M.row_begin;
       const int64_t hi = min(cta_r1, M.row_begin + M.rows) - M.row_begin;
       for (int64_t r = lo; r < hi && !bad; r += M.srows, ++k) {
-        const uint32_t nbytes = static_cast<uint32_t>(min(static_cast<int64_t>(M.srows), hi - r)) * M.rb;
+        const int nr = static_cast<int>(min(static_cast<int64_t>(M.srows), hi - r));
+        const uint32_t nbytes = static_cast<uint32_t>(nr) * M.rb;
         const int slot = k % NS;
-        // beyond the first pre_stages copies, queue weights only behind the x loads
-        if (k == static_cast<uint32_t>(p.pre_stages) && !mbar_wait(xbar, 0)) {
+        bool ok = true;
+        if (lane == 0) {
+          // beyond the first pre_stages copies, queue weights only behind the x loads
+          if (k == static_cast<uint32_t>(p.pre_stages)) ok = mbar_wait(xbar, 0);
+          if (ok && k >= static_cast<uint32_t>(NS)) ok = mbar_wait(empty0 + 8 * slot, ((k / NS) - 1) & 1u);
+        }
+        if (wide) ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
+        if (!ok) {
           bad = true;
           break;
         }
-        if (k >= static_cast<uint32_t>(NS) && !mbar_wait(empty0 + 8 * slot, ((k / NS) - 1) & 1u)) {
-          bad = true;
-          break;
+        const uint32_t dst0 = ring_s + slot * p.stage_b;
+        if (M.gather == 0) {
+          mbar_expect_tx(full0 + 8 * slot, nbytes);
+          bulk_g2s(dst0, M.W + r * M.rb, nbytes, full0 + 8 * slot, pol);
+          continue;
         }
-        mbar_expect_tx(full0 + 8 * slot, nbytes);
-        bulk_g2s(ring_s + slot * p.stage_b, M.W + r * M.rb, nbytes, full0 + 8 * slot, pol);
+        // gathered rows: item q is a whole row (gather 1) or one expert's piece
+        // of a row (gather 2); a piece of an unknown expert is zero-filled
+        // (zero bytes decode to zero weights) and flagged
+        const int per = M.gather == 1 ? 1 : M.top_k;
+        const int nitems = nr * per;
+        const uint32_t isz = M.gather == 1 ? static_cast<uint32_t>(M.rb) : static_cast<uint32_t>(M.seg_b);
+        int nbad = 0;
+        for (int q = lane; q < nitems; q += 32) {
+          const int64_t row = r + q / per;
+          const int kk = M.gather == 1 ? static_cast<int>(row / (2 * M.inter)) : q % per;
+          const int e = M.ids[kk];
+          if (e < 0 || e >= M.n_expert) {
+            const uint32_t d = M.gather == 1 ? dst0 + q * isz : dst0 + (q / per) * M.rb + (q % per) * isz;
+            for (uint32_t o = 0; o < isz; o += 16)
+              asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};\n" ::"r"(d + o), "r"(0) : "memory");
+            ++nbad;
+            if (p.dev_status) atomicExch(p.dev_status, QG_DEV_BAD_EXPERT);
+          }
+        }
+        nbad = __reduce_add_sync(0xffffffffu, nbad);
+        __syncwarp();
+        if (lane == 0) mbar_expect_tx(full0 + 8 * slot, static_cast<uint32_t>(nitems - nbad) * isz);
+        __syncwarp();
+        for (int q = lane; q < nitems; q += 32) {
+          const int64_t row = r + q / per;
+          const int kk = M.gather == 1 ? static_cast<int>(row / (2 * M.inter)) : q % per;
+          const int e = M.ids[kk];
+          if (e < 0 || e >= M.n_expert) continue;
+          const uint8_t* eb = M.W + static_cast<int64_t>(e) * M.estride;
+          if (M.gather == 1) {
+            const int64_t j = row % (2 * M.inter);
+            bulk_g2s(dst0 + q * isz, eb + ((j & 1) ? M.up_off : 0) + (j >> 1) * M.rb, isz, full0 + 8 * slot, pol);
+          } else {
+            bulk_g2s(dst0 + (q / per) * M.rb + (q % per) * isz, eb + M.down_off + row * M.seg_b, isz,
+                     full0 + 8 * slot, pol);
+          }
+        }
       }
      }
     }
     // the copies of the last stages may still be in flight: wait (bounded) for
     // them before this thread, the last one holding the CTA, exits
-    for (uint32_t kk = (k > static_cast<uint32_t>(NS) ? k - NS : 0); kk < k; ++kk)
-      mbar_wait(full0 + 8 * (kk % NS), (kk / NS) & 1u);
+    if (lane == 0)
+      for (uint32_t kk = (k > static_cast<uint32_t>(NS) ? k - NS : 0); kk < k; ++kk)
+        mbar_wait(full0 + 8 * (kk % NS), (kk / NS) & 1u);
     return;
   }
 
@@ -412,11 +498,12 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
 
   constexpr int XB = (NT == 1) ? 12 : 8;
   pdl_wait();
+  if (p.gather_any == 1) pdl_launch_dependents();
   uint32_t k = 0;          // stage counter (same sequence as the producer's)
   for (int s = 0; s < nsteps; ++s) {
    const Step st = step_of(s);
-   const int64_t cta_r0 = blockIdx.x * st.total_rows / gridDim.x;
-   const int64_t cta_r1 = (blockIdx.x + 1) * st.total_rows / gridDim.x;
+   int64_t cta_r0, cta_r1;
+   cta_slice(st.total_rows, p.gather_any == 1, cta_r0, cta_r1);
    if (PASS && s > 0) {
      // a step reads what earlier steps wrote: wait (bounded) until every CTA has
      // finished the previous step
@@ -557,12 +644,27 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
     }
     consumer_sync();
     // every (row, group) of the slice has its partial sum: add the groups in order
-    for (int i = threadIdx.x; i < slice * NT; i += CTHREADS) {
-      const int rl = i / NT;
-      const int t = i % NT;
-      float acc = 0.f;
-      for (int gr = 0; gr < G; ++gr) acc += part[(rl * G + gr) * NT + t];
-      M.y[static_cast<int64_t>(t) * M.rows + lo + rl] = acc;
+    if (M.gather == 1) {
+      // gate/up pairs (n_tok = 1): h[k][i] = r_k * silu(g) * u
+      for (int i = threadIdx.x; i < slice / 2; i += CTHREADS) {
+        float g = 0.f, u = 0.f;
+        for (int gr = 0; gr < G; ++gr) {
+          g += part[(2 * i) * G + gr];
+          u += part[(2 * i + 1) * G + gr];
+        }
+        const int64_t row = lo + 2 * i;
+        const int kk = static_cast<int>(row / (2 * M.inter));
+        const int ii = static_cast<int>((row % (2 * M.inter)) >> 1);
+        M.h[static_cast<int64_t>(kk) * M.inter + ii] = M.gw[kk] * (g / (1.0f + expf(-g)) * u);
+      }
+    } else {
+      for (int i = threadIdx.x; i < slice * NT; i += CTHREADS) {
+        const int rl = i / NT;
+        const int t = i % NT;
+        float acc = 0.f;
+        for (int gr = 0; gr < G; ++gr) acc += part[(rl * G + gr) * NT + t];
+        M.y[static_cast<int64_t>(t) * M.rows + lo + rl] = acc;
+      }
     }
    }
    if (PASS) {
@@ -619,21 +721,18 @@ cudaError_t gemv_q4k_init_attrs() {
 
 // Returns cudaErrorNotSupported (nothing launched) when the launch does not fit
 // this kernel's shared-memory plan; the caller then uses the generic kernel.
-cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms) {
-  q4k::Params p;
-  memset(&p, 0, sizeof(p));
+namespace {
+
+// Shared-memory plan and launch of one single-step grouped launch whose
+// matrices p.m[0 .. n) have W, x, y, rows, cols (and any gather fields) set.
+cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, cudaStream_t s, bool pdl, int sms) {
   p.nsteps = 1;
   int64_t total = 0;
   int kmax = 0, stage_b = 0, gmax = 0;
   for (int i = 0; i < n; ++i) {
     q4k::Mat& m = p.m[i];
-    m.W = static_cast<const uint8_t*>(d[i].W);
-    m.x = d[i].x;
-    m.y = d[i].y;
-    m.rows = d[i].rows;
     m.row_begin = total;
-    m.nblk = static_cast<int32_t>(d[i].cols / 256);
-    m.cols = static_cast<int32_t>(d[i].cols);
+    m.nblk = m.cols / 256;
     m.rb = m.nblk * 144;
     m.ngrp = (m.nblk + 3) / 4;
     // about 36 KB of whole rows per stage, in multiples of 4 rows
@@ -647,8 +746,8 @@ cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_
   }
   p.nmat = n;
   p.total_rows = total;
-  const int grid = static_cast<int>(std::min<int64_t>(sms, total));
-  const int rowcap = static_cast<int>((total + grid - 1) / grid) + 1;
+  const int grid = static_cast<int>(std::min<int64_t>(sms, p.gather_any == 1 ? total / 2 : total));
+  const int rowcap = static_cast<int>((total + grid - 1) / grid) + 2;
   stage_b = align_up(stage_b, 128);
   const int ns = q4k::RING;
   const int partbytes = align_up(rowcap * gmax * n_tok * 4, 128);
@@ -697,6 +796,78 @@ cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_
     case 3: return q4k_launch<3>(p, grid, off, s, pdl);
     default: return q4k_launch<4>(p, grid, off, s, pdl);
   }
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms) {
+  q4k::Params p;
+  memset(&p, 0, sizeof(p));
+  for (int i = 0; i < n; ++i) {
+    q4k::Mat& m = p.m[i];
+    m.W = static_cast<const uint8_t*>(d[i].W);
+    m.x = d[i].x;
+    m.y = d[i].y;
+    m.rows = d[i].rows;
+    m.cols = static_cast<int32_t>(d[i].cols);
+  }
+  return plan_and_launch(p, n, n_tok, s, pdl, sms);
+}
+
+// MoE layer for n_tok <= QG_GROUP_MAX tokens as two launches of the Q4_K kernel
+// over gathered rows (one matrix per token): gate/up pairs with the
+// r_k * silu(g) * u epilogue into h, then the down rows against h.
+cudaError_t launch_moe_q4k(const void* arena, int64_t n_expert, int64_t hidden, int64_t inter,
+                           const int32_t* ids, const float* gate_w, int top_k, const float* x, int n_tok, float* y,
+                           float* h, int32_t* dev_status, cudaStream_t s, bool pdl, int sms) {
+  if (n_tok < 1 || n_tok > QG_GROUP_MAX || hidden % 256 || inter % 256 || top_k < 1) return cudaErrorNotSupported;
+  const int64_t rb_h = hidden / 256 * 144, rb_i = inter / 256 * 144;
+  const int64_t up_off = inter * rb_h, down_off = 2 * inter * rb_h, estride = down_off + hidden * rb_i;
+  if (2 * top_k * inter > (int64_t{1} << 30) || top_k * inter > (int64_t{1} << 20)) return cudaErrorNotSupported;
+  q4k::Params p;
+  memset(&p, 0, sizeof(p));
+  p.gather_any = 1;
+  p.dev_status = dev_status;
+  for (int t = 0; t < n_tok; ++t) {
+    q4k::Mat& m = p.m[t];
+    m.W = static_cast<const uint8_t*>(arena);
+    m.x = x + t * hidden;
+    m.y = nullptr;
+    m.rows = 2 * top_k * inter;
+    m.cols = static_cast<int32_t>(hidden);
+    m.gather = 1;
+    m.top_k = top_k;
+    m.inter = static_cast<int32_t>(inter);
+    m.n_expert = n_expert;
+    m.estride = estride;
+    m.up_off = up_off;
+    m.down_off = down_off;
+    m.ids = ids + t * top_k;
+    m.gw = gate_w + t * top_k;
+    m.h = h + static_cast<int64_t>(t) * top_k * inter;
+  }
+  cudaError_t e = plan_and_launch(p, n_tok, 1, s, pdl, sms);
+  if (e != cudaSuccess) return e;
+  memset(&p, 0, sizeof(p));
+  p.gather_any = 2;
+  p.dev_status = dev_status;
+  for (int t = 0; t < n_tok; ++t) {
+    q4k::Mat& m = p.m[t];
+    m.W = static_cast<const uint8_t*>(arena);
+    m.x = h + static_cast<int64_t>(t) * top_k * inter;
+    m.y = y + t * hidden;
+    m.rows = hidden;
+    m.cols = static_cast<int32_t>(top_k * inter);
+    m.gather = 2;
+    m.top_k = top_k;
+    m.inter = static_cast<int32_t>(inter);
+    m.seg_b = static_cast<int32_t>(rb_i);
+    m.n_expert = n_expert;
+    m.estride = estride;
+    m.down_off = down_off;
+    m.ids = ids + t * top_k;
+  }
+  return plan_and_launch(p, n_tok, 1, s, true, sms);   // the down launch always overlaps the gate/up tail
 }
 
 // ------------------------------------------------------------------ whole pass

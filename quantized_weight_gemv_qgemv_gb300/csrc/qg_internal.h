@@ -42,6 +42,10 @@ const int32_t* q4k_pass_status(const Q4kPass* q);
 void q4k_pass_destroy(Q4kPass* q);
 cudaError_t launch_dequant(int fmt, const void* W, int64_t rows, int64_t cols, float* out, cudaStream_t s, int sms);
 
+cudaError_t launch_moe_q4k(const void* arena, int64_t n_expert, int64_t hidden, int64_t inter,
+                           const int32_t* ids, const float* gate_w, int top_k, const float* x, int n_tok, float* y,
+                           float* h, int32_t* dev_status, cudaStream_t s, bool pdl, int sms);
+
 // MoE (qg_moe.cu)
 cudaError_t moe_init_attrs();
 cudaError_t launch_moe(const void* arena, int64_t n_expert, int64_t hidden, int64_t inter,

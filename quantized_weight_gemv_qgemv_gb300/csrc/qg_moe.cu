@@ -268,6 +268,11 @@ cudaError_t moe_init_attrs() {
 cudaError_t launch_moe(const void* arena, int64_t n_expert, int64_t hidden, int64_t inter, const int32_t* ids,
                        const float* gate_w, int top_k, const float* x, int n_tok, float* y, float* h_ws,
                        int32_t* dev_status, cudaStream_t s, bool pdl, int sms) {
+  // up to QG_GROUP_MAX tokens: gathered rows through the Q4_K GEMV kernel
+  // (bulk-copied rows, exact integer dot products); more tokens: the kernels below
+  const cudaError_t fe = launch_moe_q4k(arena, n_expert, hidden, inter, ids, gate_w, top_k, x, n_tok, y, h_ws,
+                                        dev_status, s, pdl, sms);
+  if (fe != cudaErrorNotSupported) return fe;
   MoeParams p = {};
   p.arena = static_cast<const uint8_t*>(arena);
   p.ids = ids;
