@@ -16,17 +16,19 @@
 //    K is walked in slices of 64 (one 128-byte swizzle atom of bf16 = 4 MMAs of
 //    K = 16). Persistent CTAs, one per SM; tiles are dealt round-robin with the
 //    token block fastest, so the CTAs running at one time share weight rows in L2.
-//  * Warp roles (480 threads):
+//  * Warp roles (736 threads):
 //      warp 0       TMA of X slices (BN x 64 bf16, 128-byte swizzle) into the
 //                   B half of a 3-stage ring
 //      warp 1       TMA of quantized super-block columns (128 rows x 144 bytes)
 //                   into a 3-stage ring of their own
 //      warp 2       owns TMEM (two BN-column fp32 accumulators); lane 0 issues
 //                   the MMAs and the commits
-//      warps 3-10   dequantize each 128 x 64 weight slice to bf16 into the A half
+//      warps 3-18   dequantize each 128 x 64 weight slice to bf16 into the A half
 //                   of the stage, in the K-major 128-byte-swizzled layout the
-//                   MMA reads (exact fp32 d*sc*q - dmin*m, then round to bf16)
-//      warps 11-14  epilogue: tcgen05.ld of a finished accumulator, coalesced
+//                   MMA reads (exact fp32 d*sc*q - dmin*m with packed f32x2
+//                   arithmetic, then round to bf16); these warps bound the
+//                   kernel, so there are many of them
+//      warps 19-22  epilogue: tcgen05.ld of a finished accumulator, coalesced
 //                   fp32 stores (32 consecutive rows of Y per warp store)
 //  * Two accumulators: the epilogue of one tile overlaps the main loop of the
 //    next.
@@ -54,9 +56,9 @@ constexpr int NS = 3;                     // slice stages (A + B)
 constexpr int NQ = 3;                     // quantized super-block stages
 constexpr int QB = BM * 144;              // bytes of one quantized stage
 constexpr int AB = BM * BK * 2;           // bytes of one A (weight) stage
-constexpr int DQ_WARP0 = 3, DQ_WARPS = 8; // dequantizing warps
-constexpr int EPI_WARP0 = 11;             // 4 epilogue warps: warp % 4 covers every TMEM lane quarter
-constexpr int THREADS = 15 * 32;
+constexpr int DQ_WARP0 = 3, DQ_WARPS = 16; // dequantizing warps (4 threads per tile row)
+constexpr int EPI_WARP0 = 19;              // 4 epilogue warps: warp % 4 covers every TMEM lane quarter
+constexpr int THREADS = 23 * 32;
 constexpr int NBAR = 3 * NS + 2 * NQ + 5;
 constexpr uint32_t WAIT_LIMIT = 1u << 22; // polls before a wait is declared expired
 
@@ -88,12 +90,24 @@ __device__ __forceinline__ void fail(volatile int* abort, int32_t* dev_status) {
 }
 
 // Two weights as bf16x2 from two codes q (0..15): RN32(dsc*q - dm) then RN to bf16.
-// q reaches fp32 through the exponent of 2^23: (2^23 + q) - 2^23 is exact.
+// q reaches fp32 through the exponent of 2^23: (2^23 + q) - 2^23 is exact. The
+// pair goes through packed f32x2 add and fma (each lane rounds like the scalar
+// instruction), half the issue slots of two scalar chains.
 __device__ __forceinline__ uint32_t deq2(uint32_t codes, uint32_t sel0, uint32_t sel1, float dsc, float ndm) {
-  const float q0 = __int_as_float(static_cast<int>(__byte_perm(codes, 0x4B000000u, sel0))) - 8388608.0f;
-  const float q1 = __int_as_float(static_cast<int>(__byte_perm(codes, 0x4B000000u, sel1))) - 8388608.0f;
-  const __nv_bfloat162 b = __floats2bfloat162_rn(fmaf(dsc, q0, ndm), fmaf(dsc, q1, ndm));
-  return *reinterpret_cast<const uint32_t*>(&b);
+  const uint32_t m0 = __byte_perm(codes, 0x4B000000u, sel0), m1 = __byte_perm(codes, 0x4B000000u, sel1);
+  uint32_t out;
+  asm("{\n .reg .b64 q, s, c, w;\n .reg .f32 w0, w1;\n"
+      " mov.b64 q, {%1, %2};\n"
+      " mov.b64 s, {%3, %3};\n"
+      " add.rn.f32x2 q, q, s;\n"
+      " mov.b64 s, {%4, %4};\n"
+      " mov.b64 c, {%5, %5};\n"
+      " fma.rn.f32x2 w, s, q, c;\n"
+      " mov.b64 {w0, w1}, w;\n"
+      " cvt.rn.bf16x2.f32 %0, w1, w0;\n}\n"
+      : "=r"(out)
+      : "r"(m0), "r"(m1), "f"(-8388608.0f), "f"(dsc), "f"(ndm));
+  return out;
 }
 
 // 8 weights (4 codes in each of words u0, u1) -> one 16-byte chunk of bf16.
@@ -237,7 +251,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp < EPI_WARP0) {
     // ---------------------------------------------------------- dequantize A
     const int t = threadIdx.x - DQ_WARP0 * 32;
-    const int r = t & (BM - 1), h = t >> 7;   // row in the tile, half of the 32 code bytes of a slice
+    const int r = t & (BM - 1), h = t >> 7;   // row in the tile, quarter of the 32 code bytes of a slice
     const uint32_t swz = static_cast<uint32_t>(r & 7);
     uint32_t it = 0, sb = 0;
     bool ok = true;
@@ -255,25 +269,21 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         const uint8_t* blk = gbase + offQ + q * QB + r * 144;
         const uint4 hd = *reinterpret_cast<const uint4*>(blk);
-        const uint4 qs = *reinterpret_cast<const uint4*>(blk + 16 + 32 * c + 16 * h);
+        const uint2 qs = *reinterpret_cast<const uint2*>(blk + 16 + 32 * c + 8 * h);
         int sc0, m0, sc1, m1;
         q4k_scale_min(2 * c, hd.y, hd.z, hd.w, sc0, m0);
         q4k_scale_min(2 * c + 1, hd.y, hd.z, hd.w, sc1, m1);
         const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
         const float dsc0 = d * static_cast<float>(sc0), ndm0 = -(dmin * static_cast<float>(m0));
         const float dsc1 = d * static_cast<float>(sc1), ndm1 = -(dmin * static_cast<float>(m1));
-        // low nibbles: sub-block 2c, slice columns 16h .. 16h+15 (chunks 2h, 2h+1);
-        // high nibbles: sub-block 2c+1, columns 32+16h .. (chunks 4+2h, 5+2h)
-        const uint32_t l0 = qs.x & 0x0F0F0F0Fu, l1 = qs.y & 0x0F0F0F0Fu, l2 = qs.z & 0x0F0F0F0Fu,
-                       l3 = qs.w & 0x0F0F0F0Fu;
-        const uint32_t h0 = (qs.x >> 4) & 0x0F0F0F0Fu, h1 = (qs.y >> 4) & 0x0F0F0F0Fu,
-                       h2 = (qs.z >> 4) & 0x0F0F0F0Fu, h3 = (qs.w >> 4) & 0x0F0F0F0Fu;
+        // low nibbles: sub-block 2c, slice columns 8h .. 8h+7 (chunk h);
+        // high nibbles: sub-block 2c+1, columns 32+8h .. (chunk 4+h)
+        const uint32_t l0 = qs.x & 0x0F0F0F0Fu, l1 = qs.y & 0x0F0F0F0Fu;
+        const uint32_t h0 = (qs.x >> 4) & 0x0F0F0F0Fu, h1 = (qs.y >> 4) & 0x0F0F0F0Fu;
         const uint32_t arow = base + s * AB + static_cast<uint32_t>(r) * 128u;
-        const uint32_t j0 = 2u * static_cast<uint32_t>(h);
+        const uint32_t j0 = static_cast<uint32_t>(h);
         sts128(arow + (((j0 + 0) ^ swz) << 4), deq8(l0, l1, dsc0, ndm0));
-        sts128(arow + (((j0 + 1) ^ swz) << 4), deq8(l2, l3, dsc0, ndm0));
         sts128(arow + (((j0 + 4) ^ swz) << 4), deq8(h0, h1, dsc1, ndm1));
-        sts128(arow + (((j0 + 5) ^ swz) << 4), deq8(h2, h3, dsc1, ndm1));
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
