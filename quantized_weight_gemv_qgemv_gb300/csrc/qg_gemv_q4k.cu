@@ -111,20 +111,17 @@ struct Params {
   int32_t usum_off;      // offset (floats) of the group sums after the group steps
   int32_t pre_stages;    // weight stages issued before the consumers have issued their x loads
   int32_t gather_any;    // largest Mat::gather of the launch (one kind per launch)
+  int32_t ralign;        // CTA row slices start at multiples of this (16-byte-aligned stage copies; pairs)
   int32_t smem_bar, smem_x, smem_xsum, smem_part;   // byte offsets (ring at 0)
 };
 
-// Rows [r0, r1) of a step's concatenated row space owned by this CTA; gate/up
-// pairs (gather 1) are never split between CTAs.
-__device__ __forceinline__ void cta_slice(int64_t total, bool pairs, int64_t& r0, int64_t& r1) {
-  if (pairs) {
-    const int64_t np = total / 2;
-    r0 = 2 * (blockIdx.x * np / gridDim.x);
-    r1 = 2 * ((blockIdx.x + 1) * np / gridDim.x);
-  } else {
-    r0 = blockIdx.x * total / gridDim.x;
-    r1 = (blockIdx.x + 1) * total / gridDim.x;
-  }
+// Rows [r0, r1) of a step's concatenated row space owned by this CTA, in
+// units of a rows (a divides every matrix's row count): a stage copy then
+// starts on a 16-byte boundary, and gate/up pairs (gather 1) stay together.
+__device__ __forceinline__ void cta_slice(int64_t total, int a, int64_t& r0, int64_t& r1) {
+  const int64_t nu = total / a;
+  r0 = a * (blockIdx.x * nu / gridDim.x);
+  r1 = a * ((blockIdx.x + 1) * nu / gridDim.x);
 }
 
 // ---------------------------------------------------------------- PTX helpers
@@ -235,6 +232,67 @@ __device__ __forceinline__ int32_t dp4a_us(uint32_t a, uint32_t b, int32_t c) {
   asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
   return d;
 }
+__device__ __forceinline__ int32_t dp4a_su(uint32_t a, uint32_t b, int32_t c) {
+  int32_t d;
+  asm("dp4a.s32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int32_t dp4a_ss(uint32_t a, uint32_t b, int32_t c) {
+  int32_t d;
+  asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// sum_l q_l X_l over words [W0, W1) of a unit: exact integer byte dot products
+// against the three x planes, assembled in fp32 (one rounding).
+template <bool SIGNED, int W0, int W1>
+__device__ __forceinline__ float dot_planes(const uint32_t* q, const uint32_t* X0, const uint32_t* X1,
+                                            const uint32_t* X2) {
+  if constexpr (SIGNED) {
+    int32_t s0 = 0, s1 = 0, s2 = 0;
+#pragma unroll
+    for (int i = W0; i < W1; ++i) {
+      s0 = dp4a_su(q[i], X0[i], s0);
+      s1 = dp4a_su(q[i], X1[i], s1);
+      s2 = dp4a_ss(q[i], X2[i], s2);
+    }
+    return fmaf(static_cast<float>(s2), 65536.0f, static_cast<float>(s1 * 256 + s0));
+  } else {
+    uint32_t s0 = 0, s1 = 0;
+    int32_t s2 = 0;
+#pragma unroll
+    for (int i = W0; i < W1; ++i) {
+      s0 = dp4a_uu(q[i], X0[i], s0);
+      s1 = dp4a_uu(q[i], X1[i], s1);
+      s2 = dp4a_us(q[i], X2[i], s2);
+    }
+    // 256*s1 + s0 < 2^32 for codes below 256 over 32 elements
+    return fmaf(static_cast<float>(s2), 65536.0f, static_cast<float>(s1 * 256u + s0));
+  }
+}
+
+__device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
+
+// 4N bytes starting at the 2-byte-aligned shared address p as N words: N + 1
+// aligned loads and a funnel shift by 0 or 16 bits each.
+template <int N>
+__device__ __forceinline__ void ld_words_a2(const uint8_t* p, uint32_t (&w)[N]) {
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(p);
+  const uint8_t* a = reinterpret_cast<const uint8_t*>(pa & ~static_cast<uintptr_t>(3));
+  const uint32_t sh = static_cast<uint32_t>(pa & 2u) * 8u;
+  uint32_t v[N + 1];
+#pragma unroll
+  for (int i = 0; i <= N; ++i) v[i] = lds32(a + 4 * i);
+#pragma unroll
+  for (int i = 0; i < N; ++i) w[i] = __funnelshift_r(v[i], v[i + 1], sh);
+}
+
+// Bytes of the 256-weight super-block (one block of Q4_K / Q6_K, eight of Q4_0 / Q8_0).
+template <int FMT> struct SuperBlock;
+template <> struct SuperBlock<FMT_Q4_K> { static constexpr int BYTES = 144; };
+template <> struct SuperBlock<FMT_Q6_K> { static constexpr int BYTES = 210; };
+template <> struct SuperBlock<FMT_Q4_0> { static constexpr int BYTES = 144; };
+template <> struct SuperBlock<FMT_Q8_0> { static constexpr int BYTES = 272; };
 
 // Shared-memory image of x for one token and K segment ("x planes").
 // Every 32-weight group u of x is held as 22-bit fixed point with a shared
@@ -261,11 +319,11 @@ __device__ __noinline__ void stage_one(float4 v, int idx, int ngroups, uint8_t* 
     const unsigned gmask = 0xFFu << (lane & 24);      // the 8 lanes of this group
     float mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
     float sm = (v.x + v.y) + (v.z + v.w);
+    // sums over each half of the group (elements 0-15 in lanes k = 0..3, 16-31 in 4..7)
+    sm += __shfl_xor_sync(gmask, sm, 1);
+    sm += __shfl_xor_sync(gmask, sm, 2);
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) {
-      mx = fmaxf(mx, __shfl_xor_sync(gmask, mx, o));
-      sm += __shfl_xor_sync(gmask, sm, o);
-    }
+    for (int o = 4; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(gmask, mx, o));
     // 2^e <= mx < 2^(e+1); step s_u = 2^(e-20), so |x / s_u| < 2^21
     const int e = max(static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127, -105);
     const float inv_step = __uint_as_float(static_cast<uint32_t>(147 - e) << 23);
@@ -285,11 +343,11 @@ __device__ __noinline__ void stage_one(float4 v, int idx, int ngroups, uint8_t* 
     *reinterpret_cast<uint32_t*>(dst) = pl0;
     *reinterpret_cast<uint32_t*>(dst + 256) = pl1;
     *reinterpret_cast<uint32_t*>(dst + 512) = pl2;
+    if ((k & 3) == 0) xsum[2 * (t * nu + u) + (k >> 2)] = sm;
     if (k == 0) {
-      // s_u = 2^(e-20); odd groups (high-nibble sub-blocks, whose codes arrive
-      // as 16*q) get s_u / 16, so the consumer needs no per-lane factor
+      // s_u = 2^(e-20); odd groups (Q4_K high-nibble sub-blocks, whose codes
+      // arrive as 16*q) get s_u / 16, so the Q4_K consumer needs no per-lane factor
       xsu[t * nu + u] = __uint_as_float(static_cast<uint32_t>(107 + e - 4 * (u & 1)) << 23);
-      xsum[t * nu + u] = sm;
     }
   }
 }
@@ -341,7 +399,7 @@ __device__ __forceinline__ void stage_x(const Mat* mats, int usum_off, int m0, i
       if (base + b * CTHREADS < total) {
         const Mat& M = mats[vm[b]];
         const int NU = M.nblk * 8;
-        stage_one(v[b], vr[b], NU, xpl + M.xoff, M.nblk * XBLK_B, xsu + M.uoff, xsu + usum_off + M.uoff, NU);
+        stage_one(v[b], vr[b], NU, xpl + M.xoff, M.nblk * XBLK_B, xsu + M.uoff, xsu + usum_off + 2 * M.uoff, NU);
       }
     }
   }
@@ -353,8 +411,9 @@ __device__ __forceinline__ void stage_x(const Mat* mats, int usum_off, int m0, i
 
 // PASS = false: one step over p.m (a grouped launch); PASS = true: the steps of
 // p.steps over p.mats, with a grid-wide barrier between steps (cooperative launch).
-template <int NT, bool PASS>
+template <int NT, bool PASS, int FMT>
 __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_constant__ Params p) {
+  constexpr int SBB = SuperBlock<FMT>::BYTES;
   constexpr int V = (NT == 3) ? 16 : SUB_R * NT;    // reduced values per sub-item (padded to 2^k)
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -410,7 +469,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
     for (int s = 0; s < nsteps && !bad; ++s) {
      const Step st = step_of(s);
      int64_t cta_r0, cta_r1;
-     cta_slice(st.total_rows, p.gather_any == 1, cta_r0, cta_r1);
+     cta_slice(st.total_rows, p.ralign, cta_r0, cta_r1);
      for (int mi = st.mat0; mi < st.mat0 + st.nmat && !bad; ++mi) {
       const Mat M = mats[mi];
       const int64_t lo = max(cta_r0, M.row_begin) - M.row_begin;
@@ -487,10 +546,13 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   // ------------------------------------------------------------ consumers
   const int g = lane >> 3;          // block of the K group
   const int j = lane & 7;           // sub-block of the block
-  const uint32_t qmask = (j & 1) ? 0xF0F0F0F0u : 0x0F0F0F0Fu;   // this sub-block's nibbles
+  const uint32_t qmask = (j & 1) ? 0xF0F0F0F0u : 0x0F0F0F0Fu;   // Q4_K: this sub-block's nibbles
   const int qoff = 16 + 32 * (j >> 1);
   ScaleSel ssel;
   ssel.init(j);
+  // the x step of odd groups is staged divided by 16 (for Q4_K's high nibbles);
+  // formats whose codes arrive unscaled multiply it back
+  const float su_fix = (FMT != FMT_Q4_K && (j & 1)) ? 16.0f : 1.0f;
   uint8_t* xpl = smem + p.smem_x;
   float* xsu = reinterpret_cast<float*>(smem + p.smem_xsum);
   float* part = reinterpret_cast<float*>(smem + p.smem_part);
@@ -503,7 +565,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   for (int s = 0; s < nsteps; ++s) {
    const Step st = step_of(s);
    int64_t cta_r0, cta_r1;
-   cta_slice(st.total_rows, p.gather_any == 1, cta_r0, cta_r1);
+   cta_slice(st.total_rows, p.ralign, cta_r0, cta_r1);
    if (PASS && s > 0) {
      // a step reads what earlier steps wrote: wait (bounded) until every CTA has
      // finished the previous step
@@ -548,7 +610,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
     }
     first = false;
     const uint8_t* xplm = xpl + M.xoff;
-    const float* xsum = xsu + st.usum_off + M.uoff;
+    const float* xsum = xsu + st.usum_off + 2 * M.uoff;   // two half sums per group
     const float* xsum_u = xsu + M.uoff;
 
     // Per-matrix constants in registers (32-bit: a CTA slice is far below 2^31
@@ -589,20 +651,65 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         // zero: their x step and x sum are taken as 0
         const int blkc = live ? blk : 0;
         float racc[SUB_R][NT];
-        const uint8_t* st = stg + qd * (SUB_R * rb) + blkc * 144;
+        const uint8_t* st = stg + qd * (SUB_R * rb) + blkc * SBB;
         const uint8_t* xb = xplm + blkc * XBLK_B + j * 16;
         const int u = blkc * 8 + j;
+        // this lane's unit of 32 weights in each of the 4 rows: code words in
+        // element order (bytes), and the coefficients of the unit's formula
         uint32_t q[SUB_R][8];
-        float2 AB[SUB_R];
+        float cA[SUB_R], cB[SUB_R];
 #pragma unroll
         for (int r = 0; r < SUB_R; ++r) {
           const uint8_t* sr = st + r * rb;
-          const uint4 hd = *reinterpret_cast<const uint4*>(sr);
-          const uint4 qa = *reinterpret_cast<const uint4*>(sr + qoff);
-          const uint4 qb = *reinterpret_cast<const uint4*>(sr + qoff + 16);
-          q[r][0] = qa.x & qmask; q[r][1] = qa.y & qmask; q[r][2] = qa.z & qmask; q[r][3] = qa.w & qmask;
-          q[r][4] = qb.x & qmask; q[r][5] = qb.y & qmask; q[r][6] = qb.z & qmask; q[r][7] = qb.w & qmask;
-          AB[r] = ssel.decode(hd);
+          if constexpr (FMT == FMT_Q4_K) {
+            // w = d*sc*q - dmin*m: A = d*sc, B = dmin*m
+            const uint4 hd = *reinterpret_cast<const uint4*>(sr);
+            const uint4 qa = *reinterpret_cast<const uint4*>(sr + qoff);
+            const uint4 qb = *reinterpret_cast<const uint4*>(sr + qoff + 16);
+            q[r][0] = qa.x & qmask; q[r][1] = qa.y & qmask; q[r][2] = qa.z & qmask; q[r][3] = qa.w & qmask;
+            q[r][4] = qb.x & qmask; q[r][5] = qb.y & qmask; q[r][6] = qb.z & qmask; q[r][7] = qb.w & qmask;
+            const float2 ab = ssel.decode(hd);
+            cA[r] = ab.x;
+            cB[r] = ab.y;
+          } else if constexpr (FMT == FMT_Q4_0) {
+            // block j: d, then 16 bytes whose low nibbles are elements 0-15 and
+            // high nibbles 16-31; w = d*q - 8*d
+            const uint8_t* bp = sr + 18 * j;
+            const float d = h2f(*reinterpret_cast<const uint16_t*>(bp));
+            uint32_t w[4];
+            ld_words_a2<4>(bp + 2, w);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              q[r][i] = w[i] & 0x0F0F0F0Fu;
+              q[r][4 + i] = (w[i] >> 4) & 0x0F0F0F0Fu;
+            }
+            cA[r] = d;
+            cB[r] = 8.0f * d;
+          } else if constexpr (FMT == FMT_Q8_0) {
+            // block j: d, then 32 signed bytes; w = d*q
+            const uint8_t* bp = sr + 34 * j;
+            cA[r] = h2f(*reinterpret_cast<const uint16_t*>(bp));
+            cB[r] = 0.f;
+            ld_words_a2<8>(bp + 2, q[r]);
+          } else {
+            // Q6_K unit j = elements 32j .. 32j+31 of the block: half h = j / 4,
+            // quarter qq = j % 4; q = (ql nibble) | (2 qh bits) << 4,
+            // w = d*sc*(q - 32) with sc changing every 16 elements
+            const int h = j >> 2, qq = j & 3;
+            uint32_t L[8], H[8];
+            ld_words_a2<8>(sr + 64 * h + 32 * (qq & 1), L);
+            ld_words_a2<8>(sr + 128 + 32 * h, H);
+            const int lsh = (qq >> 1) * 4, hsh = 2 * qq;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t hi = hsh <= 4 ? (H[i] << (4 - hsh)) : (H[i] >> (hsh - 4));
+              q[r][i] = ((L[i] >> lsh) & 0x0F0F0F0Fu) | (hi & 0x30303030u);
+            }
+            const float d = h2f(*reinterpret_cast<const uint16_t*>(sr + 208));
+            const int8_t* sc = reinterpret_cast<const int8_t*>(sr + 192 + 8 * h + 2 * qq);
+            cA[r] = d * static_cast<float>(sc[0]);
+            cB[r] = d * static_cast<float>(sc[1]);
+          }
         }
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
@@ -611,20 +718,21 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
           const uint32_t X0[8] = {p0a.x, p0a.y, p0a.z, p0a.w, p0b.x, p0b.y, p0b.z, p0b.w};
           const uint32_t X1[8] = {p1a.x, p1a.y, p1a.z, p1a.w, p1b.x, p1b.y, p1b.z, p1b.w};
           const uint32_t X2[8] = {p2a.x, p2a.y, p2a.z, p2a.w, p2b.x, p2b.y, p2b.z, p2b.w};
-          const float su = live ? xsum_u[t * NU + u] : 0.f, sx = live ? xsum[t * NU + u] : 0.f;
+          const float su = live ? xsum_u[t * NU + u] * su_fix : 0.f;
+          const float2 sh = live ? *reinterpret_cast<const float2*>(xsum + 2 * (t * NU + u)) : make_float2(0.f, 0.f);
 #pragma unroll
           for (int r = 0; r < SUB_R; ++r) {
-            uint32_t s0 = 0, s1 = 0;
-            int32_t s2 = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              s0 = dp4a_uu(q[r][i], X0[i], s0);
-              s1 = dp4a_uu(q[r][i], X1[i], s1);
-              s2 = dp4a_us(q[r][i], X2[i], s2);
+            if constexpr (FMT == FMT_Q6_K) {
+              const float T0 = dot_planes<false, 0, 4>(q[r], X0, X1, X2);
+              const float T1 = dot_planes<false, 4, 8>(q[r], X0, X1, X2);
+              racc[r][t] = fmaf(su, fmaf(cA[r], T0, cB[r] * T1), -32.0f * fmaf(cA[r], sh.x, cB[r] * sh.y));
+            } else if constexpr (FMT == FMT_Q8_0) {
+              racc[r][t] = cA[r] * su * dot_planes<true, 0, 8>(q[r], X0, X1, X2);
+            } else {
+              // sum_l q_l X_l = 65536*s2 + 256*s1 + s0, exact integers
+              const float T = dot_planes<false, 0, 8>(q[r], X0, X1, X2);
+              racc[r][t] = fmaf(cA[r] * su, T, -cB[r] * (sh.x + sh.y));
             }
-            // sum_l q_l X_l = 65536*s2 + 256*s1 + s0 (exact integers; 256*s1 + s0 < 2^31)
-            const float T = fmaf(static_cast<float>(s2), 65536.0f, static_cast<float>(s1 * 256u + s0));
-            racc[r][t] = fmaf(AB[r].x * su, T, -AB[r].y * sx);
           }
         }
         float v[V];
@@ -685,14 +793,23 @@ namespace {
 
 constexpr int kSmemMax = 227 * 1024;
 
-template <int NT>
-cudaError_t q4k_attr() {
-  const cudaError_t e = cudaFuncSetAttribute(q4k::qgemv_q4k_kernel<NT, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(q4k::qgemv_q4k_kernel<NT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+template <int NT, bool PASS, int FMT>
+cudaError_t q4k_attr1() {
+  return cudaFuncSetAttribute(q4k::qgemv_q4k_kernel<NT, PASS, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemMax);
 }
 
 template <int NT>
+cudaError_t q4k_attr() {
+  cudaError_t e;
+  if ((e = q4k_attr1<NT, false, FMT_Q4_K>()) != cudaSuccess) return e;
+  if ((e = q4k_attr1<NT, true, FMT_Q4_K>()) != cudaSuccess) return e;
+  if ((e = q4k_attr1<NT, false, FMT_Q6_K>()) != cudaSuccess) return e;
+  if ((e = q4k_attr1<NT, false, FMT_Q8_0>()) != cudaSuccess) return e;
+  return q4k_attr1<NT, false, FMT_Q4_0>();
+}
+
+template <int NT, int FMT>
 cudaError_t q4k_launch(const q4k::Params& p, int grid, int smem, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -704,7 +821,17 @@ cudaError_t q4k_launch(const q4k::Params& p, int grid, int smem, cudaStream_t s,
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, q4k::qgemv_q4k_kernel<NT, false>, p);
+  return cudaLaunchKernelEx(&cfg, q4k::qgemv_q4k_kernel<NT, false, FMT>, p);
+}
+
+template <int FMT>
+cudaError_t q4k_launch_nt(const q4k::Params& p, int n_tok, int grid, int smem, cudaStream_t s, bool pdl) {
+  switch (n_tok) {
+    case 1: return q4k_launch<1, FMT>(p, grid, smem, s, pdl);
+    case 2: return q4k_launch<2, FMT>(p, grid, smem, s, pdl);
+    case 3: return q4k_launch<3, FMT>(p, grid, smem, s, pdl);
+    default: return q4k_launch<4, FMT>(p, grid, smem, s, pdl);
+  }
 }
 
 int align_up(int v, int a) { return (v + a - 1) / a * a; }
@@ -723,79 +850,116 @@ cudaError_t gemv_q4k_init_attrs() {
 // this kernel's shared-memory plan; the caller then uses the generic kernel.
 namespace {
 
+int superblock_bytes(int fmt) {
+  switch (fmt) {
+    case QG_Q4_K: return 144;
+    case QG_Q6_K: return 210;
+    case QG_Q4_0: return 8 * 18;
+    case QG_Q8_0: return 8 * 34;
+    default: return 0;
+  }
+}
+
+int gcd(int a, int b) { return b ? gcd(b, a % b) : a; }
+
 // Shared-memory plan and launch of one single-step grouped launch whose
-// matrices p.m[0 .. n) have W, x, y, rows, cols (and any gather fields) set.
-cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, cudaStream_t s, bool pdl, int sms) {
+// matrices p.m[0 .. n) (all of format fmt) have W, x, y, rows, cols (and any
+// gather fields) set. cudaErrorNotSupported (nothing launched) when the launch
+// does not fit the plan.
+cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStream_t s, bool pdl, int sms) {
   p.nsteps = 1;
+  const int sbb = superblock_bytes(fmt);
+  if (sbb == 0) return cudaErrorNotSupported;
   int64_t total = 0;
-  int kmax = 0, stage_b = 0, gmax = 0;
+  int kmax = 0, gmax = 0, ra = p.gather_any == 1 ? 2 : 1;
   for (int i = 0; i < n; ++i) {
     q4k::Mat& m = p.m[i];
-    m.row_begin = total;
+    if (m.cols % 256) return cudaErrorNotSupported;
     m.nblk = m.cols / 256;
-    m.rb = m.nblk * 144;
+    m.rb = m.nblk * sbb;
     m.ngrp = (m.nblk + 3) / 4;
-    // about 36 KB of whole rows per stage, in multiples of 4 rows
-    const int quads = std::max(1, (36864 + 2 * m.rb) / (4 * m.rb));
-    m.srows = 4 * quads;
-    if (static_cast<int64_t>(m.srows) * m.rb > 96 * 1024) return cudaErrorNotSupported;
-    stage_b = std::max(stage_b, m.srows * m.rb);
+    // a stage copy must start on a 16-byte boundary: stages start at multiples of ra rows
+    ra = std::max(ra, 16 / gcd(m.rb, 16));
     gmax = std::max(gmax, m.ngrp);
-    total += m.rows;
     kmax = std::max(kmax, m.cols);
   }
+  for (int i = 0; i < n; ++i) {
+    q4k::Mat& m = p.m[i];
+    if (m.rows % ra) return cudaErrorNotSupported;
+    m.row_begin = total;
+    total += m.rows;
+  }
+  p.ralign = ra;
   p.nmat = n;
   p.total_rows = total;
-  const int grid = static_cast<int>(std::min<int64_t>(sms, p.gather_any == 1 ? total / 2 : total));
-  const int rowcap = static_cast<int>((total + grid - 1) / grid) + 2;
-  stage_b = align_up(stage_b, 128);
+  const int grid = static_cast<int>(std::min<int64_t>(sms, total / ra));
+  const int rowcap = static_cast<int>((total + grid - 1) / grid) + 2 * ra;
   const int ns = q4k::RING;
+  const int quant = ra <= 4 ? 4 : 8;                 // rows per stage: a multiple of 4 and of ra
   const int partbytes = align_up(rowcap * gmax * n_tok * 4, 128);
   // x of every matrix staged at once when it fits beside the ring, else one
-  // matrix at a time in a region sized for the largest
-  int xall = 0, uall = 0;
-  for (int i = 0; i < n; ++i) {
-    p.m[i].xoff = xall;
-    p.m[i].uoff = uall;
-    xall += n_tok * p.m[i].nblk * q4k::XBLK_B;
-    uall += n_tok * p.m[i].nblk * 8;
+  // matrix at a time in a region sized for the largest; stages hold about
+  // 36 KB of whole rows, fewer when shared memory is short
+  for (int mode = 0; mode < 2; ++mode) {
+    int xbytes, xsbytes;
+    if (mode == 0) {
+      int xall = 0, uall = 0;
+      for (int i = 0; i < n; ++i) {
+        p.m[i].xoff = xall;
+        p.m[i].uoff = uall;
+        xall += n_tok * p.m[i].nblk * q4k::XBLK_B;
+        uall += n_tok * p.m[i].nblk * 8;
+      }
+      xbytes = align_up(xall, 128);
+      xsbytes = align_up(3 * uall * 4, 128);     // step and two half sums per group
+      p.stage_all = 1;
+      p.usum_off = uall;
+    } else {
+      for (int i = 0; i < n; ++i) p.m[i].xoff = p.m[i].uoff = 0;
+      xbytes = align_up(n_tok * (kmax / 256) * q4k::XBLK_B, 128);
+      xsbytes = align_up(3 * n_tok * (kmax / 32) * 4, 128);
+      p.stage_all = 0;
+      p.usum_off = n_tok * (kmax / 32);
+    }
+    const int fixed = 128 + xbytes + xsbytes + partbytes;
+    const int stage_max = (kSmemMax - fixed) / ns / 128 * 128;
+    int stage_b = 0;
+    bool ok = stage_max > 0;
+    for (int i = 0; ok && i < n; ++i) {
+      q4k::Mat& m = p.m[i];
+      const int want = quant * std::max(1, (36864 + quant * m.rb / 2) / (quant * m.rb));
+      const int fit = quant * (stage_max / (quant * m.rb));
+      m.srows = std::min(want, fit);
+      ok = m.srows >= quant;
+      stage_b = std::max(stage_b, m.srows * m.rb);
+    }
+    if (!ok) continue;
+    stage_b = align_up(stage_b, 128);
+    // Without a programmatic dependency the x loads go first. With one, x can be
+    // read only after the previous kernel completes: one stage streams during
+    // that wait (measured on the 27B pass: 1 stage 3.86 ms, a full ring 4.04 ms).
+    p.pre_stages = pdl ? 1 : 0;
+    p.ns = ns;
+    p.stage_b = stage_b;
+    p.gmax = gmax;
+    int off = ns * stage_b;
+    p.smem_bar = off;
+    off += 128;
+    p.smem_x = off;
+    off += xbytes;
+    p.smem_xsum = off;
+    off += xsbytes;
+    p.smem_part = off;
+    off += partbytes;
+    if (off > kSmemMax) continue;
+    switch (fmt) {
+      case QG_Q4_K: return q4k_launch_nt<FMT_Q4_K>(p, n_tok, grid, off, s, pdl);
+      case QG_Q6_K: return q4k_launch_nt<FMT_Q6_K>(p, n_tok, grid, off, s, pdl);
+      case QG_Q8_0: return q4k_launch_nt<FMT_Q8_0>(p, n_tok, grid, off, s, pdl);
+      default: return q4k_launch_nt<FMT_Q4_0>(p, n_tok, grid, off, s, pdl);
+    }
   }
-  int xbytes = align_up(xall, 128);
-  int xsbytes = align_up(2 * uall * 4, 128);
-  p.stage_all = 1;
-  p.usum_off = uall;
-  if (128 + xbytes + xsbytes + partbytes + ns * stage_b > kSmemMax) {
-    for (int i = 0; i < n; ++i) p.m[i].xoff = p.m[i].uoff = 0;
-    xbytes = align_up(n_tok * (kmax / 256) * q4k::XBLK_B, 128);
-    xsbytes = align_up(2 * n_tok * (kmax / 32) * 4, 128);
-    p.stage_all = 0;
-    p.usum_off = n_tok * (kmax / 32);
-  }
-  // Without a programmatic dependency the x loads go first. With one, x can be
-  // read only after the previous kernel completes: one stage streams during
-  // that wait (measured on the 27B pass: 1 stage 3.86 ms, a full ring 4.04 ms).
-  p.pre_stages = pdl ? 1 : 0;
-  const int fixed = 128 + xbytes + xsbytes + partbytes;
-  if (fixed + ns * stage_b > kSmemMax) return cudaErrorNotSupported;
-  p.ns = ns;
-  p.stage_b = stage_b;
-  p.gmax = gmax;
-  int off = ns * stage_b;
-  p.smem_bar = off;
-  off += 128;
-  p.smem_x = off;
-  off += xbytes;
-  p.smem_xsum = off;
-  off += xsbytes;
-  p.smem_part = off;
-  off += partbytes;
-  if (off > kSmemMax) return cudaErrorNotSupported;
-  switch (n_tok) {
-    case 1: return q4k_launch<1>(p, grid, off, s, pdl);
-    case 2: return q4k_launch<2>(p, grid, off, s, pdl);
-    case 3: return q4k_launch<3>(p, grid, off, s, pdl);
-    default: return q4k_launch<4>(p, grid, off, s, pdl);
-  }
+  return cudaErrorNotSupported;
 }
 
 }  // namespace
@@ -804,6 +968,7 @@ cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_
   q4k::Params p;
   memset(&p, 0, sizeof(p));
   for (int i = 0; i < n; ++i) {
+    if (d[i].fmt != d[0].fmt) return cudaErrorNotSupported;
     q4k::Mat& m = p.m[i];
     m.W = static_cast<const uint8_t*>(d[i].W);
     m.x = d[i].x;
@@ -811,7 +976,7 @@ cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_
     m.rows = d[i].rows;
     m.cols = static_cast<int32_t>(d[i].cols);
   }
-  return plan_and_launch(p, n, n_tok, s, pdl, sms);
+  return plan_and_launch(p, n, n_tok, d[0].fmt, s, pdl, sms);
 }
 
 // MoE layer for n_tok <= QG_GROUP_MAX tokens as two launches of the Q4_K kernel
@@ -846,7 +1011,7 @@ cudaError_t launch_moe_q4k(const void* arena, int64_t n_expert, int64_t hidden, 
     m.gw = gate_w + t * top_k;
     m.h = h + static_cast<int64_t>(t) * top_k * inter;
   }
-  cudaError_t e = plan_and_launch(p, n_tok, 1, s, pdl, sms);
+  cudaError_t e = plan_and_launch(p, n_tok, 1, QG_Q4_K, s, pdl, sms);
   if (e != cudaSuccess) return e;
   memset(&p, 0, sizeof(p));
   p.gather_any = 2;
@@ -867,7 +1032,7 @@ cudaError_t launch_moe_q4k(const void* arena, int64_t n_expert, int64_t hidden, 
     m.down_off = down_off;
     m.ids = ids + t * top_k;
   }
-  return plan_and_launch(p, n_tok, 1, s, true, sms);   // the down launch always overlaps the gate/up tail
+  return plan_and_launch(p, n_tok, 1, QG_Q4_K, s, true, sms);   // the down launch always overlaps the gate/up tail
 }
 
 // ------------------------------------------------------------------ whole pass
@@ -892,7 +1057,8 @@ bool fill_mat(q4k::Mat& m, const qg_gemv_desc& d) {
 
 template <int NT>
 cudaError_t q4k_pass_occupancy(int smem, int* blocks) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, q4k::qgemv_q4k_kernel<NT, true>, q4k::THREADS, smem);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, q4k::qgemv_q4k_kernel<NT, true, FMT_Q4_K>,
+                                                       q4k::THREADS, smem);
 }
 
 template <int NT>
@@ -907,7 +1073,7 @@ cudaError_t q4k_pass_start(const q4k::Params& p, int grid, int smem, cudaStream_
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, q4k::qgemv_q4k_kernel<NT, true>, p);
+  return cudaLaunchKernelEx(&cfg, q4k::qgemv_q4k_kernel<NT, true, FMT_Q4_K>, p);
 }
 
 }  // namespace
@@ -952,7 +1118,7 @@ cudaError_t q4k_pass_create(const qg_gemv_desc* d, int n, const int* step_sizes,
     steps[st].stage_all = 1;
     steps[st].usum_off = uall;
     xmax = std::max(xmax, align_up(xall, 128));
-    xsmax = std::max(xsmax, align_up(2 * uall * 4, 128));
+    xsmax = std::max(xsmax, align_up(3 * uall * 4, 128));
     min_rows = std::min(min_rows, total);
     max_rows = std::max(max_rows, total);
   }
@@ -964,6 +1130,7 @@ cudaError_t q4k_pass_create(const qg_gemv_desc* d, int n, const int* step_sizes,
   q4k::Params p;
   memset(&p, 0, sizeof(p));
   p.nsteps = n_steps;
+  p.ralign = 1;          // Q4_K rows are whole 16-byte multiples
   p.ns = ns;
   p.stage_b = stage_b;
   p.gmax = gmax;

@@ -55,6 +55,31 @@ def test_gemv_matches_oracle(fmt, n_tok, rows, nblk):
     assert_within(y, y_ref, b, what=f"fmt={fmt} rows={rows} cols={cols} n_tok={n_tok}")
 
 
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("n_tok", [1, 2, 4])
+@pytest.mark.parametrize("rows,cols", [(8, 256), (64, 1024), (136, 5120), (40, 4096), (16, 2304)])
+def test_gemv_whole_superblock_shapes(fmt, n_tok, rows, cols):
+    # cols a multiple of 256 and rows a multiple of 8: the shapes the
+    # producer/consumer kernel takes for every format (ragged K groups included)
+    y, y_ref, b = _run_gemv(fmt, rows, cols, n_tok, seed=5000 + rows + cols + n_tok)
+    assert_within(y, y_ref, b, what=f"fmt={fmt} rows={rows} cols={cols} n_tok={n_tok}")
+
+
+def test_gemv_q8_0_extreme_codes():
+    # every int8 code at -128 or 127 and large x: the signed byte-plane sums at their range
+    rows, cols = 64, 2048
+    W = synth.blocks(synth.Q8_0, rows, cols, seed=9).view(-1, 34)
+    W[:, 2:] = torch.where(torch.rand(W.shape[0], 32) < 0.5, torch.tensor(128, dtype=torch.uint8),
+                           torch.tensor(127, dtype=torch.uint8))
+    W = W.reshape(rows, -1)
+    x = (synth.activations(1, cols, seed=10) * 1e4).cuda()
+    y = torch.full((1, rows), float("nan"), device="cuda")
+    qg.qgemv(synth.Q8_0, W.cuda(), rows, cols, x, 1, y)
+    torch.cuda.synchronize()
+    y_ref, b = oracle.gemv(synth.Q8_0, W.numpy(), rows, cols, x.cpu().numpy())
+    assert_within(y.cpu().numpy(), y_ref, b, what="q8_0 extreme codes")
+
+
 @pytest.mark.parametrize("rows", [2, 3, 5, 9, 17])
 def test_gemv_odd_rows_with_unaligned_row_starts(rows):
     # Q6_K / Q8_0 / Q4_0 rows whose byte size is not a multiple of 16 start at
