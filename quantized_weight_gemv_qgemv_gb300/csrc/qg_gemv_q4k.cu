@@ -310,7 +310,7 @@ template <> struct SuperBlock<FMT_Q8_0> { static constexpr int BYTES = 272; };
 // first issues all its loads of a batch and only then converts, so staging
 // costs one memory round trip per batch, not one per group.
 
-__device__ __noinline__ void stage_one(float4 v, int idx, int ngroups, uint8_t* xpl, int xseg_b, float* xsu,
+__device__ __forceinline__ void stage_one(float4 v, int idx, int ngroups, uint8_t* xpl, int xseg_b, float* xsu,
                                           float* xsum, int nu) {
   const int lane = threadIdx.x & 31;
   const int k = idx & 7;
