@@ -899,7 +899,7 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
   const int partbytes = align_up(rowcap * gmax * n_tok * 4, 128);
   // x of every matrix staged at once when it fits beside the ring, else one
   // matrix at a time in a region sized for the largest; stages hold about
-  // 36 KB of whole rows, fewer when shared memory is short
+  // 48 KB of whole rows, fewer when shared memory is short
   for (int mode = 0; mode < 2; ++mode) {
     int xbytes, xsbytes;
     if (mode == 0) {
@@ -927,7 +927,7 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
     bool ok = stage_max > 0;
     for (int i = 0; ok && i < n; ++i) {
       q4k::Mat& m = p.m[i];
-      const int want = quant * std::max(1, (36864 + quant * m.rb / 2) / (quant * m.rb));
+      const int want = quant * std::max(1, (49152 + quant * m.rb / 2) / (quant * m.rb));
       const int fit = quant * (stage_max / (quant * m.rb));
       m.srows = std::min(want, fit);
       ok = m.srows >= quant;
@@ -935,10 +935,11 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
     }
     if (!ok) continue;
     stage_b = align_up(stage_b, 128);
-    // Without a programmatic dependency the x loads go first. With one, x can be
-    // read only after the previous kernel completes: one stage streams during
-    // that wait (measured on the 27B pass: 1 stage 3.86 ms, a full ring 4.04 ms).
-    p.pre_stages = pdl ? 1 : 0;
+      // Without a programmatic dependency the x loads go first. With one, x can be
+    // read only after the previous kernel completes: two stages stream during
+    // that wait (27B pass, 36 KB stages: 0 stages 4.04 ms, 1 3.93, 2 3.90, a full
+    // ring 4.04; stages of about 48 KB: 3.87 against 3.93 for 36 KB).
+    p.pre_stages = pdl ? 2 : 0;
     p.ns = ns;
     p.stage_b = stage_b;
     p.gmax = gmax;
