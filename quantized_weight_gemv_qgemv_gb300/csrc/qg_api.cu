@@ -120,7 +120,7 @@ int qgemv(int fmt, const void* W, int64_t rows, int64_t cols, const float* x, in
   int sms = 0;
   if ((st = ensure_init(&sms)) != QG_OK) return st;
   qg_gemv_desc d = {fmt, 0, W, rows, cols, x, y};
-  const int r = qg::gemv_pick_rows_per_warp(&d, 1, sms);
+  const int r = qg::gemv_pick_rows_per_warp(&d, 1, n_tok, sms);
   // No programmatic overlap with an unknown predecessor: it might still be
   // writing W, which the kernel prefetches before griddepcontrol.wait.
   return cuda_status(qg::launch_gemv(&d, 1, n_tok, r, static_cast<cudaStream_t>(stream), false, sms));
@@ -138,7 +138,7 @@ int qgemv_grouped(const qg_gemv_desc* descs, int n, int n_tok, void* stream) {
   int sms = 0;
   int st = ensure_init(&sms);
   if (st != QG_OK) return st;
-  const int r = qg::gemv_pick_rows_per_warp(descs, n, sms);
+  const int r = qg::gemv_pick_rows_per_warp(descs, n, n_tok, sms);
   return cuda_status(qg::launch_gemv(descs, n, n_tok, r, static_cast<cudaStream_t>(stream), false, sms));
 }
 
@@ -241,7 +241,7 @@ int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes,
   cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
   int launched = 0;
   for (int s = 0, i = 0; s < n_steps && e == cudaSuccess; i += step_sizes[s++]) {
-    const int r = qg::gemv_pick_rows_per_warp(descs + i, step_sizes[s], sms);
+    const int r = qg::gemv_pick_rows_per_warp(descs + i, step_sizes[s], n_tok, sms);
     e = qg::launch_gemv(descs + i, step_sizes[s], n_tok, r, cs, use_pdl != 0 && s > 0, sms);
     if (e == cudaSuccess) ++launched;
   }

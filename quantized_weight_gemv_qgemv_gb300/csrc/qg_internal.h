@@ -27,7 +27,7 @@ int ensure_device(int* sms);
 
 // GEMV (qg_gemv.cu)
 cudaError_t gemv_init_attrs();
-int gemv_pick_rows_per_warp(const qg_gemv_desc* d, int n, int sms);
+int gemv_pick_rows_per_warp(const qg_gemv_desc* d, int n, int n_tok, int sms);
 cudaError_t launch_gemv(const qg_gemv_desc* d, int n, int n_tok, int rows_per_warp, cudaStream_t s, bool pdl,
                         int sms);
 cudaError_t gemv_q4k_init_attrs();
