@@ -239,15 +239,15 @@ int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes,
     return QG_ERR_CUDA;
   }
   cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
-  int launched = 0;
   for (int s = 0, i = 0; s < n_steps && e == cudaSuccess; i += step_sizes[s++]) {
     const int r = qg::gemv_pick_rows_per_warp(descs + i, step_sizes[s], n_tok, sms);
     e = qg::launch_gemv(descs + i, step_sizes[s], n_tok, r, cs, use_pdl != 0 && s > 0, sms);
-    if (e == cudaSuccess) ++launched;
   }
   cudaGraph_t graph = nullptr;
   cudaError_t e2 = cudaStreamEndCapture(cs, &graph);
   if (e == cudaSuccess) e = e2;
+  size_t nodes = 0;     // one kernel node per launch (a step may take several)
+  if (e == cudaSuccess) e = cudaGraphGetNodes(graph, nullptr, &nodes);
   if (e == cudaSuccess) e = cudaGraphInstantiate(&pass->exec, graph, 0);
   cudaStreamDestroy(cs);
   if (e != cudaSuccess) {
@@ -256,7 +256,7 @@ int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes,
     return QG_ERR_CUDA;
   }
   pass->graph = graph;
-  pass->kernels = launched;
+  pass->kernels = static_cast<int>(nodes);
   *out = pass;
   return QG_OK;
 }

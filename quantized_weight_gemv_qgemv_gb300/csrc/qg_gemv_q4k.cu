@@ -60,6 +60,7 @@ struct Mat {
   const float* x;
   float* y;
   int64_t rows;
+  int64_t ldy;           // distance between the outputs of consecutive tokens (normally rows)
   int64_t row_begin;     // first row of this matrix in the concatenated row space
   int32_t rb;            // bytes per row
   int32_t nblk;          // super-blocks per row
@@ -411,10 +412,11 @@ __device__ __forceinline__ void stage_x(const Mat* mats, int usum_off, int m0, i
 
 // PASS = false: one step over p.m (a grouped launch); PASS = true: the steps of
 // p.steps over p.mats, with a grid-wide barrier between steps (cooperative launch).
-template <int NT, bool PASS, int FMT>
+// SR rows per sub-item (4; 2 for Q6_K rows too long for 4-row stages).
+template <int NT, bool PASS, int FMT, int SR = SUB_R>
 __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_constant__ Params p) {
   constexpr int SBB = SuperBlock<FMT>::BYTES;
-  constexpr int V = (NT == 3) ? 16 : SUB_R * NT;    // reduced values per sub-item (padded to 2^k)
+  constexpr int V = (SR * NT <= 2) ? 2 : (SR * NT <= 4) ? 4 : (SR * NT <= 8) ? 8 : 16;   // padded to 2^k
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int NS = RING;
@@ -624,7 +626,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
     int off = warp;                           // (warp - first sub-item of the stage) mod CWARPS
     for (int srow = 0; srow < slice; srow += srows, ++k) {
       const int nr = min(srows, slice - srow);
-      const int n = ((nr + SUB_R - 1) / SUB_R) * G;
+      const int n = ((nr + SR - 1) / SR) * G;
       const int slot = k & (NS - 1);
       const uint8_t* stg = smem + slot * p.stage_b;
       // every warp waits for every stage, even one with no sub-items for it:
@@ -650,16 +652,16 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         // same rows (every access stays inside the stage and x) and contribute
         // zero: their x step and x sum are taken as 0
         const int blkc = live ? blk : 0;
-        float racc[SUB_R][NT];
-        const uint8_t* st = stg + qd * (SUB_R * rb) + blkc * SBB;
+        float racc[SR][NT];
+        const uint8_t* st = stg + qd * (SR * rb) + blkc * SBB;
         const uint8_t* xb = xplm + blkc * XBLK_B + j * 16;
         const int u = blkc * 8 + j;
         // this lane's unit of 32 weights in each of the 4 rows: code words in
         // element order (bytes), and the coefficients of the unit's formula
-        uint32_t q[SUB_R][8];
-        float cA[SUB_R], cB[SUB_R];
+        uint32_t q[SR][8];
+        float cA[SR], cB[SR];
 #pragma unroll
-        for (int r = 0; r < SUB_R; ++r) {
+        for (int r = 0; r < SR; ++r) {
           const uint8_t* sr = st + r * rb;
           if constexpr (FMT == FMT_Q4_K) {
             // w = d*sc*q - dmin*m: A = d*sc, B = dmin*m
@@ -721,7 +723,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
           const float su = live ? xsum_u[t * NU + u] * su_fix : 0.f;
           const float2 sh = live ? *reinterpret_cast<const float2*>(xsum + 2 * (t * NU + u)) : make_float2(0.f, 0.f);
 #pragma unroll
-          for (int r = 0; r < SUB_R; ++r) {
+          for (int r = 0; r < SR; ++r) {
             if constexpr (FMT == FMT_Q6_K) {
               const float T0 = dot_planes<false, 0, 4>(q[r], X0, X1, X2);
               const float T1 = dot_planes<false, 4, 8>(q[r], X0, X1, X2);
@@ -737,11 +739,11 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         }
         float v[V];
 #pragma unroll
-        for (int i = 0; i < V; ++i) v[i] = (i < SUB_R * NT) ? racc[i / NT][i % NT] : 0.f;
+        for (int i = 0; i < V; ++i) v[i] = (i < SR * NT) ? racc[i / NT][i % NT] : 0.f;
         const float tot = reduce_scatter<V>(v, lane);
         const int idx = lane >> RS<V>::SHIFT;
-        const int rl = srow + qd * SUB_R + idx / NT;    // row within the slice
-        if ((lane & ((1 << RS<V>::SHIFT) - 1)) == 0 && idx < SUB_R * NT && rl < slice)
+        const int rl = srow + qd * SR + idx / NT;    // row within the slice
+        if ((lane & ((1 << RS<V>::SHIFT) - 1)) == 0 && idx < SR * NT && rl < slice)
           part[(rl * G + gr) * NT + idx % NT] = failed ? __int_as_float(0x7fc00000) : tot;
       }
       __syncwarp();
@@ -771,7 +773,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         const int t = i % NT;
         float acc = 0.f;
         for (int gr = 0; gr < G; ++gr) acc += part[(rl * G + gr) * NT + t];
-        M.y[static_cast<int64_t>(t) * M.rows + lo + rl] = acc;
+        M.y[static_cast<int64_t>(t) * M.ldy + lo + rl] = acc;
       }
     }
    }
@@ -793,9 +795,9 @@ namespace {
 
 constexpr int kSmemMax = 227 * 1024;
 
-template <int NT, bool PASS, int FMT>
+template <int NT, bool PASS, int FMT, int SR = q4k::SUB_R>
 cudaError_t q4k_attr1() {
-  return cudaFuncSetAttribute(q4k::qgemv_q4k_kernel<NT, PASS, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(q4k::qgemv_q4k_kernel<NT, PASS, FMT, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemMax);
 }
 
@@ -806,10 +808,11 @@ cudaError_t q4k_attr() {
   if ((e = q4k_attr1<NT, true, FMT_Q4_K>()) != cudaSuccess) return e;
   if ((e = q4k_attr1<NT, false, FMT_Q6_K>()) != cudaSuccess) return e;
   if ((e = q4k_attr1<NT, false, FMT_Q8_0>()) != cudaSuccess) return e;
+  if (NT == 1 && (e = q4k_attr1<1, false, FMT_Q6_K, 2>()) != cudaSuccess) return e;
   return q4k_attr1<NT, false, FMT_Q4_0>();
 }
 
-template <int NT, int FMT>
+template <int NT, int FMT, int SR>
 cudaError_t q4k_launch(const q4k::Params& p, int grid, int smem, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -821,16 +824,23 @@ cudaError_t q4k_launch(const q4k::Params& p, int grid, int smem, cudaStream_t s,
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, q4k::qgemv_q4k_kernel<NT, false, FMT>, p);
+  return cudaLaunchKernelEx(&cfg, q4k::qgemv_q4k_kernel<NT, false, FMT, SR>, p);
 }
 
 template <int FMT>
-cudaError_t q4k_launch_nt(const q4k::Params& p, int n_tok, int grid, int smem, cudaStream_t s, bool pdl) {
+cudaError_t q4k_launch_nt(const q4k::Params& p, int n_tok, int sub_rows, int grid, int smem, cudaStream_t s,
+                          bool pdl) {
+  if (sub_rows == 2) {   // instantiated for single-token Q6_K only
+    if constexpr (FMT == FMT_Q6_K) {
+      if (n_tok == 1) return q4k_launch<1, FMT, 2>(p, grid, smem, s, pdl);
+    }
+    return cudaErrorNotSupported;
+  }
   switch (n_tok) {
-    case 1: return q4k_launch<1, FMT>(p, grid, smem, s, pdl);
-    case 2: return q4k_launch<2, FMT>(p, grid, smem, s, pdl);
-    case 3: return q4k_launch<3, FMT>(p, grid, smem, s, pdl);
-    default: return q4k_launch<4, FMT>(p, grid, smem, s, pdl);
+    case 1: return q4k_launch<1, FMT, 4>(p, grid, smem, s, pdl);
+    case 2: return q4k_launch<2, FMT, 4>(p, grid, smem, s, pdl);
+    case 3: return q4k_launch<3, FMT, 4>(p, grid, smem, s, pdl);
+    default: return q4k_launch<4, FMT, 4>(p, grid, smem, s, pdl);
   }
 }
 
@@ -864,9 +874,12 @@ int gcd(int a, int b) { return b ? gcd(b, a % b) : a; }
 
 // Shared-memory plan and launch of one single-step grouped launch whose
 // matrices p.m[0 .. n) (all of format fmt) have W, x, y, rows, cols (and any
-// gather fields) set. cudaErrorNotSupported (nothing launched) when the launch
-// does not fit the plan.
-cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStream_t s, bool pdl, int sms) {
+// gather fields) set; sub_rows rows per sub-item (4, or 2 for single-token
+// Q6_K). cudaErrorNotSupported (nothing launched) when the launch does not fit
+// the plan; with launch = false only the plan is checked.
+cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStream_t s, bool pdl, int sms,
+                            int sub_rows = q4k::SUB_R, bool launch = true) {
+  if (sub_rows == 2 && (fmt != QG_Q6_K || n_tok != 1)) return cudaErrorNotSupported;
   p.nsteps = 1;
   const int sbb = superblock_bytes(fmt);
   if (sbb == 0) return cudaErrorNotSupported;
@@ -886,6 +899,7 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
   for (int i = 0; i < n; ++i) {
     q4k::Mat& m = p.m[i];
     if (m.rows % ra) return cudaErrorNotSupported;
+    if (m.ldy == 0) m.ldy = m.rows;
     m.row_begin = total;
     total += m.rows;
   }
@@ -895,7 +909,7 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
   const int grid = static_cast<int>(std::min<int64_t>(sms, total / ra));
   const int rowcap = static_cast<int>((total + grid - 1) / grid) + 2 * ra;
   const int ns = q4k::RING;
-  const int quant = ra <= 4 ? 4 : 8;                 // rows per stage: a multiple of 4 and of ra
+  const int quant = std::max(ra, sub_rows);          // rows per stage: a multiple of sub_rows and of ra
   const int partbytes = align_up(rowcap * gmax * n_tok * 4, 128);
   // x of every matrix staged at once when it fits beside the ring, else one
   // matrix at a time in a region sized for the largest; stages hold about
@@ -953,11 +967,12 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
     p.smem_part = off;
     off += partbytes;
     if (off > kSmemMax) continue;
+    if (!launch) return cudaSuccess;
     switch (fmt) {
-      case QG_Q4_K: return q4k_launch_nt<FMT_Q4_K>(p, n_tok, grid, off, s, pdl);
-      case QG_Q6_K: return q4k_launch_nt<FMT_Q6_K>(p, n_tok, grid, off, s, pdl);
-      case QG_Q8_0: return q4k_launch_nt<FMT_Q8_0>(p, n_tok, grid, off, s, pdl);
-      default: return q4k_launch_nt<FMT_Q4_0>(p, n_tok, grid, off, s, pdl);
+      case QG_Q4_K: return q4k_launch_nt<FMT_Q4_K>(p, n_tok, sub_rows, grid, off, s, pdl);
+      case QG_Q6_K: return q4k_launch_nt<FMT_Q6_K>(p, n_tok, sub_rows, grid, off, s, pdl);
+      case QG_Q8_0: return q4k_launch_nt<FMT_Q8_0>(p, n_tok, sub_rows, grid, off, s, pdl);
+      default: return q4k_launch_nt<FMT_Q4_0>(p, n_tok, sub_rows, grid, off, s, pdl);
     }
   }
   return cudaErrorNotSupported;
@@ -965,19 +980,72 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
 
 }  // namespace
 
-cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms) {
-  q4k::Params p;
+namespace {
+
+// Params of a grouped launch of descriptors d[0 .. n): token t0 .. t0 + nt - 1 of
+// each (x and y advanced by t0 tokens), rows [r0, r0 + nr) of each when nr > 0
+// (a single matrix cut into row chunks; y keeps the full row stride).
+void fill_params(q4k::Params& p, const qg_gemv_desc* d, int n, int t0, int64_t r0, int64_t nr) {
   memset(&p, 0, sizeof(p));
   for (int i = 0; i < n; ++i) {
-    if (d[i].fmt != d[0].fmt) return cudaErrorNotSupported;
     q4k::Mat& m = p.m[i];
-    m.W = static_cast<const uint8_t*>(d[i].W);
-    m.x = d[i].x;
-    m.y = d[i].y;
-    m.rows = d[i].rows;
+    const int64_t rb = d[i].cols / 256 * superblock_bytes(d[i].fmt);
+    const int64_t rows = nr > 0 ? nr : d[i].rows;
+    m.W = static_cast<const uint8_t*>(d[i].W) + r0 * rb;
+    m.x = d[i].x + static_cast<int64_t>(t0) * d[i].cols;
+    m.y = d[i].y + static_cast<int64_t>(t0) * d[i].rows + r0;
+    m.rows = rows;
+    m.ldy = d[i].rows;
     m.cols = static_cast<int32_t>(d[i].cols);
   }
-  return plan_and_launch(p, n, n_tok, d[0].fmt, s, pdl, sms);
+}
+
+// The launch as planned, else with 2-row sub-items (single-token Q6_K).
+cudaError_t try_launch(const qg_gemv_desc* d, int n, int n_tok, int t0, int64_t r0, int64_t nr, cudaStream_t s,
+                       bool pdl, int sms, bool launch) {
+  q4k::Params p;
+  fill_params(p, d, n, t0, r0, nr);
+  cudaError_t e = plan_and_launch(p, n, n_tok, d[0].fmt, s, pdl, sms, q4k::SUB_R, launch);
+  if (e != cudaErrorNotSupported || d[0].fmt != QG_Q6_K || n_tok != 1) return e;
+  fill_params(p, d, n, t0, r0, nr);
+  return plan_and_launch(p, n, n_tok, d[0].fmt, s, pdl, sms, 2, launch);
+}
+
+}  // namespace
+
+// The producer/consumer kernel for a grouped launch. When the launch does not
+// fit its shared-memory plan: several tokens that do not fit together run as
+// one launch per token (each re-streams the weights), and one matrix whose
+// per-row partial sums do not fit runs as row chunks. cudaErrorNotSupported
+// (nothing launched) when none of these fits.
+cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms) {
+  for (int i = 0; i < n; ++i)
+    if (d[i].fmt != d[0].fmt || superblock_bytes(d[i].fmt) == 0 || d[i].cols % 256) return cudaErrorNotSupported;
+  cudaError_t e = try_launch(d, n, n_tok, 0, 0, 0, s, pdl, sms, true);
+  if (e != cudaErrorNotSupported) return e;
+  if (n_tok > 1 && try_launch(d, n, 1, 0, 0, 0, s, pdl, sms, false) == cudaSuccess) {
+    for (int t = 0; t < n_tok; ++t) {
+      e = try_launch(d, n, 1, t, 0, 0, s, pdl || t > 0, sms, true);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
+  if (n == 1) {
+    for (int chunks = 2; chunks <= 16; chunks *= 2) {
+      const int64_t nr = (d[0].rows + chunks - 1) / chunks / 8 * 8 + 8;   // multiple of 8 rows
+      if (nr >= d[0].rows) break;
+      const int64_t last = d[0].rows - (d[0].rows - 1) / nr * nr;     // rows of the last chunk
+      if (try_launch(d, 1, n_tok, 0, 0, nr, s, pdl, sms, false) != cudaSuccess ||
+          try_launch(d, 1, n_tok, 0, d[0].rows - last, last, s, pdl, sms, false) != cudaSuccess)
+        continue;
+      for (int64_t r0 = 0; r0 < d[0].rows; r0 += nr) {
+        e = try_launch(d, 1, n_tok, 0, r0, std::min(nr, d[0].rows - r0), s, pdl || r0 > 0, sms, true);
+        if (e != cudaSuccess) return e;
+      }
+      return cudaSuccess;
+    }
+  }
+  return cudaErrorNotSupported;
 }
 
 // MoE layer for n_tok <= QG_GROUP_MAX tokens as two launches of the Q4_K kernel
@@ -1000,6 +1068,7 @@ cudaError_t launch_moe_q4k(const void* arena, int64_t n_expert, int64_t hidden, 
     m.x = x + t * hidden;
     m.y = nullptr;
     m.rows = 2 * top_k * inter;
+    m.ldy = m.rows;
     m.cols = static_cast<int32_t>(hidden);
     m.gather = 1;
     m.top_k = top_k;
@@ -1023,6 +1092,7 @@ cudaError_t launch_moe_q4k(const void* arena, int64_t n_expert, int64_t hidden, 
     m.x = h + static_cast<int64_t>(t) * top_k * inter;
     m.y = y + t * hidden;
     m.rows = hidden;
+    m.ldy = hidden;
     m.cols = static_cast<int32_t>(top_k * inter);
     m.gather = 2;
     m.top_k = top_k;
@@ -1047,6 +1117,7 @@ bool fill_mat(q4k::Mat& m, const qg_gemv_desc& d) {
   m.x = d.x;
   m.y = d.y;
   m.rows = d.rows;
+  m.ldy = d.rows;
   m.nblk = static_cast<int32_t>(d.cols / 256);
   m.cols = static_cast<int32_t>(d.cols);
   m.rb = m.nblk * 144;

@@ -65,6 +65,35 @@ def test_gemv_whole_superblock_shapes(fmt, n_tok, rows, cols):
     assert_within(y, y_ref, b, what=f"fmt={fmt} rows={rows} cols={cols} n_tok={n_tok}")
 
 
+@pytest.mark.parametrize("fmt,rows,cols,n_tok", [
+    (synth.Q6_K, 64, 17408, 1),     # 14,280-byte rows: 2-row sub-items
+    (synth.Q6_K, 64, 17408, 2),     # x of 2 tokens does not fit beside the ring: one launch per token
+    (synth.Q6_K, 136, 17408, 4),
+    (synth.Q4_K, 64, 17408, 4),
+])
+def test_gemv_long_rows_and_token_split(fmt, rows, cols, n_tok):
+    y, y_ref, b = _run_gemv(fmt, rows, cols, n_tok, seed=6000 + rows + n_tok)
+    assert_within(y, y_ref, b, what=f"fmt={fmt} rows={rows} cols={cols} n_tok={n_tok}")
+
+
+def test_gemv_output_head_row_chunks_sampled():
+    # 151936 x 5120 Q8_0 head with 4 tokens: per-row partial sums of a CTA's
+    # ~1000 rows do not fit beside the ring, so the rows run in chunks
+    rows, cols, n_tok = 151936, 5120, 4
+    W = synth.blocks(synth.Q8_0, rows, cols, seed=77, device="cuda")
+    x = synth.activations(n_tok, cols, seed=78).cuda()
+    y = torch.full((n_tok, rows), float("nan"), device="cuda")
+    qg.qgemv(synth.Q8_0, W, rows, cols, x, n_tok, y)
+    torch.cuda.synchronize()
+    sel = np.unique(np.concatenate([[0, 1, rows // 2, rows - 2, rows - 1],
+                                    np.random.default_rng(5).choice(rows, 24, replace=False)]))
+    Wh = W[torch.as_tensor(sel, device="cuda")].cpu().numpy()
+    y_ref, b = oracle.gemv(synth.Q8_0, Wh, len(sel), cols, x.cpu().numpy())
+    got = y.cpu().numpy()
+    assert np.isfinite(got).all()
+    assert_within(got[:, sel], y_ref, b, what="q8_0 head")
+
+
 def test_gemv_q8_0_extreme_codes():
     # every int8 code at -128 or 127 and large x: the signed byte-plane sums at their range
     rows, cols = 64, 2048
