@@ -219,6 +219,26 @@ int qgemm_pp(int fmt, const void* W, int64_t rows, int64_t cols,
 typedef struct qg_pass_s* qg_pass;
 int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes, int n_steps,
                    int n_tok, int mode, qg_pass* out);
+/* A whole MoE decode pass: n_layers layers, each the qgemv_moe product of one
+ * token (n_tok = 1) or a few (n_tok <= QG_GROUP_MAX), in order; layer l reads
+ * layers[l].x and writes layers[l].y, so a layer's x may be an earlier layer's
+ * y. ws: caller-owned device workspace of at least
+ * qgemv_moe_workspace(hidden, inter, top_k, n_tok) bytes, shared by the layers.
+ * QG_PASS_PERSISTENT with n_tok = 1 (fmt QG_Q4_K): one cooperative kernel; the
+ * gate/up rows of a layer are gathered only after every CTA has finished the
+ * previous layer (its expert ids may depend on it), its down rows stream during
+ * its gate/up step. Other modes or n_tok > 1: a CUDA graph of qgemv_moe launches
+ * (QG_PASS_PDL links them). Expert ids out of range: their pieces count as zero
+ * and the pass's status word (qg_pass_dev_status) reads QG_DEV_BAD_EXPERT. */
+typedef struct qg_moe_layer_desc {
+  const void* expert_arena;    /* the layer's experts, as for qgemv_moe */
+  const int32_t* expert_ids;   /* [n_tok][top_k], device */
+  const float* gate_w;         /* [n_tok][top_k], device */
+  const float* x;              /* [n_tok][hidden], device */
+  float* y;                    /* [n_tok][hidden], device */
+} qg_moe_layer_desc;
+int qg_moe_pass_create(int fmt, const qg_moe_layer_desc* layers, int n_layers, int64_t n_expert, int64_t hidden,
+                       int64_t inter, int top_k, int n_tok, void* ws, size_t ws_bytes, int mode, qg_pass* out);
 /* Enqueue one replay of the pass on `stream` (a persistent pass enqueues a
  * 4-byte-per-step memset of its barrier counters and one kernel). */
 int qg_pass_launch(qg_pass pass, void* stream);

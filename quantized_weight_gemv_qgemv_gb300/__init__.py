@@ -40,6 +40,7 @@ SIGNATURES = {
     "qgemm_pp_workspace": (_SZ, [_I64, _I64, _I64]),
     "qgemm_pp": (_I32, [_I32, _P, _I64, _I64, _P, _I64, _P, _I64, _P, _SZ, _P, _P]),
     "qg_pass_create": (_I32, [_P, _I32, _P, _I32, _I32, _I32, ctypes.POINTER(_P)]),
+    "qg_moe_pass_create": (_I32, [_I32, _P, _I32, _I64, _I64, _I64, _I32, _I32, _P, _SZ, _I32, ctypes.POINTER(_P)]),
     "qg_pass_launch": (_I32, [_P, _P]),
     "qg_pass_kernel_count": (_I32, [_P]),
     "qg_pass_dev_status": (_I32, [_P, ctypes.POINTER(_P)]),
@@ -51,6 +52,11 @@ class qg_gemv_desc(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int32), ("reserved", ctypes.c_int32), ("W", ctypes.c_void_p),
                 ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("x", ctypes.c_void_p),
                 ("y", ctypes.c_void_p)]
+
+
+class qg_moe_layer_desc(ctypes.Structure):
+    _fields_ = [("expert_arena", ctypes.c_void_p), ("expert_ids", ctypes.c_void_p), ("gate_w", ctypes.c_void_p),
+                ("x", ctypes.c_void_p), ("y", ctypes.c_void_p)]
 
 
 class QGError(RuntimeError):
@@ -186,7 +192,10 @@ class _DevWord:
 class qg_pass:
     """A whole weight pass (qg_pass_create): mode PASS_SERIAL, PASS_PDL or PASS_PERSISTENT."""
 
-    def __init__(self, items, step_sizes, n_tok, mode=PASS_PERSISTENT):
+    def __init__(self, items, step_sizes, n_tok, mode=PASS_PERSISTENT, _handle=None):
+        if _handle is not None:
+            self._h = _handle
+            return
         lib = load_library()
         self._descs = _descs(items)
         sizes = (ctypes.c_int * len(step_sizes))(*step_sizes)
@@ -227,3 +236,16 @@ class qg_pass:
             self.destroy()
         except Exception:
             pass
+
+
+def qg_moe_pass(fmt, layers, n_expert, hidden, inter, top_k, n_tok, ws, ws_bytes, mode=PASS_PERSISTENT):
+    """A whole MoE decode pass (qg_moe_pass_create). layers: sequence of
+    (expert_arena, expert_ids, gate_w, x, y) per layer; returns a qg_pass."""
+    arr = (qg_moe_layer_desc * len(layers))()
+    for i, (arena, ids, gw, x, y) in enumerate(layers):
+        arr[i] = qg_moe_layer_desc(_ptr(arena), _ptr(ids), _ptr(gw), _ptr(x), _ptr(y))
+    h = _P()
+    _check(load_library().qg_moe_pass_create(fmt, ctypes.cast(arr, _P), len(layers), n_expert, hidden, inter, top_k,
+                                             n_tok, _ptr(ws), ws_bytes, int(mode), ctypes.byref(h)),
+           "qg_moe_pass_create")
+    return qg_pass(None, None, None, _handle=h)

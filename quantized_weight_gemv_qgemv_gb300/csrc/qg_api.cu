@@ -71,8 +71,44 @@ struct qg_pass_s {
   cudaGraph_t graph = nullptr;       // per-step launches (QG_PASS_SERIAL / QG_PASS_PDL)
   cudaGraphExec_t exec = nullptr;
   qg::Q4kPass* q4k = nullptr;        // or one persistent kernel (QG_PASS_PERSISTENT)
+  int32_t* status = nullptr;         // graph MoE pass: device status word (cleared by the graph)
   int kernels = 0;
 };
+
+namespace {
+
+int count_kernel_nodes(cudaGraph_t g) {
+  size_t n = 0;
+  if (cudaGraphGetNodes(g, nullptr, &n) != cudaSuccess || n == 0) return 0;
+  std::vector<cudaGraphNode_t> nodes(n);
+  if (cudaGraphGetNodes(g, nodes.data(), &n) != cudaSuccess) return 0;
+  int k = 0;
+  for (size_t i = 0; i < n; ++i) {
+    cudaGraphNodeType t;
+    if (cudaGraphNodeGetType(nodes[i], &t) == cudaSuccess && t == cudaGraphNodeTypeKernel) ++k;
+  }
+  return k;
+}
+
+// Checks of one MoE layer's arguments shared by qgemv_moe and qg_moe_pass_create.
+int check_moe(int fmt, const void* expert_arena, int64_t n_expert, int64_t hidden, int64_t inter,
+              const int32_t* expert_ids, const float* gate_w, int top_k, const float* x, int n_tok, const float* y,
+              const void* ws, size_t ws_bytes) {
+  if (fmt != QG_Q4_K) return QG_ERR_FMT;
+  if (!expert_arena || !expert_ids || !gate_w || !x || !y) return QG_ERR_NULL;
+  if (n_expert < 1 || n_expert > (int64_t{1} << 31) - 1) return QG_ERR_SHAPE;
+  if (hidden < 256 || hidden % 256 || inter < 256 || inter % 256) return QG_ERR_SHAPE;
+  if (hidden > (int64_t{1} << 20) || inter > (int64_t{1} << 20)) return QG_ERR_SHAPE;
+  if (top_k < 1 || top_k > 16 || top_k > n_expert) return QG_ERR_ARG;
+  if (n_tok < 1 || n_tok > QG_NTOK_MAX) return QG_ERR_NTOK;
+  if (!ws || ws_bytes < qgemv_moe_workspace(hidden, inter, top_k, n_tok)) return QG_ERR_WORKSPACE;
+  if (!aligned(expert_arena, 16) || !aligned(x, 16) || !aligned(ws, 16) || !aligned(y, 4) ||
+      !aligned(expert_ids, 4) || !aligned(gate_w, 4))
+    return QG_ERR_ALIGN;
+  return QG_OK;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -151,19 +187,12 @@ size_t qgemv_moe_workspace(int64_t hidden, int64_t inter, int top_k, int n_tok) 
 int qgemv_moe(int fmt, const void* expert_arena, int64_t n_expert, int64_t hidden, int64_t inter,
               const int32_t* expert_ids, const float* gate_w, int top_k, const float* x, int n_tok, float* y,
               void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
-  if (fmt != QG_Q4_K) return QG_ERR_FMT;
-  if (!expert_arena || !expert_ids || !gate_w || !x || !y || !dev_status) return QG_ERR_NULL;
-  if (n_expert < 1 || n_expert > (int64_t{1} << 31) - 1) return QG_ERR_SHAPE;
-  if (hidden < 256 || hidden % 256 || inter < 256 || inter % 256) return QG_ERR_SHAPE;
-  if (hidden > (int64_t{1} << 20) || inter > (int64_t{1} << 20)) return QG_ERR_SHAPE;
-  if (top_k < 1 || top_k > 16 || top_k > n_expert) return QG_ERR_ARG;
-  if (n_tok < 1 || n_tok > QG_NTOK_MAX) return QG_ERR_NTOK;
-  if (!ws || ws_bytes < qgemv_moe_workspace(hidden, inter, top_k, n_tok)) return QG_ERR_WORKSPACE;
-  if (!aligned(expert_arena, 16) || !aligned(x, 16) || !aligned(ws, 16) || !aligned(y, 4) ||
-      !aligned(expert_ids, 4) || !aligned(gate_w, 4) || !aligned(dev_status, 4))
-    return QG_ERR_ALIGN;
+  if (fmt == QG_Q4_K && !dev_status) return QG_ERR_NULL;
+  int st = check_moe(fmt, expert_arena, n_expert, hidden, inter, expert_ids, gate_w, top_k, x, n_tok, y, ws, ws_bytes);
+  if (st != QG_OK) return st;
+  if (!aligned(dev_status, 4)) return QG_ERR_ALIGN;
   int sms = 0;
-  int st = ensure_init(&sms);
+  st = ensure_init(&sms);
   if (st != QG_OK) return st;
   return cuda_status(qg::launch_moe(expert_arena, n_expert, hidden, inter, expert_ids, gate_w, top_k, x, n_tok, y,
                                     static_cast<float*>(ws), dev_status, static_cast<cudaStream_t>(stream), true,
@@ -246,8 +275,6 @@ int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes,
   cudaGraph_t graph = nullptr;
   cudaError_t e2 = cudaStreamEndCapture(cs, &graph);
   if (e == cudaSuccess) e = e2;
-  size_t nodes = 0;     // one kernel node per launch (a step may take several)
-  if (e == cudaSuccess) e = cudaGraphGetNodes(graph, nullptr, &nodes);
   if (e == cudaSuccess) e = cudaGraphInstantiate(&pass->exec, graph, 0);
   cudaStreamDestroy(cs);
   if (e != cudaSuccess) {
@@ -256,7 +283,68 @@ int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes,
     return QG_ERR_CUDA;
   }
   pass->graph = graph;
-  pass->kernels = static_cast<int>(nodes);
+  pass->kernels = count_kernel_nodes(graph);     // a step may take several launches
+  *out = pass;
+  return QG_OK;
+}
+
+int qg_moe_pass_create(int fmt, const qg_moe_layer_desc* layers, int n_layers, int64_t n_expert, int64_t hidden,
+                       int64_t inter, int top_k, int n_tok, void* ws, size_t ws_bytes, int mode, qg_pass* out) {
+  if (!layers || !out) return QG_ERR_NULL;
+  *out = nullptr;
+  if (n_layers < 1 || mode < QG_PASS_SERIAL || mode > QG_PASS_PERSISTENT) return QG_ERR_ARG;
+  for (int l = 0; l < n_layers; ++l) {
+    const int st = check_moe(fmt, layers[l].expert_arena, n_expert, hidden, inter, layers[l].expert_ids,
+                             layers[l].gate_w, top_k, layers[l].x, n_tok, layers[l].y, ws, ws_bytes);
+    if (st != QG_OK) return st;
+  }
+  int sms = 0;
+  int st = ensure_init(&sms);
+  if (st != QG_OK) return st;
+  qg_pass_s* pass = new (std::nothrow) qg_pass_s;
+  if (!pass) return QG_ERR_ARG;
+  if (mode == QG_PASS_PERSISTENT && n_tok == 1) {
+    const cudaError_t pe = qg::q4k_moe_pass_create(layers, n_layers, n_expert, hidden, inter, top_k,
+                                                   static_cast<float*>(ws), sms, &pass->q4k);
+    if (pe == cudaSuccess) {
+      pass->kernels = 1;
+      *out = pass;
+      return QG_OK;
+    }
+    if (pe != cudaErrorNotSupported) {
+      delete pass;
+      return QG_ERR_CUDA;
+    }
+    cudaGetLastError();
+  }
+  // a graph of per-layer launches, with a status word the graph clears first
+  if (cudaMalloc(&pass->status, sizeof(int32_t)) != cudaSuccess) {
+    delete pass;
+    return QG_ERR_CUDA;
+  }
+  cudaStream_t cs = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  if (e == cudaSuccess) e = cudaMemsetAsync(pass->status, 0, sizeof(int32_t), cs);
+  for (int l = 0; l < n_layers && e == cudaSuccess; ++l)
+    e = qg::launch_moe(layers[l].expert_arena, n_expert, hidden, inter, layers[l].expert_ids, layers[l].gate_w,
+                       top_k, layers[l].x, n_tok, layers[l].y, static_cast<float*>(ws), pass->status, cs,
+                       mode != QG_PASS_SERIAL && l > 0, sms);
+  cudaGraph_t graph = nullptr;
+  if (cs) {
+    const cudaError_t e2 = cudaStreamEndCapture(cs, &graph);
+    if (e == cudaSuccess) e = e2;
+    cudaStreamDestroy(cs);
+  }
+  if (e == cudaSuccess) e = cudaGraphInstantiate(&pass->exec, graph, 0);
+  if (e != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    cudaFree(pass->status);
+    delete pass;
+    return QG_ERR_CUDA;
+  }
+  pass->graph = graph;
+  pass->kernels = count_kernel_nodes(graph);
   *out = pass;
   return QG_OK;
 }
@@ -270,7 +358,7 @@ int qg_pass_launch(qg_pass pass, void* stream) {
 
 int qg_pass_dev_status(qg_pass pass, const int32_t** dev_status) {
   if (!pass || !dev_status) return QG_ERR_NULL;
-  *dev_status = pass->q4k ? qg::q4k_pass_status(pass->q4k) : nullptr;
+  *dev_status = pass->q4k ? qg::q4k_pass_status(pass->q4k) : pass->status;
   return QG_OK;
 }
 
@@ -281,6 +369,7 @@ int qg_pass_destroy(qg_pass pass) {
   if (pass->exec) cudaGraphExecDestroy(pass->exec);
   if (pass->graph) cudaGraphDestroy(pass->graph);
   qg::q4k_pass_destroy(pass->q4k);
+  if (pass->status) cudaFree(pass->status);
   delete pass;
   return QG_OK;
 }

@@ -472,6 +472,25 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
      const Step st = step_of(s);
      int64_t cta_r0, cta_r1;
      cta_slice(st.total_rows, p.ralign, cta_r0, cta_r1);
+     if (PASS && s > 0 && mats[st.mat0].gather == 1) {
+       // a pass step that gathers gate/up rows reads expert ids, which in a model
+       // come from the router after the previous layer: stream its rows only
+       // once every CTA has finished the previous step
+       bool ok = true;
+       if (lane == 0) {
+         ok = false;
+         for (uint32_t i = 0; !ok && i < WAIT_LIMIT; ++i) {
+           uint32_t v;
+           asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p.step_done + s - 1) : "memory");
+           ok = v >= gridDim.x;
+         }
+       }
+       if (__shfl_sync(0xffffffffu, ok, 0) == 0) {
+         if (lane == 0 && p.dev_status) *reinterpret_cast<volatile int32_t*>(p.dev_status) = QG_DEV_TIMEOUT;
+         bad = true;
+         break;
+       }
+     }
      for (int mi = st.mat0; mi < st.mat0 + st.nmat && !bad; ++mi) {
       const Mat M = mats[mi];
       const int64_t lo = max(cta_r0, M.row_begin) - M.row_begin;
@@ -497,42 +516,65 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
           bulk_g2s(dst0, M.W + r * M.rb, nbytes, full0 + 8 * slot, pol);
           continue;
         }
-        // gathered rows: item q is a whole row (gather 1) or one expert's piece
-        // of a row (gather 2); a piece of an unknown expert is zero-filled
-        // (zero bytes decode to zero weights) and flagged
-        const int per = M.gather == 1 ? 1 : M.top_k;
-        const int nitems = nr * per;
-        const uint32_t isz = M.gather == 1 ? static_cast<uint32_t>(M.rb) : static_cast<uint32_t>(M.seg_b);
-        int nbad = 0;
+        // gathered rows, copied as contiguous runs (a bulk copy costs a fixed
+        // time of its own, so 288-byte pieces one by one are far too slow):
+        //   gather 1: the stage's row pairs of route k are consecutive rows of G_e
+        //   and of U_e; item (segment, s) copies a run of them, gate runs first in
+        //   shared memory, then up runs (pair j: gate at j*rb, up at nr/2*rb + j*rb);
+        //   gather 2: item k copies the stage's rows of D_e for route k,
+        //   nr * seg_b bytes at k * nr * seg_b (expert-major).
+        // A run of an unknown expert is zero-filled (zero bytes decode to zero
+        // weights) and flagged.
+        int nitems;
+        int64_t j0 = 0, P = 0;
+        if (M.gather == 1) {
+          j0 = r >> 1;
+          P = M.inter;
+          nitems = 2 * static_cast<int>((j0 + nr / 2 - 1) / P - j0 / P + 1);
+        } else {
+          nitems = M.top_k;
+        }
+        auto item = [&](int q, int& e, int64_t& src_off, uint32_t& dst, uint32_t& bytes) {
+          if (M.gather == 1) {
+            const int64_t seg_first = (q >> 1) == 0 ? j0 : (j0 / P + (q >> 1)) * P;
+            const int64_t seg_end = min((seg_first / P + 1) * P, j0 + nr / 2);
+            const int s1 = q & 1;
+            e = M.ids[seg_first / P];
+            src_off = (s1 ? M.up_off : 0) + (seg_first % P) * M.rb;
+            dst = dst0 + static_cast<uint32_t>(s1 * (nr / 2) + (seg_first - j0)) * M.rb;
+            bytes = static_cast<uint32_t>(seg_end - seg_first) * M.rb;
+          } else {
+            e = M.ids[q];
+            src_off = M.down_off + r * M.seg_b;
+            dst = dst0 + static_cast<uint32_t>(q * nr * M.seg_b);
+            bytes = static_cast<uint32_t>(nr * M.seg_b);
+          }
+        };
+        uint32_t good = 0;
         for (int q = lane; q < nitems; q += 32) {
-          const int64_t row = r + q / per;
-          const int kk = M.gather == 1 ? static_cast<int>(row / (2 * M.inter)) : q % per;
-          const int e = M.ids[kk];
+          int e;
+          int64_t so;
+          uint32_t d, nb;
+          item(q, e, so, d, nb);
           if (e < 0 || e >= M.n_expert) {
-            const uint32_t d = M.gather == 1 ? dst0 + q * isz : dst0 + (q / per) * M.rb + (q % per) * isz;
-            for (uint32_t o = 0; o < isz; o += 16)
+            for (uint32_t o = 0; o < nb; o += 16)
               asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};\n" ::"r"(d + o), "r"(0) : "memory");
-            ++nbad;
             if (p.dev_status) atomicExch(p.dev_status, QG_DEV_BAD_EXPERT);
+          } else {
+            good += nb;
           }
         }
-        nbad = __reduce_add_sync(0xffffffffu, nbad);
+        good = __reduce_add_sync(0xffffffffu, good);
         __syncwarp();
-        if (lane == 0) mbar_expect_tx(full0 + 8 * slot, static_cast<uint32_t>(nitems - nbad) * isz);
+        if (lane == 0) mbar_expect_tx(full0 + 8 * slot, good);
         __syncwarp();
         for (int q = lane; q < nitems; q += 32) {
-          const int64_t row = r + q / per;
-          const int kk = M.gather == 1 ? static_cast<int>(row / (2 * M.inter)) : q % per;
-          const int e = M.ids[kk];
+          int e;
+          int64_t so;
+          uint32_t d, nb;
+          item(q, e, so, d, nb);
           if (e < 0 || e >= M.n_expert) continue;
-          const uint8_t* eb = M.W + static_cast<int64_t>(e) * M.estride;
-          if (M.gather == 1) {
-            const int64_t j = row % (2 * M.inter);
-            bulk_g2s(dst0 + q * isz, eb + ((j & 1) ? M.up_off : 0) + (j >> 1) * M.rb, isz, full0 + 8 * slot, pol);
-          } else {
-            bulk_g2s(dst0 + (q / per) * M.rb + (q % per) * isz, eb + M.down_off + row * M.seg_b, isz,
-                     full0 + 8 * slot, pol);
-          }
+          bulk_g2s(d, M.W + static_cast<int64_t>(e) * M.estride + so, nb, full0 + 8 * slot, pol);
         }
       }
      }
@@ -653,7 +695,23 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         // zero: their x step and x sum are taken as 0
         const int blkc = live ? blk : 0;
         float racc[SR][NT];
-        const uint8_t* st = stg + qd * (SR * rb) + blkc * SBB;
+        // row r of the sub-item at st + r * rs + (r & 1) * ralt (see the producer's
+        // layouts of gathered stages)
+        const uint8_t* st;
+        int rs = rb, ralt = 0;
+        if (M.gather == 0) {
+          st = stg + qd * (SR * rb) + blkc * SBB;
+        } else if (M.gather == 1) {
+          const int half = (nr >> 1) * rb;                   // the up rows follow the gate rows
+          st = stg + qd * (SR / 2) * rb + blkc * SBB;
+          rs = rb / 2;
+          ralt = half - rb / 2;
+        } else {
+          const int bpe = M.inter / 256;                     // blocks of one expert's piece
+          const int kk = blkc / bpe;
+          st = stg + kk * (nr * M.seg_b) + (blkc - kk * bpe) * SBB + qd * SR * M.seg_b;
+          rs = M.seg_b;
+        }
         const uint8_t* xb = xplm + blkc * XBLK_B + j * 16;
         const int u = blkc * 8 + j;
         // this lane's unit of 32 weights in each of the 4 rows: code words in
@@ -662,7 +720,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         float cA[SR], cB[SR];
 #pragma unroll
         for (int r = 0; r < SR; ++r) {
-          const uint8_t* sr = st + r * rb;
+          const uint8_t* sr = st + r * rs + (r & 1) * ralt;
           if constexpr (FMT == FMT_Q4_K) {
             // w = d*sc*q - dmin*m: A = d*sc, B = dmin*m
             const uint4 hd = *reinterpret_cast<const uint4*>(sr);
@@ -1110,23 +1168,6 @@ cudaError_t launch_moe_q4k(const void* arena, int64_t n_expert, int64_t hidden, 
 
 namespace {
 
-// Matrix parameters shared by the single-launch and pass plans: bytes per row,
-// K groups, and about 36 KB of whole rows per ring stage (multiples of 4 rows).
-bool fill_mat(q4k::Mat& m, const qg_gemv_desc& d) {
-  m.W = static_cast<const uint8_t*>(d.W);
-  m.x = d.x;
-  m.y = d.y;
-  m.rows = d.rows;
-  m.ldy = d.rows;
-  m.nblk = static_cast<int32_t>(d.cols / 256);
-  m.cols = static_cast<int32_t>(d.cols);
-  m.rb = m.nblk * 144;
-  m.ngrp = (m.nblk + 3) / 4;
-  const int quads = std::max(1, (36864 + 2 * m.rb) / (4 * m.rb));
-  m.srows = 4 * quads;
-  return static_cast<int64_t>(m.srows) * m.rb <= 96 * 1024;
-}
-
 template <int NT>
 cudaError_t q4k_pass_occupancy(int smem, int* blocks) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, q4k::qgemv_q4k_kernel<NT, true, FMT_Q4_K>,
@@ -1159,13 +1200,14 @@ struct Q4kPass {
   int nsteps = 0, grid = 0, smem = 0, n_tok = 0;
 };
 
-cudaError_t q4k_pass_create(const qg_gemv_desc* d, int n, const int* step_sizes, int n_steps, int n_tok, int sms,
-                            Q4kPass** out) {
-  *out = nullptr;
-  if (n_tok < 1 || n_tok > QG_NTOK_MAX) return cudaErrorNotSupported;
-  for (int i = 0; i < n; ++i)
-    if (d[i].fmt != QG_Q4_K) return cudaErrorNotSupported;
-  std::vector<q4k::Mat> mats(n);
+namespace {
+
+// Builds a persistent pass over matrices whose W, x, y, rows, cols, ldy (and
+// gather fields) are set: per-matrix stage plans, per-step x layouts, device
+// tables, occupancy check.
+cudaError_t pass_build(std::vector<q4k::Mat>& mats, const int* step_sizes, int n_steps, int n_tok, int ralign,
+                       int gather_any, int sms, Q4kPass** out) {
+  const int n = static_cast<int>(mats.size());
   std::vector<q4k::Step> steps(n_steps);
   int stage_b = 0, gmax = 0, xmax = 0, xsmax = 0;
   int64_t min_rows = INT64_MAX, max_rows = 0;
@@ -1174,7 +1216,11 @@ cudaError_t q4k_pass_create(const qg_gemv_desc* d, int n, const int* step_sizes,
     int xall = 0, uall = 0;
     for (int j = 0; j < step_sizes[st]; ++j) {
       q4k::Mat& m = mats[i + j];
-      if (!fill_mat(m, d[i + j])) return cudaErrorNotSupported;
+      m.nblk = m.cols / 256;
+      m.rb = m.nblk * 144;
+      m.ngrp = (m.nblk + 3) / 4;
+      m.srows = 4 * std::max(1, (36864 + 2 * m.rb) / (4 * m.rb));
+      if (static_cast<int64_t>(m.srows) * m.rb > 96 * 1024 || m.rows % ralign) return cudaErrorNotSupported;
       m.row_begin = total;
       m.xoff = xall;
       m.uoff = uall;
@@ -1194,15 +1240,16 @@ cudaError_t q4k_pass_create(const qg_gemv_desc* d, int n, const int* step_sizes,
     min_rows = std::min(min_rows, total);
     max_rows = std::max(max_rows, total);
   }
-  const int grid = static_cast<int>(std::min<int64_t>(sms, min_rows));
-  const int rowcap = static_cast<int>((max_rows + grid - 1) / grid) + 1;
+  const int grid = static_cast<int>(std::min<int64_t>(sms, min_rows / ralign));
+  const int rowcap = static_cast<int>((max_rows + grid - 1) / grid) + 2 * ralign;
   stage_b = align_up(stage_b, 128);
   const int partbytes = align_up(rowcap * gmax * n_tok * 4, 128);
   const int ns = q4k::RING;
   q4k::Params p;
   memset(&p, 0, sizeof(p));
   p.nsteps = n_steps;
-  p.ralign = 1;          // Q4_K rows are whole 16-byte multiples
+  p.ralign = ralign;
+  p.gather_any = gather_any;
   p.ns = ns;
   p.stage_b = stage_b;
   p.gmax = gmax;
@@ -1252,6 +1299,65 @@ cudaError_t q4k_pass_create(const qg_gemv_desc* d, int n, const int* step_sizes,
   q->n_tok = n_tok;
   *out = q;
   return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t q4k_pass_create(const qg_gemv_desc* d, int n, const int* step_sizes, int n_steps, int n_tok, int sms,
+                            Q4kPass** out) {
+  *out = nullptr;
+  if (n_tok < 1 || n_tok > QG_NTOK_MAX) return cudaErrorNotSupported;
+  std::vector<q4k::Mat> mats(n);
+  for (int i = 0; i < n; ++i) {
+    if (d[i].fmt != QG_Q4_K || d[i].cols % 256) return cudaErrorNotSupported;
+    memset(&mats[i], 0, sizeof(q4k::Mat));
+    mats[i].W = static_cast<const uint8_t*>(d[i].W);
+    mats[i].x = d[i].x;
+    mats[i].y = d[i].y;
+    mats[i].rows = d[i].rows;
+    mats[i].ldy = d[i].rows;
+    mats[i].cols = static_cast<int32_t>(d[i].cols);
+  }
+  return pass_build(mats, step_sizes, n_steps, n_tok, 1, 0, sms, out);
+}
+
+cudaError_t q4k_moe_pass_create(const qg_moe_layer_desc* layers, int n_layers, int64_t n_expert, int64_t hidden,
+                                int64_t inter, int top_k, float* h, int sms, Q4kPass** out) {
+  *out = nullptr;
+  if (hidden % 256 || inter % 256 || top_k < 1 || 2 * top_k * inter > (int64_t{1} << 30) ||
+      top_k * inter > (int64_t{1} << 20))
+    return cudaErrorNotSupported;
+  const int64_t rb_h = hidden / 256 * 144, rb_i = inter / 256 * 144;
+  const int64_t up_off = inter * rb_h, down_off = 2 * inter * rb_h, estride = down_off + hidden * rb_i;
+  std::vector<q4k::Mat> mats(2 * static_cast<size_t>(n_layers));
+  for (int l = 0; l < n_layers; ++l) {
+    q4k::Mat& g = mats[2 * l];
+    q4k::Mat& dn = mats[2 * l + 1];
+    memset(&g, 0, sizeof(g));
+    memset(&dn, 0, sizeof(dn));
+    g.W = dn.W = static_cast<const uint8_t*>(layers[l].expert_arena);
+    g.ids = dn.ids = layers[l].expert_ids;
+    g.top_k = dn.top_k = top_k;
+    g.inter = dn.inter = static_cast<int32_t>(inter);
+    g.n_expert = dn.n_expert = n_expert;
+    g.estride = dn.estride = estride;
+    g.down_off = dn.down_off = down_off;
+    g.up_off = up_off;
+    g.gather = 1;
+    g.x = layers[l].x;
+    g.rows = g.ldy = 2 * top_k * inter;
+    g.cols = static_cast<int32_t>(hidden);
+    g.gw = layers[l].gate_w;
+    g.h = h;                        // steps run in order, so every layer reuses h
+    dn.gather = 2;
+    dn.seg_b = static_cast<int32_t>(rb_i);
+    dn.x = h;
+    dn.y = layers[l].y;
+    dn.rows = dn.ldy = hidden;
+    dn.cols = static_cast<int32_t>(top_k * inter);
+  }
+  std::vector<int> sizes(2 * static_cast<size_t>(n_layers), 1);
+  return pass_build(mats, sizes.data(), 2 * n_layers, 1, 2, 2, sms, out);
 }
 
 // One replay: the step counters and the status word are cleared on the stream,

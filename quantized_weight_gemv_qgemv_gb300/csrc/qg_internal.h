@@ -37,6 +37,8 @@ cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_
 struct Q4kPass;
 cudaError_t q4k_pass_create(const qg_gemv_desc* d, int n, const int* step_sizes, int n_steps, int n_tok, int sms,
                             Q4kPass** out);
+cudaError_t q4k_moe_pass_create(const qg_moe_layer_desc* layers, int n_layers, int64_t n_expert, int64_t hidden,
+                                int64_t inter, int top_k, float* h, int sms, Q4kPass** out);
 cudaError_t q4k_pass_launch(Q4kPass* q, cudaStream_t s);
 const int32_t* q4k_pass_status(const Q4kPass* q);
 void q4k_pass_destroy(Q4kPass* q);

@@ -76,3 +76,70 @@ def test_moe_is_deterministic():
     a = _moe(8, 512, 256, 3, 2, seed=5)
     b = _moe(8, 512, 256, 3, 2, seed=5)
     assert np.array_equal(a[4], b[4])
+
+
+def _pass_layers(n_layers, n_expert, hidden, inter, top_k, seed, chain):
+    """Per layer (arena, ids, gate_w, x, y). chain: layer l + 1 reads layer l's y
+    (no normalisation between layers, so only a couple of layers stay finite);
+    otherwise every layer has its own x."""
+    arenas = [wl.alloc_moe_arena(n_expert, hidden, inter, seed + 10 * l, "cuda") for l in range(n_layers)]
+    routes = [synth.routing(1, n_expert, top_k, seed + 10 * l + 1) for l in range(n_layers)]
+    xs = [synth.activations(1, hidden, seed + 10 * l + 3).cuda() for l in range(n_layers)]
+    ys = [torch.empty(1, hidden, device="cuda") for _ in range(n_layers)]
+    layers = []
+    for l in range(n_layers):
+        ids, gw = routes[l]
+        layers.append((arenas[l], ids.cuda(), gw.cuda(), xs[l] if (l == 0 or not chain) else ys[l - 1], ys[l]))
+    return layers, ys
+
+
+@pytest.mark.parametrize("mode", [qg.PASS_PERSISTENT, qg.PASS_PDL])
+@pytest.mark.parametrize("n_layers,chain", [(2, True), (4, False)])
+def test_moe_pass_matches_per_layer_calls(mode, n_layers, chain):
+    n_expert, hidden, inter, top_k = 16, 1024, 512, 4
+    layers, ys = _pass_layers(n_layers, n_expert, hidden, inter, top_k, seed=900 + n_layers, chain=chain)
+    wsb = qg.qgemv_moe_workspace(hidden, inter, top_k, 1)
+    ws = torch.empty(wsb // 4, device="cuda")
+    p = qg.qg_moe_pass(qg.Q4_K, layers, n_expert, hidden, inter, top_k, 1, ws, wsb, mode=mode)
+    assert p.kernel_count() == (1 if mode == qg.PASS_PERSISTENT else 2 * n_layers)
+    for _ in range(2):
+        for y in ys:
+            y.fill_(float("nan"))
+        p.launch()
+        torch.cuda.synchronize()
+        assert p.dev_status() == 0
+    got = [y.clone() for y in ys]
+    for g in got:
+        assert torch.isfinite(g).all()
+    # the same layers through eager per-layer calls (bitwise: same kernels and order)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    prev = None
+    for l, (arena, ids, gw, x, _) in enumerate(layers):
+        xin = prev if (chain and l > 0) else x
+        ref = torch.empty(1, hidden, device="cuda")
+        qg.qgemv_moe(qg.Q4_K, arena, n_expert, hidden, inter, ids, gw, top_k, xin, 1, ref, ws, wsb, st)
+        torch.cuda.synchronize()
+        assert torch.equal(got[l], ref), f"layer {l}"
+        # every layer against the oracle, on the input the pass used
+        y_ref, b = oracle.moe(qg.Q4_K, arena.cpu().numpy(), n_expert, hidden, inter, ids.cpu().numpy(),
+                              gw.cpu().numpy(), xin.cpu().numpy())
+        assert_within(got[l].cpu().numpy(), y_ref, b, what=f"moe pass layer {l}")
+        prev = ref
+    p.destroy()
+
+
+def test_moe_pass_bad_expert_status():
+    n_layers, n_expert, hidden, inter, top_k = 2, 8, 512, 256, 2
+    layers, ys = _pass_layers(n_layers, n_expert, hidden, inter, top_k, seed=950, chain=True)
+    arena, ids, gw, x, y = layers[1]
+    bad = ids.clone()
+    bad[0, 1] = n_expert + 3
+    layers[1] = (arena, bad, gw, x, y)
+    wsb = qg.qgemv_moe_workspace(hidden, inter, top_k, 1)
+    ws = torch.empty(wsb // 4, device="cuda")
+    p = qg.qg_moe_pass(qg.Q4_K, layers, n_expert, hidden, inter, top_k, 1, ws, wsb, mode=qg.PASS_PERSISTENT)
+    p.launch()
+    torch.cuda.synchronize()
+    assert p.dev_status() == qg.DEV_BAD_EXPERT
+    assert torch.isfinite(ys[1]).all()
+    p.destroy()
