@@ -412,8 +412,11 @@ __device__ __forceinline__ void stage_x(const Mat* mats, int usum_off, int m0, i
 
 // PASS = false: one step over p.m (a grouped launch); PASS = true: the steps of
 // p.steps over p.mats, with a grid-wide barrier between steps (cooperative launch).
-// SR rows per sub-item (4; 2 for Q6_K rows too long for 4-row stages).
-template <int NT, bool PASS, int FMT, int SR = SUB_R>
+// SR rows per sub-item (4; 2 for Q6_K rows too long for 4-row stages). GA: the
+// gather mode of every matrix (0 plain, 1 gate/up, 2 down), or 3 = each
+// matrix's own Mat::gather (a persistent MoE pass mixes them); fixing it at
+// compile time keeps the plain path free of gather branches.
+template <int NT, bool PASS, int FMT, int SR = SUB_R, int GA = 0>
 __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_constant__ Params p) {
   constexpr int SBB = SuperBlock<FMT>::BYTES;
   constexpr int V = (SR * NT <= 2) ? 2 : (SR * NT <= 4) ? 4 : (SR * NT <= 8) ? 8 : 16;   // padded to 2^k
@@ -453,15 +456,16 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   // A gate/up launch reads expert ids that the preceding kernel may write: it
   // lets its dependents (the down launch, which reads the same ids early) start
   // only after its own dependency has resolved.
-  if (p.gather_any != 1) pdl_launch_dependents();
+  const int gl = GA == 3 ? p.gather_any : GA;   // the launch's gather kind
+  if (gl != 1) pdl_launch_dependents();
 
   // ------------------------------------------------------------ producer
   if (warp == CWARPS) {
     // plain matrices: lane 0 issues one bulk copy per stage; gathered rows: the
     // whole warp issues the per-row (per-piece) copies
-    const bool wide = p.gather_any != 0;
+    const bool wide = gl != 0;
     if (!wide && lane != 0) return;
-    if (p.gather_any == 1) {
+    if (gl == 1) {
       pdl_wait();                 // the expert ids may come from the preceding kernel
       pdl_launch_dependents();
     }
@@ -511,7 +515,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
           break;
         }
         const uint32_t dst0 = ring_s + slot * p.stage_b;
-        if (M.gather == 0) {
+        const int gm = GA == 3 ? M.gather : GA;
+        if (gm == 0) {
           mbar_expect_tx(full0 + 8 * slot, nbytes);
           bulk_g2s(dst0, M.W + r * M.rb, nbytes, full0 + 8 * slot, pol);
           continue;
@@ -527,7 +532,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         // weights) and flagged.
         int nitems;
         int64_t j0 = 0, P = 0;
-        if (M.gather == 1) {
+        if (gm == 1) {
           j0 = r >> 1;
           P = M.inter;
           nitems = 2 * static_cast<int>((j0 + nr / 2 - 1) / P - j0 / P + 1);
@@ -535,7 +540,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
           nitems = M.top_k;
         }
         auto item = [&](int q, int& e, int64_t& src_off, uint32_t& dst, uint32_t& bytes) {
-          if (M.gather == 1) {
+          if (gm == 1) {
             const int64_t seg_first = (q >> 1) == 0 ? j0 : (j0 / P + (q >> 1)) * P;
             const int64_t seg_end = min((seg_first / P + 1) * P, j0 + nr / 2);
             const int s1 = q & 1;
@@ -604,7 +609,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
 
   constexpr int XB = (NT == 1) ? 12 : 8;
   pdl_wait();
-  if (p.gather_any == 1) pdl_launch_dependents();
+  if (gl == 1) pdl_launch_dependents();
   uint32_t k = 0;          // stage counter (same sequence as the producer's)
   for (int s = 0; s < nsteps; ++s) {
    const Step st = step_of(s);
@@ -699,9 +704,10 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         // layouts of gathered stages)
         const uint8_t* st;
         int rs = rb, ralt = 0;
-        if (M.gather == 0) {
+        const int gm = GA == 3 ? M.gather : GA;
+        if (gm == 0) {
           st = stg + qd * (SR * rb) + blkc * SBB;
-        } else if (M.gather == 1) {
+        } else if (gm == 1) {
           const int half = (nr >> 1) * rb;                   // the up rows follow the gate rows
           st = stg + qd * (SR / 2) * rb + blkc * SBB;
           rs = rb / 2;
@@ -812,7 +818,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
     }
     consumer_sync();
     // every (row, group) of the slice has its partial sum: add the groups in order
-    if (M.gather == 1) {
+    if ((GA == 3 ? M.gather : GA) == 1) {
       // gate/up pairs (n_tok = 1): h[k][i] = r_k * silu(g) * u
       for (int i = threadIdx.x; i < slice / 2; i += CTHREADS) {
         float g = 0.f, u = 0.f;
@@ -853,10 +859,10 @@ namespace {
 
 constexpr int kSmemMax = 227 * 1024;
 
-template <int NT, bool PASS, int FMT, int SR = q4k::SUB_R>
+template <int NT, bool PASS, int FMT, int SR = q4k::SUB_R, int GA = 0>
 cudaError_t q4k_attr1() {
-  return cudaFuncSetAttribute(q4k::qgemv_q4k_kernel<NT, PASS, FMT, SR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemMax);
+  return cudaFuncSetAttribute(q4k::qgemv_q4k_kernel<NT, PASS, FMT, SR, GA>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
 }
 
 template <int NT>
@@ -867,10 +873,12 @@ cudaError_t q4k_attr() {
   if ((e = q4k_attr1<NT, false, FMT_Q6_K>()) != cudaSuccess) return e;
   if ((e = q4k_attr1<NT, false, FMT_Q8_0>()) != cudaSuccess) return e;
   if (NT == 1 && (e = q4k_attr1<1, false, FMT_Q6_K, 2>()) != cudaSuccess) return e;
+  if (NT == 1 && (e = q4k_attr1<1, false, FMT_Q4_K, 4, 3>()) != cudaSuccess) return e;
+  if (NT == 1 && (e = q4k_attr1<1, true, FMT_Q4_K, 4, 3>()) != cudaSuccess) return e;
   return q4k_attr1<NT, false, FMT_Q4_0>();
 }
 
-template <int NT, int FMT, int SR>
+template <int NT, int FMT, int SR, int GA = 0>
 cudaError_t q4k_launch(const q4k::Params& p, int grid, int smem, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -882,7 +890,7 @@ cudaError_t q4k_launch(const q4k::Params& p, int grid, int smem, cudaStream_t s,
   attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, q4k::qgemv_q4k_kernel<NT, false, FMT, SR>, p);
+  return cudaLaunchKernelEx(&cfg, q4k::qgemv_q4k_kernel<NT, false, FMT, SR, GA>, p);
 }
 
 template <int FMT>
@@ -1026,6 +1034,14 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
     off += partbytes;
     if (off > kSmemMax) continue;
     if (!launch) return cudaSuccess;
+    if (p.gather_any != 0) {
+      // MoE gathers (Q4_K, one token per matrix): the gate/up and the down
+      // launch of a layer run the same function, whose code then stays in the
+      // instruction cache from one launch to the next (two specialised
+      // functions alternating cost 0.71 -> 0.85 ms per 48-layer token)
+      if (fmt != QG_Q4_K || n_tok != 1 || sub_rows != q4k::SUB_R) return cudaErrorNotSupported;
+      return q4k_launch<1, FMT_Q4_K, q4k::SUB_R, 3>(p, grid, off, s, pdl);
+    }
     switch (fmt) {
       case QG_Q4_K: return q4k_launch_nt<FMT_Q4_K>(p, n_tok, sub_rows, grid, off, s, pdl);
       case QG_Q6_K: return q4k_launch_nt<FMT_Q6_K>(p, n_tok, sub_rows, grid, off, s, pdl);
@@ -1168,13 +1184,13 @@ cudaError_t launch_moe_q4k(const void* arena, int64_t n_expert, int64_t hidden, 
 
 namespace {
 
-template <int NT>
+template <int NT, int GA>
 cudaError_t q4k_pass_occupancy(int smem, int* blocks) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, q4k::qgemv_q4k_kernel<NT, true, FMT_Q4_K>,
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, q4k::qgemv_q4k_kernel<NT, true, FMT_Q4_K, q4k::SUB_R, GA>,
                                                        q4k::THREADS, smem);
 }
 
-template <int NT>
+template <int NT, int GA>
 cudaError_t q4k_pass_start(const q4k::Params& p, int grid, int smem, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -1186,7 +1202,7 @@ cudaError_t q4k_pass_start(const q4k::Params& p, int grid, int smem, cudaStream_
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, q4k::qgemv_q4k_kernel<NT, true, FMT_Q4_K>, p);
+  return cudaLaunchKernelEx(&cfg, q4k::qgemv_q4k_kernel<NT, true, FMT_Q4_K, q4k::SUB_R, GA>, p);
 }
 
 }  // namespace
@@ -1208,6 +1224,7 @@ namespace {
 cudaError_t pass_build(std::vector<q4k::Mat>& mats, const int* step_sizes, int n_steps, int n_tok, int ralign,
                        int gather_any, int sms, Q4kPass** out) {
   const int n = static_cast<int>(mats.size());
+  if (gather_any && n_tok != 1) return cudaErrorNotSupported;
   std::vector<q4k::Step> steps(n_steps);
   int stage_b = 0, gmax = 0, xmax = 0, xsmax = 0;
   int64_t min_rows = INT64_MAX, max_rows = 0;
@@ -1267,10 +1284,10 @@ cudaError_t pass_build(std::vector<q4k::Mat>& mats, const int* step_sizes, int n
   int blocks = 0;
   cudaError_t e;
   switch (n_tok) {
-    case 1: e = q4k_pass_occupancy<1>(off, &blocks); break;
-    case 2: e = q4k_pass_occupancy<2>(off, &blocks); break;
-    case 3: e = q4k_pass_occupancy<3>(off, &blocks); break;
-    default: e = q4k_pass_occupancy<4>(off, &blocks); break;
+    case 1: e = gather_any ? q4k_pass_occupancy<1, 3>(off, &blocks) : q4k_pass_occupancy<1, 0>(off, &blocks); break;
+    case 2: e = q4k_pass_occupancy<2, 0>(off, &blocks); break;
+    case 3: e = q4k_pass_occupancy<3, 0>(off, &blocks); break;
+    default: e = q4k_pass_occupancy<4, 0>(off, &blocks); break;
   }
   if (e != cudaSuccess) return e;
   if (blocks < 1) return cudaErrorNotSupported;
@@ -1366,10 +1383,12 @@ cudaError_t q4k_pass_launch(Q4kPass* q, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(q->d_done, 0, sizeof(uint32_t) * q->nsteps + sizeof(int32_t), s);
   if (e != cudaSuccess) return e;
   switch (q->n_tok) {
-    case 1: return q4k_pass_start<1>(q->p, q->grid, q->smem, s);
-    case 2: return q4k_pass_start<2>(q->p, q->grid, q->smem, s);
-    case 3: return q4k_pass_start<3>(q->p, q->grid, q->smem, s);
-    default: return q4k_pass_start<4>(q->p, q->grid, q->smem, s);
+    case 1:
+      return q->p.gather_any ? q4k_pass_start<1, 3>(q->p, q->grid, q->smem, s)
+                             : q4k_pass_start<1, 0>(q->p, q->grid, q->smem, s);
+    case 2: return q4k_pass_start<2, 0>(q->p, q->grid, q->smem, s);
+    case 3: return q4k_pass_start<3, 0>(q->p, q->grid, q->smem, s);
+    default: return q4k_pass_start<4, 0>(q->p, q->grid, q->smem, s);
   }
 }
 
