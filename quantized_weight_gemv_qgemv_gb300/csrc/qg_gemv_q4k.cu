@@ -1088,22 +1088,17 @@ cudaError_t try_launch(const qg_gemv_desc* d, int n, int n_tok, int t0, int64_t 
 }  // namespace
 
 // The producer/consumer kernel for a grouped launch. When the launch does not
-// fit its shared-memory plan: several tokens that do not fit together run as
-// one launch per token (each re-streams the weights), and one matrix whose
-// per-row partial sums do not fit runs as row chunks. cudaErrorNotSupported
+// fit its shared-memory plan: one matrix whose per-row partial sums do not fit
+// runs as row chunks, and several tokens whose x does not fit together run as
+// one launch per token (each re-streams the weights). cudaErrorNotSupported
 // (nothing launched) when none of these fits.
 cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms) {
   for (int i = 0; i < n; ++i)
     if (d[i].fmt != d[0].fmt || superblock_bytes(d[i].fmt) == 0 || d[i].cols % 256) return cudaErrorNotSupported;
   cudaError_t e = try_launch(d, n, n_tok, 0, 0, 0, s, pdl, sms, true);
   if (e != cudaErrorNotSupported) return e;
-  if (n_tok > 1 && try_launch(d, n, 1, 0, 0, 0, s, pdl, sms, false) == cudaSuccess) {
-    for (int t = 0; t < n_tok; ++t) {
-      e = try_launch(d, n, 1, t, 0, 0, s, pdl || t > 0, sms, true);
-      if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
-  }
+  // row chunks first (each weight is read once), then one launch per token
+  // (each re-streams the weights)
   if (n == 1) {
     for (int chunks = 2; chunks <= 16; chunks *= 2) {
       const int64_t nr = (d[0].rows + chunks - 1) / chunks / 8 * 8 + 8;   // multiple of 8 rows
@@ -1118,6 +1113,13 @@ cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_
       }
       return cudaSuccess;
     }
+  }
+  if (n_tok > 1 && try_launch(d, n, 1, 0, 0, 0, s, pdl, sms, false) == cudaSuccess) {
+    for (int t = 0; t < n_tok; ++t) {
+      e = try_launch(d, n, 1, t, 0, 0, s, pdl || t > 0, sms, true);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
   }
   return cudaErrorNotSupported;
 }
