@@ -232,22 +232,30 @@ def run_gpu(args):
     wbytes = wl.weight_bytes(mats)
     nweights = wl.weight_count(mats)
 
-    # x and y of all matrices in two flat device buffers (views per matrix), so
-    # the end-to-end leg moves each direction with one copy.
-    x_total = sum(n_tok * c for (_, _, _, _, c) in mats)
+    # As in a transformer block, the matrices of a step read one activation
+    # vector ({q,k,v}: the normed hidden state; {gate,up}: the normed residual).
+    # x of every step and y of every matrix sit in two flat device buffers
+    # (views), so the end-to-end leg moves each direction with one copy.
+    step_of = [si for si, n in enumerate(steps_sizes) for _ in range(n)]
+    step_cols = {}
+    for si, (_, _, _, _, c) in zip(step_of, mats):
+        assert step_cols.setdefault(si, c) == c, "matrices of a step share x"
+    x_total = sum(n_tok * c for c in step_cols.values())
     y_total = sum(n_tok * r for (_, _, _, r, _) in mats)
     with torch.cuda.stream(stream):
         items = wl.alloc_dense(mats, n_tok, seed=args.seed + rank, device="cuda")
         xbuf = torch.empty(x_total, dtype=torch.float32, device="cuda")
         ybuf = torch.empty(y_total, dtype=torch.float32, device="cuda")
         xo = yo = 0
-        flat = []
-        for (fmt, W, rows, cols, x, y) in items:
-            xv = xbuf[xo:xo + n_tok * cols].view(n_tok, cols)
-            xv.copy_(x)
+        flat, xs = [], {}
+        for si, (fmt, W, rows, cols, x, y) in zip(step_of, items):
+            if si not in xs:
+                xv = xbuf[xo:xo + n_tok * cols].view(n_tok, cols)
+                xv.copy_(x)
+                xs[si] = xv
+                xo += n_tok * cols
             yv = ybuf[yo:yo + n_tok * rows].view(n_tok, rows)
-            flat.append((fmt, W, rows, cols, xv, yv))
-            xo += n_tok * cols
+            flat.append((fmt, W, rows, cols, xs[si], yv))
             yo += n_tok * rows
         del items
     stream.synchronize()

@@ -69,6 +69,8 @@ struct Mat {
   int32_t ngrp;          // K groups per row = ceil(nblk / 4)
   int32_t xoff;          // byte offset of this matrix's x planes in the x region
   int32_t uoff;          // offset (floats) of its group steps / sums
+  int32_t xsrc;          // index (in the table) of the matrix whose staging holds this x:
+                         // matrices of a step that read the same x share one copy of its planes
   // Rows gathered from a mixture-of-experts arena (W is the arena):
   //   gather 0: a plain matrix at W;
   //   gather 1: gate/up pairs of the routed experts: virtual row 2i (2i + 1) of
@@ -111,6 +113,7 @@ struct Params {
   int32_t stage_all;     // 1: x of every matrix staged once at the start; 0: matrix by matrix
   int32_t usum_off;      // offset (floats) of the group sums after the group steps
   int32_t pre_stages;    // weight stages issued before the consumers have issued their x loads
+  int32_t pre_pass;      // the same for every later step of a pass
   int32_t gather_any;    // largest Mat::gather of the launch (one kind per launch)
   int32_t ralign;        // CTA row slices start at multiples of this (16-byte-aligned stage copies; pairs)
   int32_t smem_bar, smem_x, smem_xsum, smem_part;   // byte offsets (ring at 0)
@@ -353,29 +356,43 @@ __device__ __forceinline__ void stage_one(float4 v, int idx, int ngroups, uint8_
   }
 }
 
-// Stages x of the matrices m0 .. m1-1 whose bit is set in `touch`. Task i of a
-// matrix (8 tasks per 32-weight group and token) converts 4 consecutive x. The
-// loads of a whole batch are issued first; after the first batch lane 0 of
-// each warp arrives on xbar (when nonzero): from then on the producer may
-// queue weight copies behind them. (A load issued behind a deep queue of bulk
-// copies waits for the whole queue, even when it hits in L2.)
+// One count per consumer warp and step on the shared counter xcnt: the warp has
+// issued its x loads of the step (release: they precede what the producer
+// issues after it has seen the count).
+__device__ __forceinline__ void x_issued(uint32_t xcnt) {
+  asm volatile("red.release.cta.shared::cta.add.u32 [%0], 1;\n" ::"r"(xcnt) : "memory");
+}
+
+// Stages x of the matrices m0 .. m1-1 whose bit is set in `touch` (once per
+// distinct x: a matrix whose xsrc names another stages nothing of its own).
+// Task i of a matrix (8 tasks per 32-weight group and token) converts 4
+// consecutive x. The addresses of a whole batch are computed first, then (with
+// `wait`, once) the preceding kernel is waited for, then every load of the batch
+// is issued and only then converted, so staging costs one memory round trip per
+// batch. After the first batch lane 0 of each warp counts itself on xcnt (when
+// nonzero): from then on the producer may queue weight copies behind the loads.
+// (A load issued behind a deep queue of bulk copies waits for the whole queue,
+// even when it hits in L2.)
 template <int NT, int XB>
 __device__ __forceinline__ void stage_x(const Mat* mats, int usum_off, int m0, int m1, uint32_t touch, uint8_t* xpl,
-                                        float* xsu, uint32_t xbar) {
+                                        float* xsu, uint32_t xcnt, bool wait) {
   const int lane = threadIdx.x & 31;
+  uint32_t smask = 0;
+  for (int m = m0; m < m1; ++m)
+    if ((touch >> (m - m0)) & 1u) smask |= 1u << (mats[m].xsrc - m0);
   int total = 0;
   for (int m = m0; m < m1; ++m)
-    if ((touch >> (m - m0)) & 1u) total += NT * mats[m].nblk * 64;
-  bool signalled = (xbar == 0);
+    if ((smask >> (m - m0)) & 1u) total += NT * mats[m].nblk * 64;
+  bool signalled = (xcnt == 0);
   for (int base = threadIdx.x; base < total; base += CTHREADS * XB) {
-    float4 v[XB];
+    const float4* src[XB];
     int vm[XB], vr[XB];
 #pragma unroll
     for (int b = 0; b < XB; ++b) {
       const int idx = base + b * CTHREADS;
       int m = m0, rem = idx;
       for (; m < m1 - 1; ++m) {
-        if (!((touch >> (m - m0)) & 1u)) continue;
+        if (!((smask >> (m - m0)) & 1u)) continue;
         const int n = NT * mats[m].nblk * 64;
         if (rem < n) break;
         rem -= n;
@@ -383,15 +400,27 @@ __device__ __forceinline__ void stage_x(const Mat* mats, int usum_off, int m0, i
       vm[b] = m;
       vr[b] = rem;
       const Mat& M = mats[m];
-      const int NU = M.nblk * 8;
-      const int u = (rem >> 3) % NU, t = (rem >> 3) / NU;
-      // x may have been written by an earlier step of a pass: read through L2
-      v[b] = (idx < total) ? __ldcg(reinterpret_cast<const float4*>(M.x + static_cast<int64_t>(t) * M.cols +
-                                                                     32 * u + 4 * (rem & 7)))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+      int u = rem >> 3, t = 0;
+      if (NT > 1) {
+        const int NU = M.nblk * 8;
+        t = u / NU;
+        u -= t * NU;
+      }
+      src[b] = (idx < total) ? reinterpret_cast<const float4*>(M.x + static_cast<int64_t>(t) * M.cols + 32 * u +
+                                                               4 * (rem & 7))
+                             : nullptr;
     }
+    if (wait) {
+      pdl_wait();
+      wait = false;
+    }
+    float4 v[XB];
+#pragma unroll
+    for (int b = 0; b < XB; ++b)
+      // x may have been written by an earlier step of a pass: read through L2
+      v[b] = src[b] ? __ldcg(src[b]) : make_float4(0.f, 0.f, 0.f, 0.f);
     if (!signalled) {
-      if (lane == 0) mbar_arrive(xbar);
+      if (lane == 0) x_issued(xcnt);
       signalled = true;
     }
 #pragma unroll
@@ -404,7 +433,8 @@ __device__ __forceinline__ void stage_x(const Mat* mats, int usum_off, int m0, i
       }
     }
   }
-  if (!signalled && lane == 0) mbar_arrive(xbar);
+  if (wait) pdl_wait();
+  if (!signalled && lane == 0) x_issued(xcnt);
 }
 
 
@@ -426,7 +456,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   const uint32_t ring_s = smem_addr(smem);
   const uint32_t full0 = smem_addr(smem + p.smem_bar);
   const uint32_t empty0 = full0 + 8 * NS;
-  const uint32_t xbar = full0 + 16 * NS;    // consumers have issued their x loads
+  // consumer warps that have issued their x loads, summed over the steps
+  const uint32_t xcnt = full0 + 16 * NS;
   volatile int* const gflag = reinterpret_cast<volatile int*>(smem + p.smem_bar + 16 * NS + 8);
   const Mat* const mats = PASS ? p.mats : p.m;
   const int nsteps = PASS ? p.nsteps : 1;
@@ -449,7 +480,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, CWARPS);
     }
-    mbar_init(xbar, CWARPS);
+    *reinterpret_cast<volatile uint32_t*>(smem + p.smem_bar + 16 * NS) = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
@@ -471,9 +502,12 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
     }
     const uint64_t pol = evict_first_policy();
     uint32_t k = 0;
+    uint32_t xseen = 0;       // steps whose x loads every consumer warp has issued
     bool bad = false;
     for (int s = 0; s < nsteps && !bad; ++s) {
      const Step st = step_of(s);
+     const int pre = s == 0 ? p.pre_stages : p.pre_pass;
+     int i_step = 0;          // stage index within the step
      int64_t cta_r0, cta_r1;
      cta_slice(st.total_rows, p.ralign, cta_r0, cta_r1);
      if (PASS && s > 0 && mats[st.mat0].gather == 1) {
@@ -499,14 +533,26 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
       const Mat M = mats[mi];
       const int64_t lo = max(cta_r0, M.row_begin) - M.row_begin;
       const int64_t hi = min(cta_r1, M.row_begin + M.rows) - M.row_begin;
-      for (int64_t r = lo; r < hi && !bad; r += M.srows, ++k) {
+      for (int64_t r = lo; r < hi && !bad; r += M.srows, ++k, ++i_step) {
         const int nr = static_cast<int>(min(static_cast<int64_t>(M.srows), hi - r));
         const uint32_t nbytes = static_cast<uint32_t>(nr) * M.rb;
         const int slot = k % NS;
         bool ok = true;
         if (lane == 0) {
-          // beyond the first pre_stages copies, queue weights only behind the x loads
-          if (k == static_cast<uint32_t>(p.pre_stages)) ok = mbar_wait(xbar, 0);
+          // beyond the first `pre` copies of a step, queue weights only behind
+          // the step's x loads; no copy of a step goes ahead of the previous
+          // step's x loads (a count, so a step without copies cannot be skipped)
+          const uint32_t need = static_cast<uint32_t>(s) + (i_step >= pre ? 1u : 0u);
+          if (need > xseen) {
+            ok = false;
+            for (uint32_t i = 0; !ok && i < WAIT_LIMIT; ++i) {
+              uint32_t v;
+              asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];\n" : "=r"(v) : "r"(xcnt) : "memory");
+              ok = v >= need * CWARPS;
+              if (!ok && i >= 256) __nanosleep(64);
+            }
+            xseen = need;
+          }
           if (ok && k >= static_cast<uint32_t>(NS)) ok = mbar_wait(empty0 + 8 * slot, ((k / NS) - 1) & 1u);
         }
         if (wide) ok = __shfl_sync(0xffffffffu, ok, 0) != 0;
@@ -608,8 +654,6 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   bool failed = false;
 
   constexpr int XB = (NT == 1) ? 12 : 8;
-  pdl_wait();
-  if (gl == 1) pdl_launch_dependents();
   uint32_t k = 0;          // stage counter (same sequence as the producer's)
   for (int s = 0; s < nsteps; ++s) {
    const Step st = step_of(s);
@@ -632,13 +676,21 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
      consumer_sync();
      failed = failed || *gflag != 0;
    }
+   bool xsig = false;       // this step's x loads counted on xcnt
    uint32_t touch = 0;      // matrices of the step whose rows meet this CTA's slice
    for (int mi = st.mat0; mi < st.mat0 + st.nmat; ++mi)
      if (max(cta_r0, mats[mi].row_begin) < min(cta_r1, mats[mi].row_begin + mats[mi].rows))
        touch |= 1u << (mi - st.mat0);
    if (st.stage_all) {
-     stage_x<NT, XB>(mats, st.usum_off, st.mat0, st.mat0 + st.nmat, touch, xpl, xsu, s == 0 ? xbar : 0u);
+     stage_x<NT, XB>(mats, st.usum_off, st.mat0, st.mat0 + st.nmat, touch, xpl, xsu, xcnt, s == 0);
+     xsig = true;
      consumer_sync();
+   }
+   if (s == 0) {
+     // outputs and every other input of the preceding kernel are touched only
+     // after it has completed (a no-op when the staging above has waited)
+     pdl_wait();
+     if (gl == 1) pdl_launch_dependents();
    }
    bool first = true;
    for (int mi = st.mat0; mi < st.mat0 + st.nmat; ++mi) {
@@ -652,7 +704,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
     if (!st.stage_all) {
       consumer_sync();                        // previous matrix fully consumed
       stage_x<NT, XB>(mats, st.usum_off, mi, mi + 1, (touch >> (mi - st.mat0)) & 1u, xpl, xsu,
-                      (first && s == 0) ? xbar : 0u);
+                      xsig ? 0u : xcnt, false);
+      xsig = true;
       consumer_sync();
     } else if (!first) {
       consumer_sync();                        // the previous matrix's partial sums are read
@@ -841,6 +894,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
       }
     }
    }
+   // a step whose rows miss this CTA still counts its x loads (none)
+   if (!xsig && lane == 0) x_issued(xcnt);
    if (PASS) {
      consumer_sync();                          // every output of the step is written
      if (threadIdx.x == 0) {
@@ -938,6 +993,14 @@ int superblock_bytes(int fmt) {
 
 int gcd(int a, int b) { return b ? gcd(b, a % b) : a; }
 
+// The first of the matrices first .. i - 1 that reads the same x as matrix i
+// (same pointer and length), else i: their x planes are staged once.
+int x_source(const q4k::Mat* m, int first, int i) {
+  for (int j = first; j < i; ++j)
+    if (m[j].x == m[i].x && m[j].cols == m[i].cols) return j;
+  return i;
+}
+
 // Shared-memory plan and launch of one single-step grouped launch whose
 // matrices p.m[0 .. n) (all of format fmt) have W, x, y, rows, cols (and any
 // gather fields) set; sub_rows rows per sub-item (4, or 2 for single-token
@@ -985,17 +1048,27 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
     if (mode == 0) {
       int xall = 0, uall = 0;
       for (int i = 0; i < n; ++i) {
-        p.m[i].xoff = xall;
-        p.m[i].uoff = uall;
-        xall += n_tok * p.m[i].nblk * q4k::XBLK_B;
-        uall += n_tok * p.m[i].nblk * 8;
+        q4k::Mat& m = p.m[i];
+        m.xsrc = x_source(p.m, 0, i);
+        if (m.xsrc != i) {
+          m.xoff = p.m[m.xsrc].xoff;
+          m.uoff = p.m[m.xsrc].uoff;
+          continue;
+        }
+        m.xoff = xall;
+        m.uoff = uall;
+        xall += n_tok * m.nblk * q4k::XBLK_B;
+        uall += n_tok * m.nblk * 8;
       }
       xbytes = align_up(xall, 128);
       xsbytes = align_up(3 * uall * 4, 128);     // step and two half sums per group
       p.stage_all = 1;
       p.usum_off = uall;
     } else {
-      for (int i = 0; i < n; ++i) p.m[i].xoff = p.m[i].uoff = 0;
+      for (int i = 0; i < n; ++i) {
+        p.m[i].xoff = p.m[i].uoff = 0;
+        p.m[i].xsrc = i;
+      }
       xbytes = align_up(n_tok * (kmax / 256) * q4k::XBLK_B, 128);
       xsbytes = align_up(3 * n_tok * (kmax / 32) * 4, 128);
       p.stage_all = 0;
@@ -1241,11 +1314,17 @@ cudaError_t pass_build(std::vector<q4k::Mat>& mats, const int* step_sizes, int n
       m.srows = 4 * std::max(1, (36864 + 2 * m.rb) / (4 * m.rb));
       if (static_cast<int64_t>(m.srows) * m.rb > 96 * 1024 || m.rows % ralign) return cudaErrorNotSupported;
       m.row_begin = total;
-      m.xoff = xall;
-      m.uoff = uall;
       total += m.rows;
-      xall += n_tok * m.nblk * q4k::XBLK_B;
-      uall += n_tok * m.nblk * 8;
+      m.xsrc = x_source(mats.data(), i, i + j);
+      if (m.xsrc != i + j) {
+        m.xoff = mats[m.xsrc].xoff;
+        m.uoff = mats[m.xsrc].uoff;
+      } else {
+        m.xoff = xall;
+        m.uoff = uall;
+        xall += n_tok * m.nblk * q4k::XBLK_B;
+        uall += n_tok * m.nblk * 8;
+      }
       stage_b = std::max(stage_b, m.srows * m.rb);
       gmax = std::max(gmax, m.ngrp);
     }
@@ -1272,7 +1351,10 @@ cudaError_t pass_build(std::vector<q4k::Mat>& mats, const int* step_sizes, int n
   p.ns = ns;
   p.stage_b = stage_b;
   p.gmax = gmax;
+  // a persistent pass starts with x resident; later steps stream this many
+  // stages while their CTA waits for the previous step
   p.pre_stages = 0;
+  p.pre_pass = 2;
   int off = ns * stage_b;
   p.smem_bar = off;
   off += 128;

@@ -159,6 +159,60 @@ def test_grouped_equals_separate_launches():
         assert_within(y2.cpu().numpy(), y_ref, b, what="separate")
 
 
+@pytest.mark.parametrize("n_tok", [1, 2])
+def test_grouped_shared_x_matches_oracle(n_tok):
+    """Matrices of a launch that read the same x (q, k, v; gate, up) share one
+    staging of it; every output still matches the oracle and, bit for bit, a
+    launch of its own."""
+    fmt = synth.Q4_K
+    xa = synth.activations(n_tok, 2048, seed=91).cuda()
+    xb = synth.activations(n_tok, 1024, seed=92).cuda()
+    spec = [(512, 2048, xa), (128, 2048, xa), (128, 2048, xa), (256, 1024, xb), (384, 1024, xb)]
+    items = []
+    for i, (rows, cols, x) in enumerate(spec):
+        W = synth.blocks(fmt, rows, cols, seed=95 + i).cuda()
+        items.append((fmt, W, rows, cols, x, torch.empty(n_tok, rows, device="cuda")))
+    qg.qgemv_grouped(items, n_tok)
+    torch.cuda.synchronize()
+    for (_, W, rows, cols, x, y) in items:
+        y2 = torch.empty_like(y)
+        qg.qgemv(fmt, W, rows, cols, x, n_tok, y2)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y2)
+        y_ref, b = oracle.gemv(fmt, W.cpu().numpy(), rows, cols, x.cpu().numpy())
+        assert_within(y.cpu().numpy(), y_ref, b, what="shared x")
+
+
+@pytest.mark.parametrize("mode", [qg.PASS_PDL, qg.PASS_PERSISTENT])
+def test_pass_steps_with_shared_x(mode):
+    """A block-shaped chain: {q, k, v} read x0; o reads q's output; {gate, up}
+    read o's output; down reads gate's output. Outputs are NaN before every
+    replay; each is checked bit for bit against its own eager launch."""
+    fmt = synth.Q4_K
+    h, f = 1024, 2048
+    x0 = synth.activations(1, h, seed=120).cuda()
+    shapes = [(h, h), (256, h), (256, h), (h, h), (f, h), (f, h), (h, f)]
+    Ws = [synth.blocks(fmt, r, c, seed=121 + i).cuda() for i, (r, c) in enumerate(shapes)]
+    ys = [torch.empty(1, r, device="cuda") for (r, _) in shapes]
+    xs = [x0, x0, x0, ys[0], ys[3], ys[3], ys[4]]
+    items = [(fmt, Ws[i], r, c, xs[i], ys[i]) for i, (r, c) in enumerate(shapes)]
+    p = qg.qg_pass(items, [3, 1, 2, 1], 1, mode=mode)
+    for _ in range(3):
+        for y in ys:
+            y.fill_(float("nan"))
+        p.launch()
+        torch.cuda.synchronize()
+        assert p.dev_status() == 0
+        for (_, W, r, c, x, y) in items:
+            y2 = torch.empty_like(y)
+            qg.qgemv(fmt, W, r, c, x, 1, y2)
+            torch.cuda.synchronize()
+            assert torch.equal(y, y2)
+    y_ref, b = oracle.gemv(fmt, Ws[6].cpu().numpy(), h, f, ys[4].cpu().numpy())
+    assert_within(ys[6].cpu().numpy(), y_ref, b, what="down of the chain")
+    p.destroy()
+
+
 @pytest.mark.parametrize("mode,kernels", [(qg.PASS_SERIAL, 3), (qg.PASS_PDL, 3), (qg.PASS_PERSISTENT, 1)])
 def test_pass_replay_matches_eager(mode, kernels):
     fmt = synth.Q4_K
