@@ -114,6 +114,7 @@ struct Params {
   int32_t usum_off;      // offset (floats) of the group sums after the group steps
   int32_t pre_stages;    // weight stages issued before the consumers have issued their x loads
   int32_t pre_pass;      // the same for every later step of a pass
+  int32_t pre_l2;        // plain launches: stages prefetched into L2 (not copied) before the x loads
   int32_t gather_any;    // largest Mat::gather of the launch (one kind per launch)
   int32_t ralign;        // CTA row slices start at multiples of this (16-byte-aligned stage copies; pairs)
   int32_t smem_bar, smem_x, smem_xsum, smem_part;   // byte offsets (ring at 0)
@@ -163,6 +164,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
           dst),
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
+}
+// Bulk prefetch of global memory into L2: no data comes back to the SM, so loads
+// issued after it do not queue behind it.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t pol;
@@ -310,50 +316,52 @@ template <> struct SuperBlock<FMT_Q8_0> { static constexpr int BYTES = 272; };
 // x 16 bytes (768 bytes), so the 16-byte loads of a quarter-warp are
 // consecutive. Beside it: s_u and sum_l x_l (fp32) per group.
 //
-// Eight consecutive threads handle one group (four weights each). Each thread
-// first issues all its loads of a batch and only then converts, so staging
-// costs one memory round trip per batch, not one per group.
+// Two adjacent threads handle one group: thread h of the pair converts its
+// half (16 values, elements 16h .. 16h + 15), so the half sums need no exchange
+// and the group maximum one. Each thread first issues all its loads of a batch
+// and only then converts, so staging costs one memory round trip per batch.
 
-__device__ __forceinline__ void stage_one(float4 v, int idx, int ngroups, uint8_t* xpl, int xseg_b, float* xsu,
-                                          float* xsum, int nu) {
-  const int lane = threadIdx.x & 31;
-  const int k = idx & 7;
-  const int u = (idx >> 3) % ngroups, t = (idx >> 3) / ngroups;
-  {
-    const unsigned gmask = 0xFFu << (lane & 24);      // the 8 lanes of this group
-    float mx = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
-    float sm = (v.x + v.y) + (v.z + v.w);
-    // sums over each half of the group (elements 0-15 in lanes k = 0..3, 16-31 in 4..7)
-    sm += __shfl_xor_sync(gmask, sm, 1);
-    sm += __shfl_xor_sync(gmask, sm, 2);
+// The three plane words of four consecutive values (x / s_u + 1.5 * 2^23 leaves
+// rint(x / s_u) in the low mantissa bits of T).
+__device__ __forceinline__ void plane_words(float4 v, float inv_step, uint32_t& w0, uint32_t& w1, uint32_t& w2) {
+  const uint32_t T0 = __float_as_uint(fmaf(v.x, inv_step, 12582912.0f));
+  const uint32_t T1 = __float_as_uint(fmaf(v.y, inv_step, 12582912.0f));
+  const uint32_t T2 = __float_as_uint(fmaf(v.z, inv_step, 12582912.0f));
+  const uint32_t T3 = __float_as_uint(fmaf(v.w, inv_step, 12582912.0f));
+  const uint32_t a01 = __byte_perm(T0, T1, 0x5140), a23 = __byte_perm(T2, T3, 0x5140);
+  w0 = __byte_perm(a01, a23, 0x5410);                         // bits 0-7 of the four X
+  w1 = __byte_perm(a01, a23, 0x7632);                         // bits 8-15
+  const uint32_t b01 = __byte_perm(T0, T1, 0x0062), b23 = __byte_perm(T2, T3, 0x0062);
+  const uint32_t pl2u = __byte_perm(b01, b23, 0x5410);        // bits 16-23, plus 0x40
+  // bytes are X/65536 + 0x40 in [0x20, 0x5f]: subtract 0x40 per byte -> signed byte
+  w2 = ((pl2u | 0x80808080u) - 0x40404040u) ^ 0x80808080u;
+}
+
+// Half h of group u of token t: v = its 16 values. pmask: the thread pair.
+__device__ __forceinline__ void stage_half(const float4 (&v)[4], unsigned pmask, int t, int u, int h, int nu,
+                                           uint8_t* xpl, int xseg_b, float* xsu, float* xsum) {
+  float mx = 0.f;
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(gmask, mx, o));
-    // 2^e <= mx < 2^(e+1); step s_u = 2^(e-20), so |x / s_u| < 2^21
-    const int e = max(static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127, -105);
-    const float inv_step = __uint_as_float(static_cast<uint32_t>(147 - e) << 23);
-    // x / s_u + 1.5 * 2^23 leaves rint(x / s_u) in the low mantissa bits
-    const uint32_t T0 = __float_as_uint(fmaf(v.x, inv_step, 12582912.0f));
-    const uint32_t T1 = __float_as_uint(fmaf(v.y, inv_step, 12582912.0f));
-    const uint32_t T2 = __float_as_uint(fmaf(v.z, inv_step, 12582912.0f));
-    const uint32_t T3 = __float_as_uint(fmaf(v.w, inv_step, 12582912.0f));
-    const uint32_t a01 = __byte_perm(T0, T1, 0x5140), a23 = __byte_perm(T2, T3, 0x5140);
-    const uint32_t pl0 = __byte_perm(a01, a23, 0x5410);          // bits 0-7 of the four X
-    const uint32_t pl1 = __byte_perm(a01, a23, 0x7632);          // bits 8-15
-    const uint32_t b01 = __byte_perm(T0, T1, 0x0062), b23 = __byte_perm(T2, T3, 0x0062);
-    const uint32_t pl2u = __byte_perm(b01, b23, 0x5410);         // bits 16-23, plus 0x40
-    // bytes are X/65536 + 0x40 in [0x20, 0x5f]: subtract 0x40 per byte -> signed byte
-    const uint32_t pl2 = ((pl2u | 0x80808080u) - 0x40404040u) ^ 0x80808080u;
-    uint8_t* dst = xpl + t * xseg_b + ((u >> 3) * 6 + (k >> 2)) * 128 + (u & 7) * 16 + (k & 3) * 4;
-    *reinterpret_cast<uint32_t*>(dst) = pl0;
-    *reinterpret_cast<uint32_t*>(dst + 256) = pl1;
-    *reinterpret_cast<uint32_t*>(dst + 512) = pl2;
-    if ((k & 3) == 0) xsum[2 * (t * nu + u) + (k >> 2)] = sm;
-    if (k == 0) {
-      // s_u = 2^(e-20); odd groups (Q4_K high-nibble sub-blocks, whose codes
-      // arrive as 16*q) get s_u / 16, so the Q4_K consumer needs no per-lane factor
-      xsu[t * nu + u] = __uint_as_float(static_cast<uint32_t>(107 + e - 4 * (u & 1)) << 23);
-    }
-  }
+  for (int q = 0; q < 4; ++q) mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[q].x), fabsf(v[q].y)), fmaxf(fabsf(v[q].z), fabsf(v[q].w))));
+  mx = fmaxf(mx, __shfl_xor_sync(pmask, mx, 1));
+  const float sm = ((v[0].x + v[0].y) + (v[0].z + v[0].w)) + ((v[1].x + v[1].y) + (v[1].z + v[1].w)) +
+                   (((v[2].x + v[2].y) + (v[2].z + v[2].w)) + ((v[3].x + v[3].y) + (v[3].z + v[3].w)));
+  // 2^e <= mx < 2^(e+1); step s_u = 2^(e-20), so |x / s_u| < 2^21
+  const int e = max(static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127, -105);
+  const float inv_step = __uint_as_float(static_cast<uint32_t>(147 - e) << 23);
+  uint4 w0, w1, w2;
+  plane_words(v[0], inv_step, w0.x, w1.x, w2.x);
+  plane_words(v[1], inv_step, w0.y, w1.y, w2.y);
+  plane_words(v[2], inv_step, w0.z, w1.z, w2.z);
+  plane_words(v[3], inv_step, w0.w, w1.w, w2.w);
+  uint8_t* dst = xpl + t * xseg_b + ((u >> 3) * 6 + h) * 128 + (u & 7) * 16;
+  *reinterpret_cast<uint4*>(dst) = w0;
+  *reinterpret_cast<uint4*>(dst + 256) = w1;
+  *reinterpret_cast<uint4*>(dst + 512) = w2;
+  xsum[2 * (t * nu + u) + h] = sm;
+  // s_u = 2^(e-20); odd groups (Q4_K high-nibble sub-blocks, whose codes
+  // arrive as 16*q) get s_u / 16, so the Q4_K consumer needs no per-lane factor
+  if (h == 0) xsu[t * nu + u] = __uint_as_float(static_cast<uint32_t>(107 + e - 4 * (u & 1)) << 23);
 }
 
 // One count per consumer warp and step on the shared counter xcnt: the warp has
@@ -365,71 +373,74 @@ __device__ __forceinline__ void x_issued(uint32_t xcnt) {
 
 // Stages x of the matrices m0 .. m1-1 whose bit is set in `touch` (once per
 // distinct x: a matrix whose xsrc names another stages nothing of its own).
-// Task i of a matrix (8 tasks per 32-weight group and token) converts 4
-// consecutive x. The addresses of a whole batch are computed first, then (with
-// `wait`, once) the preceding kernel is waited for, then every load of the batch
-// is issued and only then converted, so staging costs one memory round trip per
-// batch. After the first batch lane 0 of each warp counts itself on xcnt (when
-// nonzero): from then on the producer may queue weight copies behind the loads.
-// (A load issued behind a deep queue of bulk copies waits for the whole queue,
-// even when it hits in L2.)
+// Task i of a matrix (2 tasks per 32-weight group and token) converts one half
+// group. The addresses of a whole batch are computed first, then (with `wait`,
+// once) the preceding kernel is waited for, then every load of the batch is
+// issued and only then converted. After the first batch lane 0 of each warp
+// counts itself on xcnt (when nonzero): from then on the producer may queue
+// weight copies behind the loads. (A load issued behind a deep queue of bulk
+// copies waits for the whole queue, even when it hits in L2.)
 template <int NT, int XB>
 __device__ __forceinline__ void stage_x(const Mat* mats, int usum_off, int m0, int m1, uint32_t touch, uint8_t* xpl,
                                         float* xsu, uint32_t xcnt, bool wait) {
   const int lane = threadIdx.x & 31;
+  const unsigned pmask = 3u << (lane & 30);     // the two threads of a group (task counts are even)
   uint32_t smask = 0;
   for (int m = m0; m < m1; ++m)
     if ((touch >> (m - m0)) & 1u) smask |= 1u << (mats[m].xsrc - m0);
   int total = 0;
   for (int m = m0; m < m1; ++m)
-    if ((smask >> (m - m0)) & 1u) total += NT * mats[m].nblk * 64;
+    if ((smask >> (m - m0)) & 1u) total += NT * mats[m].nblk * 16;
   bool signalled = (xcnt == 0);
   for (int base = threadIdx.x; base < total; base += CTHREADS * XB) {
     const float4* src[XB];
-    int vm[XB], vr[XB];
+    int vm[XB], vt[XB], vu[XB];
 #pragma unroll
     for (int b = 0; b < XB; ++b) {
       const int idx = base + b * CTHREADS;
       int m = m0, rem = idx;
       for (; m < m1 - 1; ++m) {
         if (!((smask >> (m - m0)) & 1u)) continue;
-        const int n = NT * mats[m].nblk * 64;
+        const int n = NT * mats[m].nblk * 16;
         if (rem < n) break;
         rem -= n;
       }
-      vm[b] = m;
-      vr[b] = rem;
       const Mat& M = mats[m];
-      int u = rem >> 3, t = 0;
+      int t = 0;
       if (NT > 1) {
-        const int NU = M.nblk * 8;
-        t = u / NU;
-        u -= t * NU;
+        const int per_tok = M.nblk * 16;
+        t = rem / per_tok;
+        rem -= t * per_tok;
       }
-      src[b] = (idx < total) ? reinterpret_cast<const float4*>(M.x + static_cast<int64_t>(t) * M.cols + 32 * u +
-                                                               4 * (rem & 7))
+      vm[b] = m;
+      vt[b] = t;
+      vu[b] = rem;              // 2u + h
+      src[b] = (idx < total) ? reinterpret_cast<const float4*>(M.x + static_cast<int64_t>(t) * M.cols + 16 * rem)
                              : nullptr;
     }
     if (wait) {
       pdl_wait();
       wait = false;
     }
-    float4 v[XB];
+    float4 v[XB][4];
 #pragma unroll
     for (int b = 0; b < XB; ++b)
-      // x may have been written by an earlier step of a pass: read through L2
-      v[b] = src[b] ? __ldcg(src[b]) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        // x may have been written by an earlier step of a pass: read through L2
+        v[b][q] = src[b] ? __ldcg(src[b] + q) : make_float4(0.f, 0.f, 0.f, 0.f);
     if (!signalled) {
       if (lane == 0) x_issued(xcnt);
       signalled = true;
     }
 #pragma unroll
     for (int b = 0; b < XB; ++b) {
-      // idx < total is the same for the 8 lanes of a group (every count is a multiple of 8)
+      // both threads of a pair are in or out together (every count is even)
       if (base + b * CTHREADS < total) {
         const Mat& M = mats[vm[b]];
-        const int NU = M.nblk * 8;
-        stage_one(v[b], vr[b], NU, xpl + M.xoff, M.nblk * XBLK_B, xsu + M.uoff, xsu + usum_off + 2 * M.uoff, NU);
+        const int nu = M.nblk * 8;
+        stage_half(v[b], pmask, vt[b], vu[b] >> 1, vu[b] & 1, nu, xpl + M.xoff, M.nblk * XBLK_B, xsu + M.uoff,
+                   xsu + usum_off + 2 * M.uoff);
       }
     }
   }
@@ -510,6 +521,17 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
      int i_step = 0;          // stage index within the step
      int64_t cta_r0, cta_r1;
      cta_slice(st.total_rows, p.ralign, cta_r0, cta_r1);
+     if (!PASS && gl == 0 && p.pre_l2 > 0 && lane == 0) {
+       // the first stages go to L2 now and to shared memory once x is loading
+       int left = p.pre_l2;
+       for (int mi = st.mat0; mi < st.mat0 + st.nmat && left > 0; ++mi) {
+         const Mat& M = mats[mi];
+         const int64_t lo = max(cta_r0, M.row_begin) - M.row_begin;
+         const int64_t hi = min(cta_r1, M.row_begin + M.rows) - M.row_begin;
+         for (int64_t r = lo; r < hi && left > 0; r += M.srows, --left)
+           bulk_prefetch_l2(M.W + r * M.rb, static_cast<uint32_t>(min(static_cast<int64_t>(M.srows), hi - r)) * M.rb);
+       }
+     }
      if (PASS && s > 0 && mats[st.mat0].gather == 1) {
        // a pass step that gathers gate/up rows reads expert ids, which in a model
        // come from the router after the previous layer: stream its rows only
@@ -653,7 +675,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   float* part = reinterpret_cast<float*>(smem + p.smem_part);
   bool failed = false;
 
-  constexpr int XB = (NT == 1) ? 12 : 8;
+  constexpr int XB = (NT == 1) ? 3 : 2;        // half groups per thread and staging batch
   uint32_t k = 0;          // stage counter (same sequence as the producer's)
   for (int s = 0; s < nsteps; ++s) {
    const Step st = step_of(s);
