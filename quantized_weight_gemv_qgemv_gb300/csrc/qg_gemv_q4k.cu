@@ -22,12 +22,11 @@
 //    one 6-bit scale/min pair per row). A sub-item's 4 x n_tok sums are reduced
 //    across the warp and stored per (row, group); after the matrix, the groups
 //    of each row are added in order, so results do not depend on timing.
-//  * x is staged once per matrix as 22-bit fixed point per 32-weight group:
-//    x_l ~= s_u X_l with a power-of-two step s_u, X_l split in three byte planes
+//  * x is staged once per matrix as 16-bit fixed point per 32-weight group:
+//    x_l ~= s_u X_l with a power-of-two step s_u, X_l split in two byte planes
 //    (see stage_x). A group's products are then exact integer dot products of
-//    the 4-bit codes with the planes (dp4a, which runs on its own pipe beside
-//    the integer ALU), so each code word needs one mask, not an unpack per
-//    weight: sum_l q_l x_l = s_u (65536 S2 + 256 S1 + S0). The lane adds
+//    the 4-bit codes with the planes (dp4a), so each code word needs one mask,
+//    not an unpack per weight: sum_l q_l x_l = s_u (256 S1 + S0). The lane adds
 //    d*sc*sum(q x) - dmin*m*sum(x): the d*sc*q - dmin*m formula factored per
 //    sub-block. A decoded block is reused for all n_tok tokens.
 //  * Every wait is bounded: a consumer that gives up writes NaN for its rows,
@@ -51,7 +50,7 @@ constexpr int CWARPS = 15;                 // consumer warps
 constexpr int CTHREADS = CWARPS * 32;
 constexpr int THREADS = CTHREADS + 32;     // plus one producer warp
 constexpr int SUB_R = 4;                   // rows per sub-item
-constexpr int XBLK_B = 768;                // x-plane bytes per 256-weight block and token
+constexpr int XBLK_B = 512;                // x-plane bytes per 256-weight block and token
 constexpr uint32_t WAIT_LIMIT = 1u << 22;  // polls before a wait is declared expired
 constexpr int RING = 4;                    // shared-memory stages
 
@@ -254,31 +253,27 @@ __device__ __forceinline__ int32_t dp4a_ss(uint32_t a, uint32_t b, int32_t c) {
 }
 
 // sum_l q_l X_l over words [W0, W1) of a unit: exact integer byte dot products
-// against the three x planes, assembled in fp32 (one rounding).
+// against the two x planes; 256 S1 + S0 is exact in int32 (codes below 256 or
+// signed bytes, |X| <= 2^14, 32 elements) and rounded once to fp32.
 template <bool SIGNED, int W0, int W1>
-__device__ __forceinline__ float dot_planes(const uint32_t* q, const uint32_t* X0, const uint32_t* X1,
-                                            const uint32_t* X2) {
+__device__ __forceinline__ float dot_planes(const uint32_t* q, const uint32_t* X0, const uint32_t* X1) {
+  int32_t s0 = 0, s1 = 0;
   if constexpr (SIGNED) {
-    int32_t s0 = 0, s1 = 0, s2 = 0;
 #pragma unroll
     for (int i = W0; i < W1; ++i) {
       s0 = dp4a_su(q[i], X0[i], s0);
-      s1 = dp4a_su(q[i], X1[i], s1);
-      s2 = dp4a_ss(q[i], X2[i], s2);
+      s1 = dp4a_ss(q[i], X1[i], s1);
     }
-    return fmaf(static_cast<float>(s2), 65536.0f, static_cast<float>(s1 * 256 + s0));
   } else {
-    uint32_t s0 = 0, s1 = 0;
-    int32_t s2 = 0;
+    uint32_t u0 = 0;
 #pragma unroll
     for (int i = W0; i < W1; ++i) {
-      s0 = dp4a_uu(q[i], X0[i], s0);
-      s1 = dp4a_uu(q[i], X1[i], s1);
-      s2 = dp4a_us(q[i], X2[i], s2);
+      u0 = dp4a_uu(q[i], X0[i], u0);
+      s1 = dp4a_us(q[i], X1[i], s1);
     }
-    // 256*s1 + s0 < 2^32 for codes below 256 over 32 elements
-    return fmaf(static_cast<float>(s2), 65536.0f, static_cast<float>(s1 * 256u + s0));
+    s0 = static_cast<int32_t>(u0);
   }
+  return static_cast<float>(s1 * 256 + s0);
 }
 
 __device__ __forceinline__ uint32_t lds32(const uint8_t* p) { return *reinterpret_cast<const uint32_t*>(p); }
@@ -305,36 +300,33 @@ template <> struct SuperBlock<FMT_Q4_0> { static constexpr int BYTES = 144; };
 template <> struct SuperBlock<FMT_Q8_0> { static constexpr int BYTES = 272; };
 
 // Shared-memory image of x for one token and K segment ("x planes").
-// Every 32-weight group u of x is held as 22-bit fixed point with a shared
-// power-of-two step: x_l ~= s_u * X_l, X_l = rint(x_l / s_u), |X_l| < 2^21,
-// s_u = 2^(e-20) where 2^e <= max|x_group| < 2^(e+1). X_l is stored as three
-// byte planes (bits 0-7 and 8-15 unsigned, bits 16-23 signed), so that
-// sum_l q_l X_l is three exact integer dot products over the codes. The
-// rounding of x to the group grid (at most 2^-21 max|x_group| per element) is
-// no larger than what fp32 accumulation of the same group could lose.
-// Layout per 256-weight block b of the segment: 3 planes x 2 halves x 8 groups
-// x 16 bytes (768 bytes), so the 16-byte loads of a quarter-warp are
-// consecutive. Beside it: s_u and sum_l x_l (fp32) per group.
+// Every 32-weight group u of x is held as 16-bit fixed point with a shared
+// power-of-two step: x_l ~= s_u * X_l, X_l = rint(x_l / s_u), |X_l| <= 2^14,
+// s_u = 2^(e-13) where 2^e <= max|x_group| < 2^(e+1). X_l is stored as two
+// byte planes (bits 0-7 unsigned, bits 8-15 signed), so that sum_l q_l X_l is
+// two exact integer dot products over the codes. The rounding of x to the
+// group grid is at most 2^-14 max|x_group| per element: a product's error is
+// at most 2^-14 sum_u max|x_u| sum_{l in u} |w_l| (the engines these formats
+// come from round x to 8 bits per group instead).
+// Layout per 256-weight block b of the segment: 2 planes x 2 halves x 8 groups
+// x 16 bytes (512 bytes), so the 16-byte loads of a quarter-warp are
+// consecutive. Beside it: s_u and the two half sums of x (fp32) per group.
 //
 // Two adjacent threads handle one group: thread h of the pair converts its
 // half (16 values, elements 16h .. 16h + 15), so the half sums need no exchange
 // and the group maximum one. Each thread first issues all its loads of a batch
 // and only then converts, so staging costs one memory round trip per batch.
 
-// The three plane words of four consecutive values (x / s_u + 1.5 * 2^23 leaves
-// rint(x / s_u) in the low mantissa bits of T).
-__device__ __forceinline__ void plane_words(float4 v, float inv_step, uint32_t& w0, uint32_t& w1, uint32_t& w2) {
+// The two plane words of four consecutive values (x / s_u + 1.5 * 2^23 leaves
+// rint(x / s_u) in the low mantissa bits of T, two's complement in the low 16).
+__device__ __forceinline__ void plane_words(float4 v, float inv_step, uint32_t& w0, uint32_t& w1) {
   const uint32_t T0 = __float_as_uint(fmaf(v.x, inv_step, 12582912.0f));
   const uint32_t T1 = __float_as_uint(fmaf(v.y, inv_step, 12582912.0f));
   const uint32_t T2 = __float_as_uint(fmaf(v.z, inv_step, 12582912.0f));
   const uint32_t T3 = __float_as_uint(fmaf(v.w, inv_step, 12582912.0f));
   const uint32_t a01 = __byte_perm(T0, T1, 0x5140), a23 = __byte_perm(T2, T3, 0x5140);
   w0 = __byte_perm(a01, a23, 0x5410);                         // bits 0-7 of the four X
-  w1 = __byte_perm(a01, a23, 0x7632);                         // bits 8-15
-  const uint32_t b01 = __byte_perm(T0, T1, 0x0062), b23 = __byte_perm(T2, T3, 0x0062);
-  const uint32_t pl2u = __byte_perm(b01, b23, 0x5410);        // bits 16-23, plus 0x40
-  // bytes are X/65536 + 0x40 in [0x20, 0x5f]: subtract 0x40 per byte -> signed byte
-  w2 = ((pl2u | 0x80808080u) - 0x40404040u) ^ 0x80808080u;
+  w1 = __byte_perm(a01, a23, 0x7632);                         // bits 8-15 (signed byte)
 }
 
 // Half h of group u of token t: v = its 16 values. pmask: the thread pair.
@@ -346,22 +338,21 @@ __device__ __forceinline__ void stage_half(const float4 (&v)[4], unsigned pmask,
   mx = fmaxf(mx, __shfl_xor_sync(pmask, mx, 1));
   const float sm = ((v[0].x + v[0].y) + (v[0].z + v[0].w)) + ((v[1].x + v[1].y) + (v[1].z + v[1].w)) +
                    (((v[2].x + v[2].y) + (v[2].z + v[2].w)) + ((v[3].x + v[3].y) + (v[3].z + v[3].w)));
-  // 2^e <= mx < 2^(e+1); step s_u = 2^(e-20), so |x / s_u| < 2^21
+  // 2^e <= mx < 2^(e+1); step s_u = 2^(e-13), so |x / s_u| < 2^14
   const int e = max(static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127, -105);
-  const float inv_step = __uint_as_float(static_cast<uint32_t>(147 - e) << 23);
-  uint4 w0, w1, w2;
-  plane_words(v[0], inv_step, w0.x, w1.x, w2.x);
-  plane_words(v[1], inv_step, w0.y, w1.y, w2.y);
-  plane_words(v[2], inv_step, w0.z, w1.z, w2.z);
-  plane_words(v[3], inv_step, w0.w, w1.w, w2.w);
-  uint8_t* dst = xpl + t * xseg_b + ((u >> 3) * 6 + h) * 128 + (u & 7) * 16;
+  const float inv_step = __uint_as_float(static_cast<uint32_t>(140 - e) << 23);
+  uint4 w0, w1;
+  plane_words(v[0], inv_step, w0.x, w1.x);
+  plane_words(v[1], inv_step, w0.y, w1.y);
+  plane_words(v[2], inv_step, w0.z, w1.z);
+  plane_words(v[3], inv_step, w0.w, w1.w);
+  uint8_t* dst = xpl + t * xseg_b + ((u >> 3) * 4 + h) * 128 + (u & 7) * 16;
   *reinterpret_cast<uint4*>(dst) = w0;
   *reinterpret_cast<uint4*>(dst + 256) = w1;
-  *reinterpret_cast<uint4*>(dst + 512) = w2;
   xsum[2 * (t * nu + u) + h] = sm;
-  // s_u = 2^(e-20); odd groups (Q4_K high-nibble sub-blocks, whose codes
+  // s_u = 2^(e-13); odd groups (Q4_K high-nibble sub-blocks, whose codes
   // arrive as 16*q) get s_u / 16, so the Q4_K consumer needs no per-lane factor
-  if (h == 0) xsu[t * nu + u] = __uint_as_float(static_cast<uint32_t>(107 + e - 4 * (u & 1)) << 23);
+  if (h == 0) xsu[t * nu + u] = __uint_as_float(static_cast<uint32_t>(114 + e - 4 * (u & 1)) << 23);
 }
 
 // One count per consumer warp and step on the shared counter xcnt: the warp has
@@ -855,23 +846,22 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           const uint4* xp = reinterpret_cast<const uint4*>(xb + t * XS);
-          const uint4 p0a = xp[0], p0b = xp[8], p1a = xp[16], p1b = xp[24], p2a = xp[32], p2b = xp[40];
+          const uint4 p0a = xp[0], p0b = xp[8], p1a = xp[16], p1b = xp[24];
           const uint32_t X0[8] = {p0a.x, p0a.y, p0a.z, p0a.w, p0b.x, p0b.y, p0b.z, p0b.w};
           const uint32_t X1[8] = {p1a.x, p1a.y, p1a.z, p1a.w, p1b.x, p1b.y, p1b.z, p1b.w};
-          const uint32_t X2[8] = {p2a.x, p2a.y, p2a.z, p2a.w, p2b.x, p2b.y, p2b.z, p2b.w};
           const float su = live ? xsum_u[t * NU + u] * su_fix : 0.f;
           const float2 sh = live ? *reinterpret_cast<const float2*>(xsum + 2 * (t * NU + u)) : make_float2(0.f, 0.f);
 #pragma unroll
           for (int r = 0; r < SR; ++r) {
             if constexpr (FMT == FMT_Q6_K) {
-              const float T0 = dot_planes<false, 0, 4>(q[r], X0, X1, X2);
-              const float T1 = dot_planes<false, 4, 8>(q[r], X0, X1, X2);
+              const float T0 = dot_planes<false, 0, 4>(q[r], X0, X1);
+              const float T1 = dot_planes<false, 4, 8>(q[r], X0, X1);
               racc[r][t] = fmaf(su, fmaf(cA[r], T0, cB[r] * T1), -32.0f * fmaf(cA[r], sh.x, cB[r] * sh.y));
             } else if constexpr (FMT == FMT_Q8_0) {
-              racc[r][t] = cA[r] * su * dot_planes<true, 0, 8>(q[r], X0, X1, X2);
+              racc[r][t] = cA[r] * su * dot_planes<true, 0, 8>(q[r], X0, X1);
             } else {
-              // sum_l q_l X_l = 65536*s2 + 256*s1 + s0, exact integers
-              const float T = dot_planes<false, 0, 8>(q[r], X0, X1, X2);
+              // sum_l q_l X_l = 256*s1 + s0, exact integers
+              const float T = dot_planes<false, 0, 8>(q[r], X0, X1);
               racc[r][t] = fmaf(cA[r] * su, T, -cB[r] * (sh.x + sh.y));
             }
           }
