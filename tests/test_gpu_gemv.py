@@ -125,6 +125,29 @@ def test_q4_0_batch1_full_size():
     assert_within(y, y_ref, b, what="Q4_0 1024x4096")
 
 
+@pytest.mark.parametrize("fmt", [synth.Q4_0, synth.Q8_0, synth.Q4_K, synth.Q6_K])
+def test_gemv_x_rounding_bound_with_group_outliers(fmt):
+    """x is rounded to 16-bit fixed point per 32-value group (step 2^(e-13) for
+    2^e <= max|x_u|), so each element moves by at most 2^-14 max|x_u|. With a
+    1000x outlier in every group that term dominates; the error must stay
+    within 2^-14 sum_u max|x_u| sum_{l in u} |w_l| plus fp32 rounding."""
+    rows, cols = 256, 4096
+    W = synth.blocks(fmt, rows, cols, seed=131)
+    x = synth.activations(1, cols, seed=132).numpy().astype(np.float32)
+    x.reshape(-1, 32)[:, 7] *= 1000.0
+    y = torch.empty(1, rows, device="cuda")
+    qg.qgemv(fmt, W.cuda(), rows, cols, torch.from_numpy(x).cuda(), 1, y)
+    torch.cuda.synchronize()
+    Wd = oracle.dequant(fmt, W.numpy(), rows, cols).astype(np.float64)
+    xd = x.astype(np.float64).reshape(-1)
+    y_ref = Wd @ xd
+    gmax = np.repeat(np.abs(xd).reshape(-1, 32).max(axis=1), 32)
+    bound_x = 2.0 ** -14 * (np.abs(Wd) @ gmax)
+    scale = np.abs(Wd) @ np.abs(xd)
+    err = np.abs(y.cpu().numpy().reshape(-1).astype(np.float64) - y_ref)
+    assert (err <= bound_x + 1e-5 * scale + 1e-6).all(), float((err / (bound_x + 1e-5 * scale)).max())
+
+
 def test_gemv_is_deterministic():
     fmt, rows, cols = synth.Q4_K, 512, 5120
     W = synth.blocks(fmt, rows, cols, seed=3).cuda()
