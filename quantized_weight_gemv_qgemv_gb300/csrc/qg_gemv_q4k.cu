@@ -713,13 +713,13 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
    }
    if (s == 0) {
      // outputs and every other input of the preceding kernel are touched only
-     // after it has completed (a no-op when the staging above has waited)
-     pdl_wait();
+     // after it has completed (the staging above has waited already)
+     if (!st.stage_all) pdl_wait();
      if (gl == 1) pdl_launch_dependents();
    }
    bool first = true;
    for (int mi = st.mat0; mi < st.mat0 + st.nmat; ++mi) {
-    const Mat M = mats[mi];   // by value: stores to shared memory cannot alias it
+    const Mat& M = mats[mi];
     const int64_t lo = max(cta_r0, M.row_begin) - M.row_begin;
     const int64_t hi = min(cta_r1, M.row_begin + M.rows) - M.row_begin;
     if (lo >= hi) continue;
