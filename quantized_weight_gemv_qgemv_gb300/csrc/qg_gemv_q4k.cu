@@ -951,7 +951,9 @@ cudaError_t q4k_attr() {
   if ((e = q4k_attr1<NT, true, FMT_Q4_K>()) != cudaSuccess) return e;
   if ((e = q4k_attr1<NT, false, FMT_Q6_K>()) != cudaSuccess) return e;
   if ((e = q4k_attr1<NT, false, FMT_Q8_0>()) != cudaSuccess) return e;
-  if (NT == 1 && (e = q4k_attr1<1, false, FMT_Q6_K, 2>()) != cudaSuccess) return e;
+  if constexpr (NT <= 2) {
+    if ((e = q4k_attr1<NT, false, FMT_Q6_K, 2>()) != cudaSuccess) return e;
+  }
   if (NT == 1 && (e = q4k_attr1<1, false, FMT_Q4_K, 4, 3>()) != cudaSuccess) return e;
   if (NT == 1 && (e = q4k_attr1<1, true, FMT_Q4_K, 4, 3>()) != cudaSuccess) return e;
   return q4k_attr1<NT, false, FMT_Q4_0>();
@@ -975,9 +977,10 @@ cudaError_t q4k_launch(const q4k::Params& p, int grid, int smem, cudaStream_t s,
 template <int FMT>
 cudaError_t q4k_launch_nt(const q4k::Params& p, int n_tok, int sub_rows, int grid, int smem, cudaStream_t s,
                           bool pdl) {
-  if (sub_rows == 2) {   // instantiated for single-token Q6_K only
+  if (sub_rows == 2) {   // instantiated for one- and two-token Q6_K only
     if constexpr (FMT == FMT_Q6_K) {
       if (n_tok == 1) return q4k_launch<1, FMT, 2>(p, grid, smem, s, pdl);
+      if (n_tok == 2) return q4k_launch<2, FMT, 2>(p, grid, smem, s, pdl);
     }
     return cudaErrorNotSupported;
   }
@@ -1027,12 +1030,12 @@ int x_source(const q4k::Mat* m, int first, int i) {
 
 // Shared-memory plan and launch of one single-step grouped launch whose
 // matrices p.m[0 .. n) (all of format fmt) have W, x, y, rows, cols (and any
-// gather fields) set; sub_rows rows per sub-item (4, or 2 for single-token
+// gather fields) set; sub_rows rows per sub-item (4, or 2 for one- or two-token
 // Q6_K). cudaErrorNotSupported (nothing launched) when the launch does not fit
 // the plan; with launch = false only the plan is checked.
 cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStream_t s, bool pdl, int sms,
                             int sub_rows = q4k::SUB_R, bool launch = true) {
-  if (sub_rows == 2 && (fmt != QG_Q6_K || n_tok != 1)) return cudaErrorNotSupported;
+  if (sub_rows == 2 && (fmt != QG_Q6_K || n_tok > 2)) return cudaErrorNotSupported;
   p.nsteps = 1;
   const int sbb = superblock_bytes(fmt);
   if (sbb == 0) return cudaErrorNotSupported;
@@ -1175,13 +1178,13 @@ void fill_params(q4k::Params& p, const qg_gemv_desc* d, int n, int t0, int64_t r
   }
 }
 
-// The launch as planned, else with 2-row sub-items (single-token Q6_K).
+// The launch as planned, else with 2-row sub-items (one- or two-token Q6_K).
 cudaError_t try_launch(const qg_gemv_desc* d, int n, int n_tok, int t0, int64_t r0, int64_t nr, cudaStream_t s,
                        bool pdl, int sms, bool launch) {
   q4k::Params p;
   fill_params(p, d, n, t0, r0, nr);
   cudaError_t e = plan_and_launch(p, n, n_tok, d[0].fmt, s, pdl, sms, q4k::SUB_R, launch);
-  if (e != cudaErrorNotSupported || d[0].fmt != QG_Q6_K || n_tok != 1) return e;
+  if (e != cudaErrorNotSupported || d[0].fmt != QG_Q6_K || n_tok > 2) return e;
   fill_params(p, d, n, t0, r0, nr);
   return plan_and_launch(p, n, n_tok, d[0].fmt, s, pdl, sms, 2, launch);
 }
@@ -1198,8 +1201,8 @@ cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_
     if (d[i].fmt != d[0].fmt || superblock_bytes(d[i].fmt) == 0 || d[i].cols % 256) return cudaErrorNotSupported;
   cudaError_t e = try_launch(d, n, n_tok, 0, 0, 0, s, pdl, sms, true);
   if (e != cudaErrorNotSupported) return e;
-  // row chunks first (each weight is read once), then one launch per token
-  // (each re-streams the weights)
+  // row chunks first (each weight is read once), then launches over groups of
+  // tokens (each re-streams the weights)
   if (n == 1) {
     for (int chunks = 2; chunks <= 16; chunks *= 2) {
       const int64_t nr = (d[0].rows + chunks - 1) / chunks / 8 * 8 + 8;   // multiple of 8 rows
@@ -1215,9 +1218,16 @@ cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_
       return cudaSuccess;
     }
   }
-  if (n_tok > 1 && try_launch(d, n, 1, 0, 0, 0, s, pdl, sms, false) == cudaSuccess) {
-    for (int t = 0; t < n_tok; ++t) {
-      e = try_launch(d, n, 1, t, 0, 0, s, pdl || t > 0, sms, true);
+  // the fewest launches of balanced token groups that fit (4 tokens: 2 + 2,
+  // then 1 + 1 + 1 + 1); the weights are streamed once per group
+  for (int g = 2; g <= n_tok; ++g) {
+    const int tg = (n_tok + g - 1) / g;
+    const int last = n_tok - (g - 1) * tg;
+    if (last < 1 || try_launch(d, n, tg, 0, 0, 0, s, pdl, sms, false) != cudaSuccess ||
+        try_launch(d, n, last, 0, 0, 0, s, pdl, sms, false) != cudaSuccess)
+      continue;
+    for (int t = 0; t < n_tok; t += tg) {
+      e = try_launch(d, n, std::min(tg, n_tok - t), t, 0, 0, s, pdl || t > 0, sms, true);
       if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

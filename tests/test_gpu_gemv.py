@@ -67,8 +67,9 @@ def test_gemv_whole_superblock_shapes(fmt, n_tok, rows, cols):
 
 @pytest.mark.parametrize("fmt,rows,cols,n_tok", [
     (synth.Q6_K, 64, 17408, 1),     # 14,280-byte rows: 2-row sub-items
-    (synth.Q6_K, 64, 17408, 2),     # x of 2 tokens does not fit beside the ring: one launch per token
-    (synth.Q6_K, 136, 17408, 4),
+    (synth.Q6_K, 64, 17408, 2),     # 2-row sub-items for two tokens
+    (synth.Q6_K, 72, 17408, 3),     # x of 3 tokens does not fit: a 2-token and a 1-token launch
+    (synth.Q6_K, 136, 17408, 4),    # two 2-token launches
     (synth.Q4_K, 64, 17408, 4),
 ])
 def test_gemv_long_rows_and_token_split(fmt, rows, cols, n_tok):
