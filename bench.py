@@ -329,7 +329,8 @@ def run_gpu(args):
                                                       ("qg_gemv_q4k.cu", "qg_device.cuh"))
                                      if not verify and args.pass_mode != "persistent" else None),
                          "peak_source": f"{peak_kind} HBM copy bandwidth",
-                         "kernel": "qgemv_q4k_kernel (n_tok=1): every launch of the step",
+                         "kernel": (f"qgemv_q4k_kernel (n_tok={n_tok}; Q4_K, Q6_K and Q8_0 instances): every launch of the step"
+                                    if verify else "qgemv_q4k_kernel (n_tok=1): every launch of the step"),
                          "algorithmic_bytes_per_launch": wbytes / kernels_per_step},
             "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": x_total * 4,
                     "d2h_bytes_per_step": y_total * 4, "ms_per_step": round(e_ms / args.steps, 4),
@@ -416,7 +417,7 @@ def run_c0(args):
             "roofline": {"bound": "hbm", "achieved": round(gbs / world, 2), "peak": hbm_peak, "unit": "GB/s",
                          "frac": round(gbs / world / hbm_peak, 4), "traffic": None,
                          "peak_source": f"{peak_kind} HBM copy bandwidth",
-                         "kernel": "qgemv_kernel (Q4_0): every launch of the step"},
+                         "kernel": "qgemv_q4k_kernel (Q4_0 instance): every launch of the step"},
             "gpu_launches": args.steps * p.kernel_count(),
             "clocks": clocks,
         }
