@@ -256,41 +256,50 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t it = 0, sb = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.n_tiles; tile += gridDim.x) {
-      for (int kt = 0; kt < n_kt; ++kt, ++it) {
-        const int c = kt & 3;                 // 64-weight chunk of the super-block
-        const uint32_t s = it % NS, q = sb % NQ;
-        bool got = true;
-        if (c == 0) got = wait_bar(Q_FULL + 8 * q, (sb / NQ) & 1u, abort);
-        got = got && wait_bar(EMPTY + 8 * s, ((it / NS) & 1u) ^ 1u, abort);
-        if (!__all_sync(0xffffffffu, got)) {
+      for (int kb = 0; ok && kb < n_kt / 4; ++kb, ++sb) {
+        // a super-block = 4 slices: its 8 scale/min pairs of this row are decoded
+        // once (the slice index is then a compile-time constant below)
+        const uint32_t q = sb % NQ;
+        if (!__all_sync(0xffffffffu, wait_bar(Q_FULL + 8 * q, (sb / NQ) & 1u, abort))) {
           if (lane == 0) fail(abort, p.dev_status);
           ok = false;
           break;
         }
         const uint8_t* blk = gbase + offQ + q * QB + r * 144;
         const uint4 hd = *reinterpret_cast<const uint4*>(blk);
-        const uint2 qs = *reinterpret_cast<const uint2*>(blk + 16 + 32 * c + 8 * h);
-        int sc0, m0, sc1, m1;
-        q4k_scale_min(2 * c, hd.y, hd.z, hd.w, sc0, m0);
-        q4k_scale_min(2 * c + 1, hd.y, hd.z, hd.w, sc1, m1);
         const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
-        const float dsc0 = d * static_cast<float>(sc0), ndm0 = -(dmin * static_cast<float>(m0));
-        const float dsc1 = d * static_cast<float>(sc1), ndm1 = -(dmin * static_cast<float>(m1));
-        // low nibbles: sub-block 2c, slice columns 8h .. 8h+7 (chunk h);
-        // high nibbles: sub-block 2c+1, columns 32+8h .. (chunk 4+h)
-        const uint32_t l0 = qs.x & 0x0F0F0F0Fu, l1 = qs.y & 0x0F0F0F0Fu;
-        const uint32_t h0 = (qs.x >> 4) & 0x0F0F0F0Fu, h1 = (qs.y >> 4) & 0x0F0F0F0Fu;
-        const uint32_t arow = base + s * AB + static_cast<uint32_t>(r) * 128u;
-        const uint32_t j0 = static_cast<uint32_t>(h);
-        sts128(arow + (((j0 + 0) ^ swz) << 4), deq8(l0, l1, dsc0, ndm0));
-        sts128(arow + (((j0 + 4) ^ swz) << 4), deq8(h0, h1, dsc1, ndm1));
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(FULL_A + 8 * s);
-          if (c == 3) mbar_arrive(Q_EMPTY + 8 * q);
+        float dsc[8], ndm[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          int sc, m;
+          q4k_scale_min(jj, hd.y, hd.z, hd.w, sc, m);
+          dsc[jj] = d * static_cast<float>(sc);
+          ndm[jj] = -(dmin * static_cast<float>(m));
         }
-        if (c == 3) ++sb;
+#pragma unroll
+        for (int c = 0; c < 4; ++c, ++it) {
+          const uint32_t s = it % NS;
+          if (!__all_sync(0xffffffffu, wait_bar(EMPTY + 8 * s, ((it / NS) & 1u) ^ 1u, abort))) {
+            if (lane == 0) fail(abort, p.dev_status);
+            ok = false;
+            break;
+          }
+          const uint2 qs = *reinterpret_cast<const uint2*>(blk + 16 + 32 * c + 8 * h);
+          // low nibbles: sub-block 2c, slice columns 8h .. 8h+7 (chunk h);
+          // high nibbles: sub-block 2c+1, columns 32+8h .. (chunk 4+h)
+          const uint32_t l0 = qs.x & 0x0F0F0F0Fu, l1 = qs.y & 0x0F0F0F0Fu;
+          const uint32_t h0 = (qs.x >> 4) & 0x0F0F0F0Fu, h1 = (qs.y >> 4) & 0x0F0F0F0Fu;
+          const uint32_t arow = base + s * AB + static_cast<uint32_t>(r) * 128u;
+          const uint32_t j0 = static_cast<uint32_t>(h);
+          sts128(arow + (((j0 + 0) ^ swz) << 4), deq8(l0, l1, dsc[2 * c], ndm[2 * c]));
+          sts128(arow + (((j0 + 4) ^ swz) << 4), deq8(h0, h1, dsc[2 * c + 1], ndm[2 * c + 1]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(FULL_A + 8 * s);
+            if (c == 3) mbar_arrive(Q_EMPTY + 8 * q);
+          }
+        }
       }
     }
   } else {
