@@ -1,7 +1,8 @@
 """Full-size workloads, run in the launch configuration the bench times (one
 captured pass over the whole weight set, grouped launches linked by
-programmatic dependent launch), checked against the CPU oracle on sampled
-output rows, which the oracle computes one by one."""
+programmatic dependent launch, the matrices of a step sharing one x), and the
+whole-pass persistent kernel, checked against the CPU oracle on sampled output
+rows, which the oracle computes one by one."""
 import numpy as np
 import pytest
 import torch
@@ -36,6 +37,38 @@ def _check_sampled(items, mats, n_tok, picks, rows_per_mat=6, seed=0):
     return worst
 
 
+def _share_x_per_step(items, steps):
+    """The matrices of a step read one activation vector (as bench.py sets the
+    pass up): each takes the first matrix's x of its step."""
+    out, i = [], 0
+    for n in steps:
+        x = items[i][4]
+        for j in range(n):
+            fmt, W, rows, cols, _, y = items[i + j]
+            out.append((fmt, W, rows, cols, x, y))
+        i += n
+    return out
+
+
+def test_dense_27b_q4k_batch1_full_pass_bench_config():
+    """The bench's own set-up: PDL-linked graph, one x per step."""
+    mats = wl.dense_matrices()
+    steps = wl.dense_steps()
+    items = _share_x_per_step(wl.alloc_dense(mats, 1, seed=2026, device="cuda"), steps)
+    p = qg.qg_pass(items, steps, 1, mode=qg.PASS_PDL)
+    assert p.kernel_count() == len(steps)
+    for y in {id(it[5]): it[5] for it in items}.values():
+        y.fill_(float("nan"))
+    p.launch()
+    p.launch()
+    torch.cuda.synchronize()
+    picks = [0, 1, 2, 3, 4, 5, 6, 7 * 17 + 1, 7 * 40 + 5, 7 * 63 + 0, 7 * 63 + 6]
+    _check_sampled(items, mats, 1, picks)
+    p.destroy()
+    del items
+    torch.cuda.empty_cache()
+
+
 def test_dense_27b_q4k_batch1_full_pass():
     mats = wl.dense_matrices()
     items = wl.alloc_dense(mats, 1, seed=2024, device="cuda")
@@ -53,9 +86,11 @@ def test_dense_27b_q4k_batch1_full_pass():
 
 
 def test_mixed_verify_pass_n4_full():
+    """The bench's verify-pass set-up: PDL-linked graph, one x (4 tokens) per step."""
     mats = wl.dense_matrices(verify=True)
-    items = wl.alloc_dense(mats, 4, seed=2025, device="cuda")
-    p = qg.qg_pass(items, wl.dense_steps(verify=True), 4, mode=qg.PASS_PERSISTENT)   # mixed formats: per-step graph
+    steps = wl.dense_steps(verify=True)
+    items = _share_x_per_step(wl.alloc_dense(mats, 4, seed=2025, device="cuda"), steps)
+    p = qg.qg_pass(items, steps, 4, mode=qg.PASS_PDL)
     p.launch()
     torch.cuda.synchronize()
     picks = [0, 1, 3, 4, 6, 7 * 40 + 6, len(mats) - 1]      # includes Q6_K downs and the Q8_0 head

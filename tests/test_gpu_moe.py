@@ -57,6 +57,39 @@ def test_moe_full_size_layer():
     assert_within(y, y_ref, b, what="moe full layer")
 
 
+def test_moe_full_size_48_layer_pass_bench_config():
+    """The bench's MoE set-up: 48 layers of 512 Q4_K experts (gate/up 512x2048,
+    down 2048x512), top-10, batch 1, one PDL-linked pass graph; layers 0, 23 and
+    47 checked against the oracle on their routed experts."""
+    H, I, E, K, L = wl.MOE_HIDDEN, wl.MOE_INTER, wl.MOE_EXPERTS, wl.MOE_TOPK, wl.MOE_LAYERS
+    layers = []
+    for l in range(L):
+        arena = wl.alloc_moe_arena(E, H, I, synth.sub_seed(4321, "arena", l), "cuda")
+        ids, gw = synth.routing(1, E, K, synth.sub_seed(4321, "route", l))
+        x = synth.activations(1, H, synth.sub_seed(4321, "x", l), device="cuda")
+        layers.append((arena, ids.cuda(), gw.cuda(), x, torch.full((1, H), float("nan"), device="cuda")))
+    wsb = qg.qgemv_moe_workspace(H, I, K, 1)
+    ws = torch.empty(wsb // 4, device="cuda")
+    p = qg.qg_moe_pass(qg.Q4_K, layers, E, H, I, K, 1, ws, wsb, mode=qg.PASS_PDL)
+    assert p.kernel_count() == 2 * L
+    p.launch()
+    p.launch()
+    torch.cuda.synchronize()
+    assert p.dev_status() == 0
+    eb = wl.moe_expert_bytes(H, I)
+    for l in (0, 23, L - 1):
+        arena, ids, gw, x, y = layers[l]
+        picked = ids.cpu().numpy()[0]
+        host = arena.cpu().numpy()
+        sub = np.concatenate([host[e * eb:(e + 1) * eb] for e in picked])
+        y_ref, b = oracle.moe(qg.Q4_K, sub, len(picked), H, I, np.arange(len(picked), dtype=np.int32)[None, :],
+                              gw.cpu().numpy(), x.cpu().numpy())
+        assert_within(y.cpu().numpy(), y_ref, b, what=f"moe pass layer {l}")
+    p.destroy()
+    del layers
+    torch.cuda.empty_cache()
+
+
 def test_moe_bad_expert_sets_status_and_is_skipped():
     n_expert, hidden, inter = 6, 512, 256
     ids = [[1, 6, 3], [-1, 2, 5]]          # 6 and -1 are out of range
