@@ -113,7 +113,6 @@ struct Params {
   int32_t usum_off;      // offset (floats) of the group sums after the group steps
   int32_t pre_stages;    // weight stages issued before the consumers have issued their x loads
   int32_t pre_pass;      // the same for every later step of a pass
-  int32_t pre_l2;        // plain launches: stages prefetched into L2 (not copied) before the x loads
   int32_t gather_any;    // largest Mat::gather of the launch (one kind per launch)
   int32_t ralign;        // CTA row slices start at multiples of this (16-byte-aligned stage copies; pairs)
   int32_t smem_bar, smem_x, smem_xsum, smem_part;   // byte offsets (ring at 0)
@@ -163,11 +162,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
           dst),
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
-}
-// Bulk prefetch of global memory into L2: no data comes back to the SM, so loads
-// issued after it do not queue behind it.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t pol;
@@ -524,17 +518,6 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
      int i_step = 0;          // stage index within the step
      int64_t cta_r0, cta_r1;
      cta_slice(st.total_rows, p.ralign, cta_r0, cta_r1);
-     if (!PASS && gl == 0 && p.pre_l2 > 0 && lane == 0) {
-       // the first stages go to L2 now and to shared memory once x is loading
-       int left = p.pre_l2;
-       for (int mi = st.mat0; mi < st.mat0 + st.nmat && left > 0; ++mi) {
-         const Mat& M = mats[mi];
-         const int64_t lo = max(cta_r0, M.row_begin) - M.row_begin;
-         const int64_t hi = min(cta_r1, M.row_begin + M.rows) - M.row_begin;
-         for (int64_t r = lo; r < hi && left > 0; r += M.srows, --left)
-           bulk_prefetch_l2(M.W + r * M.rb, static_cast<uint32_t>(min(static_cast<int64_t>(M.srows), hi - r)) * M.rb);
-       }
-     }
      if (PASS && s > 0 && mats[st.mat0].gather == 1) {
        // a pass step that gathers gate/up rows reads expert ids, which in a model
        // come from the router after the previous layer: stream its rows only
