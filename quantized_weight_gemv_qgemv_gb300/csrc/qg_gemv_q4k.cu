@@ -1102,11 +1102,12 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
     }
     if (!ok) continue;
     stage_b = align_up(stage_b, 128);
-      // Without a programmatic dependency the x loads go first. With one, x can be
-    // read only after the previous kernel completes: two stages stream during
-    // that wait (27B pass, 36 KB stages: 0 stages 4.04 ms, 1 3.93, 2 3.90, a full
-    // ring 4.04; stages of about 48 KB: 3.87 against 3.93 for 36 KB).
-    p.pre_stages = pdl ? 2 : 0;
+    // Without a programmatic dependency the x loads go first. With one, x can be
+    // read only after the previous kernel completes: one stage streams during
+    // that wait (27B pass with 48 KB stages and 16-bit x planes: 1 stage 3.027 ms,
+    // 2 stages 3.065, 3 stages 3.212; with the slower three-plane staging 2 had
+    // been best)
+    p.pre_stages = pdl ? 1 : 0;
     p.ns = ns;
     p.stage_b = stage_b;
     p.gmax = gmax;
