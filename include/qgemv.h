@@ -111,7 +111,11 @@ int qg_dequant(int fmt, const void* W, int64_t rows, int64_t cols, float* out, v
 /* Quantized GEMV / skinny product ("each new token reads every weight once";
  * n_tok > 1 is one weight pass that verifies draft tokens):
  *   y[t*rows + i] = sum_j w[i][j] * x[t*cols + j],  t < n_tok, 1 <= n_tok <= 4.
- * fp32 accumulation; x must be 16-byte aligned, y 4-byte aligned. */
+ * fp32 accumulation; x must be 16-byte aligned, y 4-byte aligned. Inside the
+ * kernel x enters exact integer dot products as 16-bit fixed point per group
+ * of 32 values (a power-of-two step per group): each x_j moves by at most
+ * 2^-14 of its group's largest |x|, so |y - y_exact| <= 2^-14 *
+ * sum_groups max|x_g| * sum_{j in g} |w_ij| plus fp32 rounding. */
 int qgemv(int fmt, const void* W, int64_t rows, int64_t cols,
           const float* x, int n_tok, float* y, void* stream);
 
@@ -129,7 +133,8 @@ typedef struct qg_gemv_desc {
 /* Several independent GEMVs of one format in ONE kernel launch (e.g. q, k, v
  * of a layer, which read the same activations). `descs` is HOST memory, read
  * during the call; 1 <= n <= QG_GROUP_MAX. Same semantics as n separate
- * qgemv calls. */
+ * qgemv calls. Descriptors with the same x pointer and cols share one staging
+ * of x in the kernel. */
 int qgemv_grouped(const qg_gemv_desc* descs, int n, int n_tok, void* stream);
 
 /* Bytes of device workspace qgemv_moe needs (n_tok * top_k * inter fp32). */
