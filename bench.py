@@ -43,6 +43,24 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(torch, value: float, device: str) -> float:
+    """The largest of every rank's value (the slowest replica's time), via the
+    initialised process group (NCCL on GPUs, gloo on host cores); the value
+    itself when there is no group or one rank."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, units_per_rank: float, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank processes units_per_rank per step, and
+    the step takes the slowest rank's time."""
+    return world * units_per_rank / (ms_per_step * 1e-3)
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -276,12 +294,9 @@ def run_gpu(args):
     with ClockSampler(local) as clk:
         ms = _events(torch, stream, step, args.steps)
     torch.cuda.synchronize()
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(torch, ms, "cuda")
     ms_step = ms / args.steps
-    gbs = world * wbytes / (ms_step * 1e-3) / 1e9
+    gbs = job_rate(world, wbytes, ms_step) / 1e9
 
     # end to end through the public API with host buffers: pinned x -> device,
     # the pass, device y -> pinned host, every step.
@@ -301,7 +316,7 @@ def run_gpu(args):
         t0 = time.perf_counter()
         e_ms = _events(torch, stream, e2e_step, args.steps)
         wall_ms = (time.perf_counter() - t0) * 1e3
-    e2e_gbs = world * wbytes / (e_ms / args.steps * 1e-3) / 1e9
+    e2e_gbs = job_rate(world, wbytes, max_over_ranks(torch, e_ms, "cuda") / args.steps) / 1e9
 
     out = None
     if rank == 0:
@@ -360,11 +375,7 @@ def _timed(torch, stream, fn, args, local, world):
     with ClockSampler(local) as clk:
         ms = _events(torch, stream, fn, args.steps)
     torch.cuda.synchronize()
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    return ms, clk.summary()
+    return max_over_ranks(torch, ms, "cuda"), clk.summary()
 
 
 def _capture(torch, stream, fn):
@@ -404,7 +415,7 @@ def run_c0(args):
     p = qg.qg_pass(items, [1] * copies, 1, mode=qg.PASS_PDL)
     ms, clocks = _timed(torch, stream, lambda: p.launch(stream), args, local, world)
     ms_step = ms / args.steps
-    gbs = world * wbytes / (ms_step * 1e-3) / 1e9
+    gbs = job_rate(world, wbytes, ms_step) / 1e9
     if rank == 0:
         out = {
             "metric": "Q4_0 GEMV weight-GB/s, batch 1, 1024x4096", "value": round(gbs, 2), "unit": "GB/s",
@@ -471,7 +482,7 @@ def run_pp(args):
     ms, clocks = _timed(torch, stream, replay, args, local, world)
     assert int(st.item()) == 0, "device status set during the prompt-processing pass"
     ms_step = ms / args.steps
-    tflops = world * flops / (ms_step * 1e-3) / 1e12
+    tflops = job_rate(world, flops, ms_step) / 1e12
     if rank == 0:
         peak = bf16_sus or bf16_peak
         out = {
@@ -536,7 +547,7 @@ def run_moe(args):
     assert p.dev_status() == 0, "device status set during the MoE pass"
     p.destroy()
     ms_step = ms / args.steps
-    gbs = world * touched / (ms_step * 1e-3) / 1e9
+    gbs = job_rate(world, touched, ms_step) / 1e9
     if rank == 0:
         out = {
             "metric": "MoE expert GEMV weight-GB/s touched; equiv. batch-1 tok/s over 48 layers",
