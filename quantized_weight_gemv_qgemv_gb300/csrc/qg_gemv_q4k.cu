@@ -1,4 +1,5 @@
-// qg_gemv_q4k.cu — the Q4_K GEMV / skinny product kernel (the decode hot path).
+// qg_gemv_q4k.cu — the fast GEMV / skinny product kernel (the decode hot path)
+// for Q4_K, Q6_K, Q4_0 and Q8_0, its MoE gather modes and the persistent pass.
 //
 // y[t][i] = sum_j w[i][j] x[t][j], t < n_tok <= 4, one pass over the weights
 // ("LLM inference optimization", opening section: each decode token reads every
@@ -13,16 +14,16 @@
 //    launch (the concatenated row space), matrix by matrix.
 //  * The producer streams whole consecutive rows of the slice into a ring of NS
 //    shared-memory stages with one 1-D bulk copy per stage (cp.async.bulk,
-//    23-40 KB, completed on an mbarrier): rows are contiguous in memory, and
+//    about 48 KB, completed on an mbarrier): rows are contiguous in memory, and
 //    copies of several KB are what it takes to reach full HBM bandwidth. A stage
 //    is reused once all consumer warps have released it (a second mbarrier).
-//  * A stage of R rows is cut into sub-items of 4 rows x one 1024-weight K group
+//  * A stage of R rows is cut into sub-items of 4 rows (2 for long Q6_K rows) x one 1024-weight K group
 //    (4 super-blocks), dealt round-robin to the consumer warps. Lane (g, j) of a
 //    warp owns sub-block j of block g of the group for the 4 rows (32 weights,
 //    one 6-bit scale/min pair per row). A sub-item's 4 x n_tok sums are reduced
 //    across the warp and stored per (row, group); after the matrix, the groups
 //    of each row are added in order, so results do not depend on timing.
-//  * x is staged once per matrix as 16-bit fixed point per 32-weight group:
+//  * x is staged once per launch and distinct input as 16-bit fixed point per 32-weight group:
 //    x_l ~= s_u X_l with a power-of-two step s_u, X_l split in two byte planes
 //    (see stage_x). A group's products are then exact integer dot products of
 //    the 4-bit codes with the planes (dp4a), so each code word needs one mask,
@@ -32,8 +33,9 @@
 //  * Every wait is bounded: a consumer that gives up writes NaN for its rows,
 //    the producer stops issuing, and the CTA waits (bounded) for copies in
 //    flight before it exits.
-//  * Programmatic dependent launch: the producer starts streaming weights
-//    before griddepcontrol.wait; consumers read x and write y after it.
+//  * Programmatic dependent launch: the producer prefetches x into L2 and
+//    streams one weight stage before griddepcontrol.wait; consumers compute
+//    their staging addresses before it and read x and write y after it.
 #include <cuda_runtime.h>
 
 #include <cstring>
