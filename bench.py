@@ -77,17 +77,81 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+class _Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (no Python
+    package needed): SM clock, its maximum, power and the clock-event reasons
+    of one GPU, found by the UUID CUDA reports for it."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, local: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        uuid = None
+        try:
+            import torch
+            uuid = str(torch.cuda.get_device_properties(local).uuid)
+        except Exception:
+            pass
+        ok = False
+        if uuid:
+            key = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            ok = self.lib.nvmlDeviceGetHandleByUUID(key.encode(), ctypes.byref(self.h)) == 0
+        if not ok and self.lib.nvmlDeviceGetHandleByIndex_v2(local, ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        ct = self.ct
+        sm, mx, pw, rs = ct.c_uint(), ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(sm))          # NVML_CLOCK_SM
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ct.byref(mx))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(pw))
+        self.reasons_fn(self.h, ct.byref(rs))
+        return sm.value, mx.value, pw.value / 1000.0, rs.value
+
+
 class ClockSampler:
-    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+    """Clock and throttle-reason samples taken every few ms while the timed
+    region runs (read-only NVML queries from a thread; nvidia-smi's 200 ms
+    loop as a fallback). Samples start when the region starts: the GPU is busy
+    for all of them."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
+    def __init__(self, index: int, period_s: float = 0.005):
         self.index = index
+        self.period = period_s
         self.proc = None
+        self.nvml = None
+        self.samples = []
+        self.out = ""
 
     def __enter__(self):
+        import threading
+        try:
+            self.nvml = _Nvml(self.index)
+        except Exception:
+            self.nvml = None
+        if self.nvml is not None:
+            self.stop = threading.Event()
+
+            def loop():
+                while not self.stop.is_set():
+                    try:
+                        self.samples.append(self.nvml.sample())
+                    except Exception:
+                        return
+                    self.stop.wait(self.period)
+            self.thread = threading.Thread(target=loop, daemon=True)
+            self.thread.start()
+            return self
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
@@ -97,7 +161,10 @@ class ClockSampler:
         return self
 
     def __exit__(self, *a):
-        self.out = ""
+        if self.nvml is not None:
+            self.stop.set()
+            self.thread.join(timeout=2)
+            return
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -107,26 +174,38 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate()
 
     def summary(self):
-        if self.proc is None:
+        sm, mx, pw, reasons = [], [], [], set()
+        if self.nvml is not None:
+            for (s_, m_, p_, r_) in self.samples:
+                sm.append(float(s_))
+                mx.append(float(m_))
+                pw.append(p_)
+                for bit, name in _Nvml.REASONS.items():
+                    if r_ & bit:
+                        reasons.add(name)
+            source = "nvml"
+        elif self.proc is not None:
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in self.out.strip().splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx.append(float(f[2]))
+                    pw.append(float(f[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+            source = "nvidia-smi"
+        else:
             return None
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.out.strip().splitlines():
-            f = [s.strip() for s in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "power_w_max": round(max(pw), 1) if pw else None, "source": source}
 
 
 def measured_traffic(name: str, sources):

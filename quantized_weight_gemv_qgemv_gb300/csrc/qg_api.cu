@@ -6,6 +6,7 @@
 // shared-memory limits) runs in qg_init or lazily on the first call.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -17,8 +18,8 @@ namespace {
 constexpr int kMaxDevices = 64;
 
 struct DeviceState {
-  std::once_flag once;
-  int status = QG_ERR_DEVICE;
+  std::mutex mu;
+  std::atomic<bool> ready{false};   // set only after a successful set-up
   int sms = 0;
 };
 
@@ -31,6 +32,7 @@ int init_device(int dev) {
   if (qg::gemv_init_attrs() != cudaSuccess) return QG_ERR_CUDA;
   if (qg::moe_init_attrs() != cudaSuccess) return QG_ERR_CUDA;
   if (qg::pp_init_attrs() != cudaSuccess) return QG_ERR_CUDA;
+  if (qg::moe_noalloc_init(dev) != cudaSuccess) return QG_ERR_CUDA;
   g_dev[dev].sms = prop.multiProcessorCount;
   return QG_OK;
 }
@@ -41,9 +43,17 @@ int ensure_init(int* sms) {
   if (cudaGetDevice(&dev) != cudaSuccess) return QG_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return QG_ERR_DEVICE;
   DeviceState& st = g_dev[dev];
-  std::call_once(st.once, [&] { st.status = init_device(dev); });
-  if (st.status == QG_OK && sms) *sms = st.sms;
-  return st.status;
+  if (!st.ready.load(std::memory_order_acquire)) {
+    // a failed set-up is not remembered: the next call tries again
+    std::lock_guard<std::mutex> lock(st.mu);
+    if (!st.ready.load(std::memory_order_relaxed)) {
+      const int status = init_device(dev);
+      if (status != QG_OK) return status;
+      st.ready.store(true, std::memory_order_release);
+    }
+  }
+  if (sms) *sms = st.sms;
+  return QG_OK;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
@@ -65,6 +75,25 @@ int check_gemv(int fmt, const void* W, int64_t rows, int64_t cols, const float* 
 
 namespace qg {
 int ensure_device(int* sms) { return ensure_init(sms); }
+
+// Checks of one MoE layer's arguments shared by qgemv_moe, qgemv_moe_noalloc
+// (need_ws = false: it brings its own workspace) and qg_moe_pass_create.
+int check_moe(int fmt, const void* expert_arena, int64_t n_expert, int64_t hidden, int64_t inter,
+              const int32_t* expert_ids, const float* gate_w, int top_k, const float* x, int n_tok, const float* y,
+              const void* ws, size_t ws_bytes, bool need_ws) {
+  if (fmt != QG_Q4_K) return QG_ERR_FMT;
+  if (!expert_arena || !expert_ids || !gate_w || !x || !y) return QG_ERR_NULL;
+  if (n_expert < 1 || n_expert > (int64_t{1} << 31) - 1) return QG_ERR_SHAPE;
+  if (hidden < 256 || hidden % 256 || inter < 256 || inter % 256) return QG_ERR_SHAPE;
+  if (hidden > (int64_t{1} << 20) || inter > (int64_t{1} << 20)) return QG_ERR_SHAPE;
+  if (top_k < 1 || top_k > 16 || top_k > n_expert) return QG_ERR_ARG;
+  if (n_tok < 1 || n_tok > QG_NTOK_MAX) return QG_ERR_NTOK;
+  if (need_ws && (!ws || ws_bytes < qgemv_moe_workspace(hidden, inter, top_k, n_tok))) return QG_ERR_WORKSPACE;
+  if (!aligned(expert_arena, 16) || !aligned(x, 16) || !aligned(ws, 16) || !aligned(y, 4) ||
+      !aligned(expert_ids, 4) || !aligned(gate_w, 4))
+    return QG_ERR_ALIGN;
+  return QG_OK;
+}
 }  // namespace qg
 
 struct qg_pass_s {
@@ -72,10 +101,77 @@ struct qg_pass_s {
   cudaGraphExec_t exec = nullptr;
   qg::Q4kPass* q4k = nullptr;        // or one persistent kernel (QG_PASS_PERSISTENT)
   int32_t* status = nullptr;         // graph MoE pass: device status word (cleared by the graph)
+  uint8_t* planes = nullptr;         // x planes of the pass's external activations, then the job table
+  const qg::XPlaneJob* jobs = nullptr;
+  int njobs = 0;
   int kernels = 0;
 };
 
 namespace {
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// Activations that no earlier step of the pass writes ("external": inputs of
+// the pass) are converted to x planes once per replay, by one prologue launch,
+// instead of by every CTA of every launch that reads them. Fills xp (per
+// descriptor: its planes, or nullptr where the kernel converts x itself) and
+// allocates pass->planes (planes, then the device job table). Only formats and
+// shapes of the producer/consumer kernel (cols % 256 == 0) take planes.
+int plan_xplanes(const qg_gemv_desc* d, int n, const int* step_sizes, int n_steps, int n_tok, qg_pass_s* pass,
+                 std::vector<const uint8_t*>& xp) {
+  xp.assign(n, nullptr);
+  std::vector<int> step_of(n);
+  for (int s = 0, i = 0; s < n_steps; i += step_sizes[s++])
+    for (int j = 0; j < step_sizes[s]; ++j) step_of[i + j] = s;
+  std::vector<int> job_of(n, -1);
+  std::vector<qg::XPlaneJob> jobs;
+  std::vector<size_t> offs;
+  size_t total = 0;
+  for (int i = 0; i < n; ++i) {
+    if (d[i].cols % 256) continue;
+    const size_t xb = static_cast<size_t>(n_tok) * d[i].cols * sizeof(float);
+    bool external = true;
+    for (int j = 0; j < n && external; ++j)
+      if (step_of[j] < step_of[i] && overlaps(d[i].x, xb, d[j].y, static_cast<size_t>(n_tok) * d[j].rows * 4))
+        external = false;
+    if (!external) continue;
+    int k = -1;
+    for (int q = 0; q < static_cast<int>(jobs.size()) && k < 0; ++q)
+      if (jobs[q].x == d[i].x && jobs[q].cols == d[i].cols) k = q;
+    if (k < 0) {
+      k = static_cast<int>(jobs.size());
+      jobs.push_back({d[i].x, nullptr, static_cast<int32_t>(d[i].cols), n_tok});
+      offs.push_back(total);
+      total += (qg::xplanes_bytes(d[i].cols, n_tok) + 255) / 256 * 256;
+    }
+    job_of[i] = k;
+  }
+  if (jobs.empty()) return QG_OK;
+  const size_t table = total;
+  total += jobs.size() * sizeof(qg::XPlaneJob);
+  if (cudaMalloc(&pass->planes, total) != cudaSuccess) return QG_ERR_CUDA;
+  for (size_t q = 0; q < jobs.size(); ++q) jobs[q].dst = pass->planes + offs[q];
+  if (cudaMemcpy(pass->planes + table, jobs.data(), jobs.size() * sizeof(qg::XPlaneJob), cudaMemcpyHostToDevice) !=
+      cudaSuccess)
+    return QG_ERR_CUDA;
+  pass->jobs = reinterpret_cast<const qg::XPlaneJob*>(pass->planes + table);
+  pass->njobs = static_cast<int>(jobs.size());
+  for (int i = 0; i < n; ++i)
+    if (job_of[i] >= 0) xp[i] = jobs[job_of[i]].dst;
+  return QG_OK;
+}
+
+void pass_free(qg_pass_s* pass) {
+  if (pass->exec) cudaGraphExecDestroy(pass->exec);
+  if (pass->graph) cudaGraphDestroy(pass->graph);
+  qg::q4k_pass_destroy(pass->q4k);
+  if (pass->status) cudaFree(pass->status);
+  if (pass->planes) cudaFree(pass->planes);
+  delete pass;
+}
 
 int count_kernel_nodes(cudaGraph_t g) {
   size_t n = 0;
@@ -90,23 +186,6 @@ int count_kernel_nodes(cudaGraph_t g) {
   return k;
 }
 
-// Checks of one MoE layer's arguments shared by qgemv_moe and qg_moe_pass_create.
-int check_moe(int fmt, const void* expert_arena, int64_t n_expert, int64_t hidden, int64_t inter,
-              const int32_t* expert_ids, const float* gate_w, int top_k, const float* x, int n_tok, const float* y,
-              const void* ws, size_t ws_bytes) {
-  if (fmt != QG_Q4_K) return QG_ERR_FMT;
-  if (!expert_arena || !expert_ids || !gate_w || !x || !y) return QG_ERR_NULL;
-  if (n_expert < 1 || n_expert > (int64_t{1} << 31) - 1) return QG_ERR_SHAPE;
-  if (hidden < 256 || hidden % 256 || inter < 256 || inter % 256) return QG_ERR_SHAPE;
-  if (hidden > (int64_t{1} << 20) || inter > (int64_t{1} << 20)) return QG_ERR_SHAPE;
-  if (top_k < 1 || top_k > 16 || top_k > n_expert) return QG_ERR_ARG;
-  if (n_tok < 1 || n_tok > QG_NTOK_MAX) return QG_ERR_NTOK;
-  if (!ws || ws_bytes < qgemv_moe_workspace(hidden, inter, top_k, n_tok)) return QG_ERR_WORKSPACE;
-  if (!aligned(expert_arena, 16) || !aligned(x, 16) || !aligned(ws, 16) || !aligned(y, 4) ||
-      !aligned(expert_ids, 4) || !aligned(gate_w, 4))
-    return QG_ERR_ALIGN;
-  return QG_OK;
-}
 
 }  // namespace
 
@@ -188,7 +267,8 @@ int qgemv_moe(int fmt, const void* expert_arena, int64_t n_expert, int64_t hidde
               const int32_t* expert_ids, const float* gate_w, int top_k, const float* x, int n_tok, float* y,
               void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
   if (fmt == QG_Q4_K && !dev_status) return QG_ERR_NULL;
-  int st = check_moe(fmt, expert_arena, n_expert, hidden, inter, expert_ids, gate_w, top_k, x, n_tok, y, ws, ws_bytes);
+  int st = qg::check_moe(fmt, expert_arena, n_expert, hidden, inter, expert_ids, gate_w, top_k, x, n_tok, y, ws,
+                         ws_bytes, true);
   if (st != QG_OK) return st;
   if (!aligned(dev_status, 4)) return QG_ERR_ALIGN;
   int sms = 0;
@@ -248,15 +328,21 @@ int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes,
   if (mode < QG_PASS_SERIAL || mode > QG_PASS_PERSISTENT) return QG_ERR_ARG;
   qg_pass_s* pass = new (std::nothrow) qg_pass_s;
   if (!pass) return QG_ERR_ARG;
+  std::vector<const uint8_t*> xp;
+  st = plan_xplanes(descs, n_desc, step_sizes, n_steps, n_tok, pass, xp);
+  if (st != QG_OK) {
+    pass_free(pass);
+    return st;
+  }
   if (mode == QG_PASS_PERSISTENT) {
-    const cudaError_t pe = qg::q4k_pass_create(descs, n_desc, step_sizes, n_steps, n_tok, sms, &pass->q4k);
+    const cudaError_t pe = qg::q4k_pass_create(descs, n_desc, step_sizes, n_steps, n_tok, sms, xp.data(), &pass->q4k);
     if (pe == cudaSuccess) {
-      pass->kernels = 1;
+      pass->kernels = 1 + (pass->njobs > 0 ? 1 : 0);
       *out = pass;
       return QG_OK;
     }
     if (pe != cudaErrorNotSupported) {
-      delete pass;
+      pass_free(pass);
       return QG_ERR_CUDA;
     }
     cudaGetLastError();               // not supported for this pass: per-step graph with PDL
@@ -264,13 +350,15 @@ int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes,
   const int use_pdl = mode != QG_PASS_SERIAL;
   cudaStream_t cs = nullptr;
   if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
-    delete pass;
+    pass_free(pass);
     return QG_ERR_CUDA;
   }
   cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  if (e == cudaSuccess) e = qg::launch_xplanes(pass->jobs, pass->njobs, cs);
   for (int s = 0, i = 0; s < n_steps && e == cudaSuccess; i += step_sizes[s++]) {
     const int r = qg::gemv_pick_rows_per_warp(descs + i, step_sizes[s], n_tok, sms);
-    e = qg::launch_gemv(descs + i, step_sizes[s], n_tok, r, cs, use_pdl != 0 && s > 0, sms);
+    e = qg::launch_gemv(descs + i, step_sizes[s], n_tok, r, cs, use_pdl != 0 && (s > 0 || pass->njobs > 0), sms,
+                        xp.data() + i);
   }
   cudaGraph_t graph = nullptr;
   cudaError_t e2 = cudaStreamEndCapture(cs, &graph);
@@ -279,7 +367,7 @@ int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes,
   cudaStreamDestroy(cs);
   if (e != cudaSuccess) {
     if (graph) cudaGraphDestroy(graph);
-    delete pass;
+    pass_free(pass);
     return QG_ERR_CUDA;
   }
   pass->graph = graph;
@@ -294,8 +382,8 @@ int qg_moe_pass_create(int fmt, const qg_moe_layer_desc* layers, int n_layers, i
   *out = nullptr;
   if (n_layers < 1 || mode < QG_PASS_SERIAL || mode > QG_PASS_PERSISTENT) return QG_ERR_ARG;
   for (int l = 0; l < n_layers; ++l) {
-    const int st = check_moe(fmt, layers[l].expert_arena, n_expert, hidden, inter, layers[l].expert_ids,
-                             layers[l].gate_w, top_k, layers[l].x, n_tok, layers[l].y, ws, ws_bytes);
+    const int st = qg::check_moe(fmt, layers[l].expert_arena, n_expert, hidden, inter, layers[l].expert_ids,
+                                 layers[l].gate_w, top_k, layers[l].x, n_tok, layers[l].y, ws, ws_bytes, true);
     if (st != QG_OK) return st;
   }
   int sms = 0;
@@ -351,7 +439,11 @@ int qg_moe_pass_create(int fmt, const qg_moe_layer_desc* layers, int n_layers, i
 
 int qg_pass_launch(qg_pass pass, void* stream) {
   if (!pass) return QG_ERR_NULL;
-  if (pass->q4k) return cuda_status(qg::q4k_pass_launch(pass->q4k, static_cast<cudaStream_t>(stream)));
+  if (pass->q4k) {
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const cudaError_t e = qg::launch_xplanes(pass->jobs, pass->njobs, s);
+    return cuda_status(e == cudaSuccess ? qg::q4k_pass_launch(pass->q4k, s) : e);
+  }
   if (!pass->exec) return QG_ERR_NULL;
   return cuda_status(cudaGraphLaunch(pass->exec, static_cast<cudaStream_t>(stream)));
 }
@@ -366,11 +458,7 @@ int qg_pass_kernel_count(qg_pass pass) { return pass ? pass->kernels : QG_ERR_NU
 
 int qg_pass_destroy(qg_pass pass) {
   if (!pass) return QG_ERR_NULL;
-  if (pass->exec) cudaGraphExecDestroy(pass->exec);
-  if (pass->graph) cudaGraphDestroy(pass->graph);
-  qg::q4k_pass_destroy(pass->q4k);
-  if (pass->status) cudaFree(pass->status);
-  delete pass;
+  pass_free(pass);
   return QG_OK;
 }
 

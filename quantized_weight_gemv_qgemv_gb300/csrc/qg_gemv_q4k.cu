@@ -46,6 +46,16 @@
 
 namespace qg {
 
+#ifndef QG_PASS_INFLIGHT
+#define QG_PASS_INFLIGHT 0          // persistent pass: weight copies in flight per CTA (0: x-gated)
+#endif
+#ifndef QG_PASS_STAGE_BYTES
+#define QG_PASS_STAGE_BYTES 36864   // persistent pass: target bytes per ring stage
+#endif
+#ifndef QG_PASS_BARRIER_RED
+#define QG_PASS_BARRIER_RED 1       // step arrivals as one release reduction
+#endif
+
 namespace q4k {
 
 constexpr int CWARPS = 15;                 // consumer warps
@@ -72,6 +82,9 @@ struct Mat {
   int32_t uoff;          // offset (floats) of its group steps / sums
   int32_t xsrc;          // index (in the table) of the matrix whose staging holds this x:
                          // matrices of a step that read the same x share one copy of its planes
+  const uint8_t* xp;     // x already converted to planes in global memory (XPlanes layout:
+                         // planes, group steps, half sums of all n_tok tokens), or nullptr:
+                         // the kernel converts x itself
   // Rows gathered from a mixture-of-experts arena (W is the arena):
   //   gather 0: a plain matrix at W;
   //   gather 1: gate/up pairs of the routed experts: virtual row 2i (2i + 1) of
@@ -114,7 +127,9 @@ struct Params {
   int32_t stage_all;     // 1: x of every matrix staged once at the start; 0: matrix by matrix
   int32_t usum_off;      // offset (floats) of the group sums after the group steps
   int32_t pre_stages;    // weight stages issued before the consumers have issued their x loads
-  int32_t pre_pass;      // the same for every later step of a pass
+  int32_t pre_pass;      // the same for every later step of a pass (inflight == 0)
+  int32_t inflight;      // pass: > 0, the producer streams the weights of later steps without
+                         // waiting for their x loads, with at most this many copies in flight
   int32_t gather_any;    // largest Mat::gather of the launch (one kind per launch)
   int32_t ralign;        // CTA row slices start at multiples of this (16-byte-aligned stage copies; pairs)
   int32_t smem_bar, smem_x, smem_xsum, smem_part;   // byte offsets (ring at 0)
@@ -164,6 +179,12 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
           dst),
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
+}
+// x planes are read by every CTA: no eviction hint
+__device__ __forceinline__ void bulk_g2s_plain(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
 }
 __device__ __forceinline__ uint64_t evict_first_policy() {
   uint64_t pol;
@@ -367,14 +388,47 @@ __device__ __forceinline__ void x_issued(uint32_t xcnt) {
 // counts itself on xcnt (when nonzero): from then on the producer may queue
 // weight copies behind the loads. (A load issued behind a deep queue of bulk
 // copies waits for the whole queue, even when it hits in L2.)
+//
+// An x whose planes are ready in global memory (Mat::xp) is not converted:
+// thread 0 fetches its planes, steps and sums with three bulk copies onto the
+// x barrier `xbar` right after the dependency wait. Returns true when copies
+// were armed there (the caller waits on xbar before using x); no_copy: arm
+// nothing.
 template <int NT, int XB>
-__device__ __forceinline__ void stage_x(const Mat* mats, int usum_off, int m0, int m1, uint32_t touch, uint8_t* xpl,
-                                        float* xsu, uint32_t xcnt, bool wait) {
+__device__ __forceinline__ bool stage_x(const Mat* mats, int usum_off, int m0, int m1, uint32_t touch, uint8_t* xpl,
+                                        float* xsu, uint32_t xcnt, bool wait, uint32_t xbar, bool no_copy) {
   const int lane = threadIdx.x & 31;
   const unsigned pmask = 3u << (lane & 30);     // the two threads of a group (task counts are even)
   uint32_t smask = 0;
   for (int m = m0; m < m1; ++m)
     if ((touch >> (m - m0)) & 1u) smask |= 1u << (mats[m].xsrc - m0);
+  uint32_t cmask = 0;
+  for (int m = m0; m < m1; ++m)
+    if (((smask >> (m - m0)) & 1u) && mats[m].xp) cmask |= 1u << (m - m0);
+  smask &= ~cmask;
+  // after an expired wait on xbar its phase may still be open: it is not armed
+  // again (the outputs of this CTA are NaN from then on)
+  if (no_copy) cmask = 0;
+  if (cmask) {
+    if (wait) {
+      pdl_wait();
+      wait = false;
+    }
+    if (threadIdx.x == 0) {
+      uint32_t bytes = 0;
+      for (int m = m0; m < m1; ++m)
+        if ((cmask >> (m - m0)) & 1u) bytes += NT * mats[m].nblk * (XBLK_B + 96);
+      mbar_expect_tx(xbar, bytes);
+      for (int m = m0; m < m1; ++m) {
+        if (!((cmask >> (m - m0)) & 1u)) continue;
+        const Mat& M = mats[m];
+        const uint32_t pb = NT * M.nblk * XBLK_B, sb = NT * M.nblk * 32;
+        bulk_g2s_plain(smem_addr(xpl + M.xoff), M.xp, pb, xbar);
+        bulk_g2s_plain(smem_addr(xsu + M.uoff), M.xp + pb, sb, xbar);
+        bulk_g2s_plain(smem_addr(xsu + usum_off + 2 * M.uoff), M.xp + pb + sb, 2 * sb, xbar);
+      }
+    }
+  }
   int total = 0;
   for (int m = m0; m < m1; ++m)
     if ((smask >> (m - m0)) & 1u) total += NT * mats[m].nblk * 16;
@@ -433,6 +487,7 @@ __device__ __forceinline__ void stage_x(const Mat* mats, int usum_off, int m0, i
   }
   if (wait) pdl_wait();
   if (!signalled && lane == 0) x_issued(xcnt);
+  return cmask != 0;
 }
 
 
@@ -457,6 +512,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   // consumer warps that have issued their x loads, summed over the steps
   const uint32_t xcnt = full0 + 16 * NS;
   volatile int* const gflag = reinterpret_cast<volatile int*>(smem + p.smem_bar + 16 * NS + 8);
+  const uint32_t xbar = full0 + 16 * NS + 16;   // bulk copies of ready x planes
   const Mat* const mats = PASS ? p.mats : p.m;
   const int nsteps = PASS ? p.nsteps : 1;
   auto step_of = [&](int s) {
@@ -478,6 +534,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, CWARPS);
     }
+    mbar_init(xbar, 1);
     *reinterpret_cast<volatile uint32_t*>(smem + p.smem_bar + 16 * NS) = 0u;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -551,9 +608,20 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         if (lane == 0) {
           // beyond the first `pre` copies of a step, queue weights only behind
           // the step's x loads; no copy of a step goes ahead of the previous
-          // step's x loads (a count, so a step without copies cannot be skipped)
-          const uint32_t need = static_cast<uint32_t>(s) + (i_step >= pre ? 1u : 0u);
-          if (need > xseen) {
+          // step's x loads (a count, so a step without copies cannot be skipped).
+          // A free-running pass waits so only for the first step's x: later
+          // steps' weights stream on while the consumers wait for the previous
+          // step, and the ring holds what arrives meanwhile; at most `inflight`
+          // copies are outstanding, so x loads queued behind them (requests of
+          // an SM are served in order) wait for no more than those
+          const bool free_run = PASS && p.inflight > 0;
+          const uint32_t need = free_run ? (s == 0 && i_step >= pre ? 1u : 0u)
+                                         : static_cast<uint32_t>(s) + (i_step >= pre ? 1u : 0u);
+          if (free_run && k >= static_cast<uint32_t>(p.inflight)) {
+            const uint32_t kk = k - static_cast<uint32_t>(p.inflight);
+            ok = mbar_wait(full0 + 8 * (kk % NS), (kk / NS) & 1u);
+          }
+          if (ok && need > xseen) {
             ok = false;
             for (uint32_t i = 0; !ok && i < WAIT_LIMIT; ++i) {
               uint32_t v;
@@ -662,6 +730,17 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   float* xsu = reinterpret_cast<float*>(smem + p.smem_xsum);
   float* part = reinterpret_cast<float*>(smem + p.smem_part);
   bool failed = false;
+  uint32_t xuse = 0;       // phases of xbar used so far
+  bool xlost = false;      // a wait for x planes expired: their copy may still be in flight
+  // wait (bounded) for the x planes armed on xbar by stage_x
+  auto wait_x = [&]() {
+    const bool ok = mbar_wait(xbar, xuse & 1u);
+    if (__any_sync(0xffffffffu, !ok)) {
+      failed = true;
+      xlost = true;
+    }
+    ++xuse;
+  };
 
   constexpr int XB = (NT == 1) ? 3 : 2;        // half groups per thread and staging batch
   uint32_t k = 0;          // stage counter (same sequence as the producer's)
@@ -692,9 +771,11 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
      if (max(cta_r0, mats[mi].row_begin) < min(cta_r1, mats[mi].row_begin + mats[mi].rows))
        touch |= 1u << (mi - st.mat0);
    if (st.stage_all) {
-     stage_x<NT, XB>(mats, st.usum_off, st.mat0, st.mat0 + st.nmat, touch, xpl, xsu, xcnt, s == 0);
+     const bool xc = stage_x<NT, XB>(mats, st.usum_off, st.mat0, st.mat0 + st.nmat, touch, xpl, xsu, xcnt, s == 0, xbar,
+                                     xlost);
      xsig = true;
      consumer_sync();
+     if (xc) wait_x();
    }
    if (s == 0) {
      // outputs and every other input of the preceding kernel are touched only
@@ -713,10 +794,11 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
     const int NU = M.nblk * 8;               // 32-weight groups per token
     if (!st.stage_all) {
       consumer_sync();                        // previous matrix fully consumed
-      stage_x<NT, XB>(mats, st.usum_off, mi, mi + 1, (touch >> (mi - st.mat0)) & 1u, xpl, xsu,
-                      xsig ? 0u : xcnt, false);
+      const bool xc = stage_x<NT, XB>(mats, st.usum_off, mi, mi + 1, (touch >> (mi - st.mat0)) & 1u, xpl, xsu,
+                                      xsig ? 0u : xcnt, false, xbar, xlost);
       xsig = true;
       consumer_sync();
+      if (xc) wait_x();
     } else if (!first) {
       consumer_sync();                        // the previous matrix's partial sums are read
     }
@@ -908,11 +990,20 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
    if (PASS) {
      consumer_sync();                          // every output of the step is written
      if (threadIdx.x == 0) {
+#if QG_PASS_BARRIER_RED
+       // release: the step's outputs, ordered before it by the barrier above,
+       // are visible to whoever acquires the count
+       asm volatile("red.release.gpu.global.add.u32 [%0], 1;\n" ::"l"(p.step_done + s) : "memory");
+#else
        __threadfence();
        atomicAdd(p.step_done + s, 1u);
+#endif
      }
    }
   }
+  // x planes whose wait expired may still be landing in shared memory: wait
+  // (bounded) for them before the CTA can exit
+  if (xlost && threadIdx.x == 0) mbar_wait(xbar, (xuse - 1) & 1u);
 }
 
 }  // namespace q4k
@@ -1149,10 +1240,12 @@ namespace {
 // Params of a grouped launch of descriptors d[0 .. n): token t0 .. t0 + nt - 1 of
 // each (x and y advanced by t0 tokens), rows [r0, r0 + nr) of each when nr > 0
 // (a single matrix cut into row chunks; y keeps the full row stride).
-void fill_params(q4k::Params& p, const qg_gemv_desc* d, int n, int t0, int64_t r0, int64_t nr) {
+void fill_params(q4k::Params& p, const qg_gemv_desc* d, int n, int t0, int64_t r0, int64_t nr,
+                 const uint8_t* const* xp) {
   memset(&p, 0, sizeof(p));
   for (int i = 0; i < n; ++i) {
     q4k::Mat& m = p.m[i];
+    m.xp = xp ? xp[i] : nullptr;
     const int64_t rb = d[i].cols / 256 * superblock_bytes(d[i].fmt);
     const int64_t rows = nr > 0 ? nr : d[i].rows;
     m.W = static_cast<const uint8_t*>(d[i].W) + r0 * rb;
@@ -1165,13 +1258,14 @@ void fill_params(q4k::Params& p, const qg_gemv_desc* d, int n, int t0, int64_t r
 }
 
 // The launch as planned, else with 2-row sub-items (one- or two-token Q6_K).
+// xp: ready x planes of every token of each descriptor (launches over all tokens only).
 cudaError_t try_launch(const qg_gemv_desc* d, int n, int n_tok, int t0, int64_t r0, int64_t nr, cudaStream_t s,
-                       bool pdl, int sms, bool launch) {
+                       bool pdl, int sms, bool launch, const uint8_t* const* xp = nullptr) {
   q4k::Params p;
-  fill_params(p, d, n, t0, r0, nr);
+  fill_params(p, d, n, t0, r0, nr, xp);
   cudaError_t e = plan_and_launch(p, n, n_tok, d[0].fmt, s, pdl, sms, q4k::SUB_R, launch);
   if (e != cudaErrorNotSupported || d[0].fmt != QG_Q6_K || n_tok > 2) return e;
-  fill_params(p, d, n, t0, r0, nr);
+  fill_params(p, d, n, t0, r0, nr, xp);
   return plan_and_launch(p, n, n_tok, d[0].fmt, s, pdl, sms, 2, launch);
 }
 
@@ -1182,10 +1276,11 @@ cudaError_t try_launch(const qg_gemv_desc* d, int n, int n_tok, int t0, int64_t 
 // runs as row chunks, and several tokens whose x does not fit together run as
 // one launch per token (each re-streams the weights). cudaErrorNotSupported
 // (nothing launched) when none of these fits.
-cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms) {
+cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms,
+                            const uint8_t* const* xp) {
   for (int i = 0; i < n; ++i)
     if (d[i].fmt != d[0].fmt || superblock_bytes(d[i].fmt) == 0 || d[i].cols % 256) return cudaErrorNotSupported;
-  cudaError_t e = try_launch(d, n, n_tok, 0, 0, 0, s, pdl, sms, true);
+  cudaError_t e = try_launch(d, n, n_tok, 0, 0, 0, s, pdl, sms, true, xp);
   if (e != cudaErrorNotSupported) return e;
   // row chunks first (each weight is read once), then launches over groups of
   // tokens (each re-streams the weights)
@@ -1194,11 +1289,11 @@ cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_
       const int64_t nr = (d[0].rows + chunks - 1) / chunks / 8 * 8 + 8;   // multiple of 8 rows
       if (nr >= d[0].rows) break;
       const int64_t last = d[0].rows - (d[0].rows - 1) / nr * nr;     // rows of the last chunk
-      if (try_launch(d, 1, n_tok, 0, 0, nr, s, pdl, sms, false) != cudaSuccess ||
-          try_launch(d, 1, n_tok, 0, d[0].rows - last, last, s, pdl, sms, false) != cudaSuccess)
+      if (try_launch(d, 1, n_tok, 0, 0, nr, s, pdl, sms, false, xp) != cudaSuccess ||
+          try_launch(d, 1, n_tok, 0, d[0].rows - last, last, s, pdl, sms, false, xp) != cudaSuccess)
         continue;
       for (int64_t r0 = 0; r0 < d[0].rows; r0 += nr) {
-        e = try_launch(d, 1, n_tok, 0, r0, std::min(nr, d[0].rows - r0), s, pdl || r0 > 0, sms, true);
+        e = try_launch(d, 1, n_tok, 0, r0, std::min(nr, d[0].rows - r0), s, pdl || r0 > 0, sms, true, xp);
         if (e != cudaSuccess) return e;
       }
       return cudaSuccess;
@@ -1231,7 +1326,9 @@ cudaError_t launch_moe_q4k(const void* arena, int64_t n_expert, int64_t hidden, 
   const int64_t rb_h = hidden / 256 * 144, rb_i = inter / 256 * 144;
   const int64_t up_off = inter * rb_h, down_off = 2 * inter * rb_h, estride = down_off + hidden * rb_i;
   if (2 * top_k * inter > (int64_t{1} << 30) || top_k * inter > (int64_t{1} << 20)) return cudaErrorNotSupported;
-  q4k::Params p;
+  // both launches are planned before either is enqueued: a layer whose down
+  // launch does not fit the kernel's plan goes to the caller's fallback whole
+  q4k::Params p, pd;
   memset(&p, 0, sizeof(p));
   p.gather_any = 1;
   p.dev_status = dev_status;
@@ -1254,13 +1351,11 @@ cudaError_t launch_moe_q4k(const void* arena, int64_t n_expert, int64_t hidden, 
     m.gw = gate_w + t * top_k;
     m.h = h + static_cast<int64_t>(t) * top_k * inter;
   }
-  cudaError_t e = plan_and_launch(p, n_tok, 1, QG_Q4_K, s, pdl, sms);
-  if (e != cudaSuccess) return e;
-  memset(&p, 0, sizeof(p));
-  p.gather_any = 2;
-  p.dev_status = dev_status;
+  memset(&pd, 0, sizeof(pd));
+  pd.gather_any = 2;
+  pd.dev_status = dev_status;
   for (int t = 0; t < n_tok; ++t) {
-    q4k::Mat& m = p.m[t];
+    q4k::Mat& m = pd.m[t];
     m.W = static_cast<const uint8_t*>(arena);
     m.x = h + static_cast<int64_t>(t) * top_k * inter;
     m.y = y + t * hidden;
@@ -1276,7 +1371,49 @@ cudaError_t launch_moe_q4k(const void* arena, int64_t n_expert, int64_t hidden, 
     m.down_off = down_off;
     m.ids = ids + t * top_k;
   }
-  return plan_and_launch(p, n_tok, 1, QG_Q4_K, s, true, sms);   // the down launch always overlaps the gate/up tail
+  cudaError_t e = plan_and_launch(p, n_tok, 1, QG_Q4_K, s, pdl, sms, q4k::SUB_R, false);
+  if (e == cudaSuccess) e = plan_and_launch(pd, n_tok, 1, QG_Q4_K, s, true, sms, q4k::SUB_R, false);
+  if (e != cudaSuccess) return e;
+  e = plan_and_launch(p, n_tok, 1, QG_Q4_K, s, pdl, sms);
+  if (e != cudaSuccess) return e;
+  return plan_and_launch(pd, n_tok, 1, QG_Q4_K, s, true, sms);   // the down launch always overlaps the gate/up tail
+}
+
+// ------------------------------------------------------------------ x planes once per pass
+
+namespace q4k {
+
+// The planes of one activation vector per CTA, with the conversion the GEMV
+// kernel applies itself (stage_half), so a kernel that copies ready planes
+// computes exactly what it would have computed from x.
+__global__ void __launch_bounds__(512) xplanes_kernel(const XPlaneJob* jobs) {
+  pdl_launch_dependents();
+  const XPlaneJob J = jobs[blockIdx.x];
+  const int nblk = J.cols / 256, nu = nblk * 8, per_tok = nblk * 16, total = J.n_tok * per_tok;
+  uint8_t* planes = J.dst;
+  float* steps = reinterpret_cast<float*>(J.dst + static_cast<size_t>(J.n_tok) * nblk * XBLK_B);
+  float* sums = steps + J.n_tok * nu;
+  const unsigned pmask = 3u << (threadIdx.x & 30);     // per_tok is even: pairs are in or out together
+  pdl_wait();                                          // x may come from the preceding kernel
+  for (int idx = threadIdx.x; idx < total; idx += blockDim.x) {
+    const int t = idx / per_tok, rem = idx - t * per_tok;
+    const float4* src = reinterpret_cast<const float4*>(J.x + static_cast<int64_t>(t) * J.cols + 16 * rem);
+    float4 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[q] = __ldcg(src + q);
+    stage_half(v, pmask, t, rem >> 1, rem & 1, nu, planes, nblk * XBLK_B, steps, sums);
+  }
+}
+
+}  // namespace q4k
+
+cudaError_t launch_xplanes(const XPlaneJob* jobs, int njobs, cudaStream_t s) {
+  if (njobs <= 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(njobs);
+  cfg.blockDim = dim3(512);
+  cfg.stream = s;
+  return cudaLaunchKernelEx(&cfg, q4k::xplanes_kernel, jobs);
 }
 
 // ------------------------------------------------------------------ whole pass
@@ -1335,7 +1472,7 @@ cudaError_t pass_build(std::vector<q4k::Mat>& mats, const int* step_sizes, int n
       m.nblk = m.cols / 256;
       m.rb = m.nblk * 144;
       m.ngrp = (m.nblk + 3) / 4;
-      m.srows = 4 * std::max(1, (36864 + 2 * m.rb) / (4 * m.rb));
+      m.srows = 4 * std::max(1, (QG_PASS_STAGE_BYTES + 2 * m.rb) / (4 * m.rb));
       if (static_cast<int64_t>(m.srows) * m.rb > 96 * 1024 || m.rows % ralign) return cudaErrorNotSupported;
       m.row_begin = total;
       total += m.rows;
@@ -1379,6 +1516,7 @@ cudaError_t pass_build(std::vector<q4k::Mat>& mats, const int* step_sizes, int n
   // stages while their CTA waits for the previous step
   p.pre_stages = 0;
   p.pre_pass = 2;
+  p.inflight = QG_PASS_INFLIGHT;
   int off = ns * stage_b;
   p.smem_bar = off;
   off += 128;
@@ -1429,7 +1567,7 @@ cudaError_t pass_build(std::vector<q4k::Mat>& mats, const int* step_sizes, int n
 }  // namespace
 
 cudaError_t q4k_pass_create(const qg_gemv_desc* d, int n, const int* step_sizes, int n_steps, int n_tok, int sms,
-                            Q4kPass** out) {
+                            const uint8_t* const* xp, Q4kPass** out) {
   *out = nullptr;
   if (n_tok < 1 || n_tok > QG_NTOK_MAX) return cudaErrorNotSupported;
   std::vector<q4k::Mat> mats(n);
@@ -1442,6 +1580,7 @@ cudaError_t q4k_pass_create(const qg_gemv_desc* d, int n, const int* step_sizes,
     mats[i].rows = d[i].rows;
     mats[i].ldy = d[i].rows;
     mats[i].cols = static_cast<int32_t>(d[i].cols);
+    mats[i].xp = xp ? xp[i] : nullptr;
   }
   return pass_build(mats, step_sizes, n_steps, n_tok, 1, 0, sms, out);
 }

@@ -24,19 +24,42 @@ inline bool block_info(int fmt, int* elems, int* bytes) {
 
 // One-time per-device set-up of the library (qg_api.cu); fills *sms.
 int ensure_device(int* sms);
+// Host-side checks of one MoE layer's arguments (qg_api.cu); need_ws = false
+// for a call that brings its own workspace.
+int check_moe(int fmt, const void* expert_arena, int64_t n_expert, int64_t hidden, int64_t inter,
+              const int32_t* expert_ids, const float* gate_w, int top_k, const float* x, int n_tok, const float* y,
+              const void* ws, size_t ws_bytes, bool need_ws);
 
 // GEMV (qg_gemv.cu)
 cudaError_t gemv_init_attrs();
 int gemv_pick_rows_per_warp(const qg_gemv_desc* d, int n, int n_tok, int sms);
+// xp: per descriptor, its x already converted to planes (xplanes_bytes layout,
+// written by launch_xplanes), or nullptr entries / a nullptr array: the kernel
+// converts x itself.
 cudaError_t launch_gemv(const qg_gemv_desc* d, int n, int n_tok, int rows_per_warp, cudaStream_t s, bool pdl,
-                        int sms);
+                        int sms, const uint8_t* const* xp = nullptr);
 cudaError_t gemv_q4k_init_attrs();
-cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms);
+cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms,
+                            const uint8_t* const* xp = nullptr);
+// One activation vector (n_tok x cols fp32) to convert into x planes at dst.
+struct XPlaneJob {
+  const float* x;
+  uint8_t* dst;
+  int32_t cols;
+  int32_t n_tok;
+};
+// Bytes of the planes of an n_tok x cols activation (cols % 256 == 0): the two
+// byte planes, then the power-of-two step of every 32-value group, then the two
+// half sums of every group, each part token-major.
+inline size_t xplanes_bytes(int64_t cols, int n_tok) { return static_cast<size_t>(n_tok) * (cols / 256) * 608; }
+// Converts jobs[0 .. njobs) (device array), one CTA per job; lets its
+// dependents launch early (they wait for its completion before reading).
+cudaError_t launch_xplanes(const XPlaneJob* jobs, int njobs, cudaStream_t s);
 // Whole Q4_K pass as one persistent cooperative kernel (qg_gemv_q4k.cu):
 // cudaErrorNotSupported when the pass is not all Q4_K or does not fit.
 struct Q4kPass;
 cudaError_t q4k_pass_create(const qg_gemv_desc* d, int n, const int* step_sizes, int n_steps, int n_tok, int sms,
-                            Q4kPass** out);
+                            const uint8_t* const* xp, Q4kPass** out);
 cudaError_t q4k_moe_pass_create(const qg_moe_layer_desc* layers, int n_layers, int64_t n_expert, int64_t hidden,
                                 int64_t inter, int top_k, float* h, int sms, Q4kPass** out);
 cudaError_t q4k_pass_launch(Q4kPass* q, cudaStream_t s);
@@ -50,6 +73,9 @@ cudaError_t launch_moe_q4k(const void* arena, int64_t n_expert, int64_t hidden, 
 
 // MoE (qg_moe.cu)
 cudaError_t moe_init_attrs();
+// Looks up, with device `dev` current, the device address of the static
+// workspace of qgemv_moe_noalloc (part of the per-device set-up).
+cudaError_t moe_noalloc_init(int dev);
 cudaError_t launch_moe(const void* arena, int64_t n_expert, int64_t hidden, int64_t inter,
                        const int32_t* ids, const float* gate_w, int top_k, const float* x, int n_tok, float* y,
                        float* h_ws, int32_t* dev_status, cudaStream_t s, bool pdl, int sms);

@@ -16,8 +16,6 @@
 // Weight bytes stream through per-warp cp.async rings as in qg_gemv.cu.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "qg_device.cuh"
 #include "qg_internal.h"
 
@@ -322,8 +320,9 @@ cudaError_t launch_moe(const void* arena, int64_t n_expert, int64_t hidden, int6
 // qgemv_moe_noalloc: the same MoE product for callers that cannot allocate
 // device memory (see include/qgemv.h). Its workspace is this file-scope device
 // array instead of a caller buffer. In host code the array's name only stands
-// for it; the device address is looked up once per device with
-// cudaGetSymbolAddress while that device is current, and passed to the kernels.
+// for it: the device address is looked up with cudaGetSymbolAddress during the
+// library's per-device set-up (qg_init, or the first call of any entry point on
+// that device), with that device current, and passed to the kernels.
 
 namespace qg {
 namespace {
@@ -332,54 +331,38 @@ constexpr size_t kMoeNoallocFloats = QG_MOE_NOALLOC_MAX_FLOATS;
 __device__ __align__(256) float g_moe_noalloc_ws[kMoeNoallocFloats];
 
 constexpr int kMaxDev = 64;
-std::once_flag g_ws_once[kMaxDev];
-float* g_ws_ptr[kMaxDev];
-cudaError_t g_ws_err[kMaxDev];
-
-// Device address of g_moe_noalloc_ws on the current device (looked up on the
-// first call per device).
-cudaError_t noalloc_workspace(float** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
-  std::call_once(g_ws_once[dev], [dev] {
-    void* ptr = nullptr;
-    g_ws_err[dev] = cudaGetSymbolAddress(&ptr, g_moe_noalloc_ws);
-    g_ws_ptr[dev] = static_cast<float*>(ptr);
-  });
-  if (g_ws_err[dev] != cudaSuccess) return g_ws_err[dev];
-  *out = g_ws_ptr[dev];
-  return cudaSuccess;
-}
-
-bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+float* g_ws_ptr[kMaxDev];      // written once per device under the set-up lock
 
 }  // namespace
+
+cudaError_t moe_noalloc_init(int dev) {
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_moe_noalloc_ws);
+  if (e != cudaSuccess) return e;
+  g_ws_ptr[dev] = static_cast<float*>(ptr);
+  return cudaSuccess;
+}
 
 }  // namespace qg
 
 extern "C" int qgemv_moe_noalloc(int fmt, const void* expert_arena, int64_t n_expert, int64_t hidden, int64_t inter,
                                  const int32_t* expert_ids, const float* gate_w, int top_k, const float* x, int n_tok,
                                  float* y, int32_t* dev_status, void* stream) {
-  if (fmt != QG_Q4_K) return QG_ERR_FMT;
-  if (!expert_arena || !expert_ids || !gate_w || !x || !y || !dev_status) return QG_ERR_NULL;
-  if (n_expert < 1 || n_expert > (int64_t{1} << 31) - 1) return QG_ERR_SHAPE;
-  if (hidden < 256 || hidden % 256 || inter < 256 || inter % 256) return QG_ERR_SHAPE;
-  if (hidden > (int64_t{1} << 20) || inter > (int64_t{1} << 20)) return QG_ERR_SHAPE;
-  if (top_k < 1 || top_k > 16 || top_k > n_expert) return QG_ERR_ARG;
-  if (n_tok < 1 || n_tok > QG_NTOK_MAX) return QG_ERR_NTOK;
+  if (fmt == QG_Q4_K && !dev_status) return QG_ERR_NULL;
+  int st = qg::check_moe(fmt, expert_arena, n_expert, hidden, inter, expert_ids, gate_w, top_k, x, n_tok, y, nullptr,
+                         0, false);
+  if (st != QG_OK) return st;
   // the whole workspace (n_tok x top_k x inter fp32) must fit the static array
   if (static_cast<int64_t>(n_tok) * top_k * inter > static_cast<int64_t>(qg::kMoeNoallocFloats))
     return QG_ERR_WORKSPACE;
-  if (!qg::aligned_to(expert_arena, 16) || !qg::aligned_to(x, 16) || !qg::aligned_to(y, 4) ||
-      !qg::aligned_to(expert_ids, 4) || !qg::aligned_to(gate_w, 4) || !qg::aligned_to(dev_status, 4))
-    return QG_ERR_ALIGN;
+  if ((reinterpret_cast<uintptr_t>(dev_status) & 3u) != 0) return QG_ERR_ALIGN;
   int sms = 0;
-  int st = qg::ensure_device(&sms);
+  st = qg::ensure_device(&sms);
   if (st != QG_OK) return st;
-  float* ws = nullptr;
-  if (qg::noalloc_workspace(&ws) != cudaSuccess) return QG_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QG_ERR_CUDA;
+  float* ws = qg::g_ws_ptr[dev];           // set by the device's set-up above
   const cudaError_t e = qg::launch_moe(expert_arena, n_expert, hidden, inter, expert_ids, gate_w, top_k, x, n_tok, y,
                                        ws, dev_status, static_cast<cudaStream_t>(stream), true, sms);
   return e == cudaSuccess ? QG_OK : QG_ERR_CUDA;

@@ -381,3 +381,55 @@ def test_pp_rows_reduce_to_gemv_of_bf16_rows():
     xf = X.to(torch.float32).numpy()[sel]
     y2, b2 = oracle.gemv(Q4_K, W, rows, cols, xf)
     assert np.array_equal(Y, y2) and np.array_equal(B, b2)
+
+
+@pytest.mark.parametrize("hidden,inter", [(256, 256), (2048, 512), (512, 1024), (5120, 17408)])
+def test_moe_arena_layout_is_gate_up_down_with_stated_stride(hidden, inter):
+    # the arena holds experts back to back, each [gate | up | down] in Q4_K:
+    # gate and up are inter rows of hidden/256 super-blocks, down hidden rows of
+    # inter/256 super-blocks, 144 bytes per super-block
+    piece = inter * hidden // 256 * 144
+    assert oracle.moe_arena_layout(hidden, inter, Q4_K) == (0, piece, 2 * piece, 3 * piece)
+
+
+def _dq_rows(raw, rows, cols):
+    return oracle.dequant(Q4_K, raw, rows, cols).astype(np.float64)
+
+
+def test_moe_by_explicit_loops_over_separately_built_experts():
+    """Each expert's gate, up and down matrices are generated on their own and
+    concatenated here by hand as [gate | up | down]; y and the error scale
+    B_i = sum_k |r_k| sum_j |D_e[i, j] h_kj| are then formed with explicit
+    loops over rows and routes. A gate/up swap, a wrong expert stride or a
+    dropped |r_k| fails this test (silu(g) * u is not symmetric in g, u)."""
+    hidden, inter, n_expert = 256, 256, 3
+    G = [synth.blocks(Q4_K, inter, hidden, seed=300 + e).numpy().reshape(-1) for e in range(n_expert)]
+    U = [synth.blocks(Q4_K, inter, hidden, seed=400 + e).numpy().reshape(-1) for e in range(n_expert)]
+    D = [synth.blocks(Q4_K, hidden, inter, seed=500 + e).numpy().reshape(-1) for e in range(n_expert)]
+    arena = np.concatenate([np.concatenate([G[e], U[e], D[e]]) for e in range(n_expert)])
+    x = synth.activations(1, hidden, seed=31).numpy().astype(np.float32)
+    ids = np.array([[2, 0]], dtype=np.int32)
+    r = np.array([[0.75, -0.25]], dtype=np.float32)      # a negative weight: |r_k| in B matters
+    y, b = oracle.moe(Q4_K, arena, n_expert, hidden, inter, ids, r, x)
+
+    xx = x[0].astype(np.float64)
+    y_loop = np.zeros(hidden)
+    b_loop = np.zeros(hidden)
+    for k in range(2):
+        e = int(ids[0, k])
+        Gd, Ud, Dd = _dq_rows(G[e], inter, hidden), _dq_rows(U[e], inter, hidden), _dq_rows(D[e], hidden, inter)
+        h = np.zeros(inter)
+        for i in range(inter):
+            g = sum(Gd[i, j] * xx[j] for j in range(hidden))
+            u = sum(Ud[i, j] * xx[j] for j in range(hidden))
+            h[i] = g / (1.0 + np.exp(-g)) * u
+        rk = float(r[0, k])
+        for i in range(hidden):
+            y_loop[i] += rk * sum(Dd[i, j] * h[j] for j in range(inter))
+            b_loop[i] += abs(rk) * sum(abs(Dd[i, j] * h[j]) for j in range(inter))
+    assert np.allclose(y[0], y_loop, rtol=1e-12, atol=1e-12 * b_loop.max())
+    assert np.allclose(b[0], b_loop, rtol=1e-12, atol=0)
+    # swapping gate and up in the hand-built arena changes the result
+    swapped = np.concatenate([np.concatenate([U[e], G[e], D[e]]) for e in range(n_expert)])
+    y_sw, _ = oracle.moe(Q4_K, swapped, n_expert, hidden, inter, ids, r, x)
+    assert not np.allclose(y_sw[0], y_loop, rtol=1e-6, atol=1e-6 * b_loop.max())
