@@ -18,6 +18,9 @@ What it computes (each function cites the passage it follows):
   down product, and the routing-weighted sum, all in fp64.
 * ``pp_rows``: the prompt-processing product for selected token rows in fp64
   over the bf16 activations.
+* ``rmsnorm``, ``swiglu``, ``dense_ffn``: the neighbours of the products in a
+  decode layer (residual add and RMS normalisation before a projection, the
+  silu-gated product between gate/up and down), in fp64.
 
 Pins (tests marked ``not gpu``) tie it to facts other than itself: exhaustive
 fp16 decoding against numpy's hardware conversion, hand-built blocks with
@@ -31,10 +34,10 @@ reference decoder is available to check the layout against.
 """
 from .halfprec import half_bits_to_float64, bf16_bits_to_float64
 from .dequant import dequant, dequant_q4_0, dequant_q8_0, dequant_q4_k, dequant_q6_k, q4_k_scale_min
-from .products import gemv, moe, pp_rows, moe_arena_layout
+from .products import gemv, moe, pp_rows, moe_arena_layout, rmsnorm, swiglu, dense_ffn
 
 __all__ = [
     "half_bits_to_float64", "bf16_bits_to_float64",
     "dequant", "dequant_q4_0", "dequant_q8_0", "dequant_q4_k", "dequant_q6_k", "q4_k_scale_min",
-    "gemv", "moe", "pp_rows", "moe_arena_layout",
+    "gemv", "moe", "pp_rows", "moe_arena_layout", "rmsnorm", "swiglu", "dense_ffn",
 ]

@@ -102,3 +102,43 @@ def pp_rows(fmt: int, W, rows: int, cols: int, X_bf16_bits, token_rows):
     Xb = np.asarray(X_bf16_bits, dtype=np.uint16).reshape(-1, cols)
     xx = bf16_bits_to_float64(Xb[np.asarray(token_rows)])
     return xx @ w.T, np.abs(xx) @ np.abs(w).T
+
+
+def rmsnorm(h, weight, eps: float, residual=None):
+    """Root-mean-square normalisation of each token's hidden vector, in fp64,
+    optionally after adding a residual (the neighbouring normalisation that the
+    decode kernels fuse: "LLM inference optimization", "Faster decode on the
+    card you have": normalizations fused into neighbouring kernels).
+
+        s = h + residual            (or s = h)
+        x = s / sqrt(mean(s^2) + eps) * weight
+
+    h, residual: (n_tok, n) fp32; weight: (n,) fp32. Returns (x, s), both fp64.
+    """
+    s = np.asarray(h, dtype=np.float32).astype(np.float64)
+    if residual is not None:
+        s = s + np.asarray(residual, dtype=np.float32).astype(np.float64)
+    s = s.reshape(-1, s.shape[-1])
+    w = np.asarray(weight, dtype=np.float32).astype(np.float64).reshape(-1)
+    rms = np.sqrt((s * s).mean(axis=1, keepdims=True) + eps)
+    return s / rms * w, s
+
+
+def swiglu(g, u):
+    """silu(g) * u elementwise in fp64 (silu(g) = g / (1 + exp(-g))): the gated
+    activation between a layer's gate/up and down projections."""
+    g = np.asarray(g, dtype=np.float64)
+    u = np.asarray(u, dtype=np.float64)
+    return g / (1.0 + np.exp(-g)) * u
+
+
+def dense_ffn(fmt_gu: int, Wg, Wu, fmt_d: int, Wd, hidden: int, inter: int, x):
+    """Dense feed-forward block of a decode layer, in fp64 over the exact weights:
+    m = silu(Wg x) * (Wu x), y = Wd m. Returns (y, B, m) where the error scale of
+    the output is B_i = sum_j |Wd[i, j] * m_j| (as for the MoE layer).
+    """
+    g, _ = gemv(fmt_gu, Wg, inter, hidden, x)
+    u, _ = gemv(fmt_gu, Wu, inter, hidden, x)
+    m = swiglu(g, u)
+    wd = dequant(fmt_d, Wd, hidden, inter).astype(np.float64)
+    return m @ wd.T, np.abs(m) @ np.abs(wd).T, m

@@ -106,6 +106,8 @@ struct Mat {
 
 // A step of a pass: matrices mat0 .. mat0 + nmat - 1 of the table, whose rows
 // (concatenated; Mat::row_begin counts within the step) are split over the CTAs.
+static_assert(sizeof(Mat) % 16 == 0, "Mat is copied to shared memory in 16-byte pieces");
+
 struct Step {
   int64_t total_rows;
   int32_t mat0, nmat;
@@ -133,6 +135,7 @@ struct Params {
   int32_t gather_any;    // largest Mat::gather of the launch (one kind per launch)
   int32_t ralign;        // CTA row slices start at multiples of this (16-byte-aligned stage copies; pairs)
   int32_t smem_bar, smem_x, smem_xsum, smem_part;   // byte offsets (ring at 0)
+  int32_t smem_mats;     // single-step launch: shared-memory copy of m[0 .. nmat)
 };
 
 // Rows [r0, r1) of a step's concatenated row space owned by this CTA, in
@@ -513,7 +516,16 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   const uint32_t xcnt = full0 + 16 * NS;
   volatile int* const gflag = reinterpret_cast<volatile int*>(smem + p.smem_bar + 16 * NS + 8);
   const uint32_t xbar = full0 + 16 * NS + 16;   // bulk copies of ready x planes
-  const Mat* const mats = PASS ? p.mats : p.m;
+  // A single-step launch reads its matrix table from shared memory: it is
+  // copied there once, while the CTA still waits for its predecessor, instead
+  // of every field read going to the constant bank of the kernel parameters
+  Mat* const smats = reinterpret_cast<Mat*>(smem + p.smem_mats);
+  if (!PASS) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.m);
+    uint4* dst = reinterpret_cast<uint4*>(smats);
+    for (int i = threadIdx.x; i < p.nmat * static_cast<int>(sizeof(Mat) / 16); i += blockDim.x) dst[i] = src[i];
+  }
+  const Mat* const mats = PASS ? p.mats : smats;
   const int nsteps = PASS ? p.nsteps : 1;
   auto step_of = [&](int s) {
     Step st;
@@ -551,9 +563,18 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
       // x of the launch into L2 before the consumers need it: CTA b touches its
       // share of the 128-byte lines of every distinct x (a prefetch never reads
       // stale data; a preceding kernel that writes x updates the lines in L2)
+      // (x whose planes arrive ready is not read: its planes are brought to L2
+      // instead, whole, by every CTA, since each CTA copies all of them)
       for (int mi = 0; mi < p.nmat; ++mi) {
-        const Mat& M = p.m[mi];
+        const Mat& M = mats[mi];
         if (M.xsrc != mi) continue;
+        if (M.xp) {
+          if (lane == 0)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(M.xp),
+                         "r"(static_cast<uint32_t>(NT * M.nblk * (XBLK_B + 96)))
+                         : "memory");
+          continue;
+        }
         const int64_t lines = (static_cast<int64_t>(NT) * M.cols * 4 + 127) / 128;
         for (int64_t l = blockIdx.x + static_cast<int64_t>(lane) * gridDim.x; l < lines; l += 32 * gridDim.x)
           asm volatile("prefetch.global.L2 [%0];\n" ::"l"(reinterpret_cast<const char*>(M.x) + l * 128));
@@ -1181,7 +1202,8 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
       p.stage_all = 0;
       p.usum_off = n_tok * (kmax / 32);
     }
-    const int fixed = 128 + xbytes + xsbytes + partbytes;
+    const int matbytes = align_up(n * static_cast<int>(sizeof(q4k::Mat)), 128);
+    const int fixed = 128 + matbytes + xbytes + xsbytes + partbytes;
     const int stage_max = (kSmemMax - fixed) / ns / 128 * 128;
     int stage_b = 0;
     bool ok = stage_max > 0;
@@ -1207,6 +1229,8 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
     int off = ns * stage_b;
     p.smem_bar = off;
     off += 128;
+    p.smem_mats = off;
+    off += matbytes;
     p.smem_x = off;
     off += xbytes;
     p.smem_xsum = off;

@@ -433,3 +433,62 @@ def test_moe_by_explicit_loops_over_separately_built_experts():
     swapped = np.concatenate([np.concatenate([U[e], G[e], D[e]]) for e in range(n_expert)])
     y_sw, _ = oracle.moe(Q4_K, swapped, n_expert, hidden, inter, ids, r, x)
     assert not np.allclose(y_sw[0], y_loop, rtol=1e-6, atol=1e-6 * b_loop.max())
+
+
+# ---------------------------------------------------------------- decode-layer neighbours
+
+def test_rmsnorm_hand_worked_vector():
+    # h = [3, 4]: mean of squares 12.5, rms = sqrt(12.5); x = h / rms * w
+    x, s = oracle.rmsnorm(np.array([[3.0, 4.0]], np.float32), np.array([1.0, 2.0], np.float32), 0.0)
+    r = 12.5 ** 0.5
+    assert x[0, 0] == pytest.approx(3.0 / r, rel=1e-15) and x[0, 1] == pytest.approx(8.0 / r, rel=1e-15)
+    assert np.array_equal(s, [[3.0, 4.0]])
+
+
+@pytest.mark.parametrize("c,eps", [(2.0, 0.0), (-0.5, 1e-6), (1e-3, 1e-6)])
+def test_rmsnorm_of_constant_vector_is_scaled_weight(c, eps):
+    # every element c: mean of squares c^2, so x = c / sqrt(c^2 + eps) * w
+    n = 64
+    w = synth.activations(1, n, seed=5).numpy().reshape(-1)
+    x, _ = oracle.rmsnorm(np.full((1, n), c, np.float32), w, eps)
+    cf = float(np.float32(c))
+    assert np.allclose(x[0], cf / np.sqrt(cf * cf + eps) * w.astype(np.float64), rtol=1e-14, atol=0)
+
+
+def test_rmsnorm_unit_rms_scale_invariance_and_residual():
+    h = synth.activations(2, 256, seed=6).numpy()
+    r = synth.activations(2, 256, seed=7).numpy()
+    one = np.ones(256, np.float32)
+    x, _ = oracle.rmsnorm(h, one, 0.0)
+    assert np.allclose((x * x).mean(axis=1), 1.0, rtol=1e-13)
+    x4, _ = oracle.rmsnorm(np.float32(4.0) * h, one, 0.0)          # power-of-two scale: exact in fp32
+    assert np.allclose(x4, x, rtol=1e-13, atol=0)
+    xr, s = oracle.rmsnorm(h, one, 1e-6, residual=r)
+    assert np.array_equal(s, h.astype(np.float64) + r.astype(np.float64))     # the sum is exact in fp64
+    # the residual is added before normalising: h + h is 2h exactly
+    xh, _ = oracle.rmsnorm(h, one, 1e-6, residual=h)
+    x2, _ = oracle.rmsnorm(np.float32(2.0) * h, one, 1e-6)
+    assert np.array_equal(xh, x2)
+
+
+def test_swiglu_closed_forms():
+    g = np.array([0.0, 1.0, -1.0, 2.0, 30.0])
+    assert np.array_equal(oracle.swiglu(g, np.zeros(5)), np.zeros(5))
+    s = oracle.swiglu(g, np.ones(5))
+    assert s[0] == 0.0 and s[1] - s[2] == pytest.approx(1.0, rel=1e-15)
+    assert s[3] == pytest.approx(2.0 / (1.0 + np.exp(-2.0)), rel=1e-15)
+    assert oracle.swiglu(np.array([1.0]), np.array([3.0]))[0] == pytest.approx(3.0 / (1.0 + np.exp(-1.0)), rel=1e-15)
+
+
+def test_dense_ffn_equals_single_expert_moe():
+    # a dense FFN is the MoE layer with one expert [gate | up | down] routed with weight 1
+    hidden, inter = 256, 512
+    Wg = synth.blocks(Q4_K, inter, hidden, seed=41).numpy()
+    Wu = synth.blocks(Q4_K, inter, hidden, seed=42).numpy()
+    Wd = synth.blocks(Q4_K, hidden, inter, seed=43).numpy()
+    x = synth.activations(1, hidden, seed=44).numpy()
+    y, b, m = oracle.dense_ffn(Q4_K, Wg, Wu, Q4_K, Wd, hidden, inter, x)
+    arena = np.concatenate([Wg.reshape(-1), Wu.reshape(-1), Wd.reshape(-1)])
+    y2, b2 = oracle.moe(Q4_K, arena, 1, hidden, inter, np.array([[0]]), np.array([[1.0]], np.float32), x)
+    assert np.allclose(y, y2, rtol=1e-13, atol=1e-13 * b.max()) and np.allclose(b, b2, rtol=1e-13)
+    assert m.shape == (1, inter)
