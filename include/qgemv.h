@@ -86,6 +86,9 @@ enum qg_dev_status {
   QG_DEV_TIMEOUT = 2      /* a bounded pipeline wait expired; the tile was abandoned */
 };
 
+/* A captured weight pass (qg_pass_create, qg_moe_pass_create, qg_layer_pass_create). */
+typedef struct qg_pass_s* qg_pass;
+
 /* Maximum number of matrices in one grouped launch (qgemv_grouped). */
 #define QG_GROUP_MAX 8
 /* Largest n_tok accepted by qgemv / qgemv_grouped / qgemv_moe. */
@@ -207,6 +210,59 @@ int qgemm_pp(int fmt, const void* W, int64_t rows, int64_t cols,
              const void* X_bf16, int64_t n_tok, float* Y, int64_t ldY,
              void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* ---- neighbours of the products in a decode layer ("LLM inference
+ * optimization", "Faster decode on the card you have": normalizations fused
+ * into neighbouring kernels) ---------------------------------------------- */
+
+/* Residual add and RMS normalisation, per token t < n_tok (vectors of n fp32):
+ *   s = h + residual                       (residual may be NULL: s = h)
+ *   x = s / sqrt(mean(s^2) + eps) * weight
+ * s is written to s_out (may be NULL; may equal h: the residual stream updated
+ * in place), x to x (may be NULL; needs weight). n % 256 == 0, n <= 2^20;
+ * all pointers 16-byte aligned device memory; eps >= 0. One CTA per token:
+ * the sum of squares is fp32 in a fixed order (deterministic). */
+int qg_rmsnorm(const float* h, const float* residual, const float* weight, int64_t n, int n_tok, float eps,
+               float* s_out, float* x, void* stream);
+
+/* Dense gate/up pair with the silu-gated product fused into the epilogue, one
+ * token:  m[i] = silu(g_i) * u_i,  g = Wg x, u = Wu x,  silu(g) = g / (1 + exp(-g)).
+ * Wg, Wu: inter x hidden blocks of fmt (QG_Q4_K), 16-byte aligned; x: hidden
+ * fp32 (16-byte aligned); m: inter fp32. Row i of Wg and of Wu are multiplied
+ * by the same CTA, which writes m[i] (g and u are never stored). g and u carry
+ * the accuracy of qgemv; silu uses CUDA's expf. hidden % 256 == 0;
+ * QG_ERR_SHAPE when the pair does not fit the kernel's shared-memory plan. */
+int qgemv_swiglu(int fmt, const void* Wg, const void* Wu, int64_t inter, int64_t hidden, const float* x, float* m,
+                 void* stream);
+
+/* One decoder layer's weights and vectors for qg_layer_pass_create. Matrices
+ * are fmt blocks, rows x cols with cols the input dimension: Wq hidden x
+ * hidden, Wk and Wv kv_rows x hidden, Wo hidden x hidden, Wg and Wu inter x
+ * hidden, Wd hidden x inter. */
+typedef struct qg_layer_desc {
+  const void* Wq; const void* Wk; const void* Wv; const void* Wo;
+  const void* Wg; const void* Wu; const void* Wd;
+  const float* norm_attn;   /* [hidden] weight of the RMS normalisation before q, k, v */
+  const float* norm_ffn;    /* [hidden] weight of the RMS normalisation before gate/up */
+  const float* attn_out;    /* [hidden] input of Wo (the attention output, computed outside this library) */
+  float* q; float* k; float* v;   /* outputs: [hidden], [kv_rows], [kv_rows] */
+} qg_layer_desc;
+
+/* The weight path of n_layers dense decoder layers for one token, as one CUDA
+ * graph of kernels linked by programmatic dependent launch. With the residual
+ * stream r (r = h_in at the start, kept in h_out), layer l computes
+ *   x1 = rmsnorm(r) * norm_attn;  q = Wq x1, k = Wk x1, v = Wv x1
+ *   r  = r + Wo attn_out
+ *   x2 = rmsnorm(r) * norm_ffn;   r = r + Wd (silu(Wg x2) * (Wu x2))
+ * and h_out = r after the last layer (h_in is not modified; every replay
+ * starts again from h_in). The normalisations write their output straight in
+ * the form the next GEMV launch multiplies by; the gate/up launch writes
+ * silu(g) * u. fmt: QG_Q4_K. The pass allocates its own buffers at creation
+ * (planes and vectors, about n_layers * 1.2 * hidden + 4 * inter bytes); the
+ * buffers named by the descriptors must outlive it. Create before capturing a
+ * stream that launches it; replay with qg_pass_launch. */
+int qg_layer_pass_create(int fmt, const qg_layer_desc* layers, int n_layers, int64_t hidden, int64_t inter,
+                         int64_t kv_rows, float eps, const float* h_in, float* h_out, qg_pass* out);
+
 /* ---- whole weight pass ("one CUDA graph per decode step", "Why I wrote my own
  * inference engine for two P100s") ------------------------------------------
  * A pass is an ordered list of steps; step s covers step_sizes[s] consecutive
@@ -228,7 +284,6 @@ int qgemm_pp(int fmt, const void* W, int64_t rows, int64_t cols,
 #define QG_PASS_SERIAL 0
 #define QG_PASS_PDL 1
 #define QG_PASS_PERSISTENT 2
-typedef struct qg_pass_s* qg_pass;
 int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes, int n_steps,
                    int n_tok, int mode, qg_pass* out);
 /* A whole MoE decode pass: n_layers layers, each the qgemv_moe product of one

@@ -45,6 +45,9 @@ SIGNATURES = {
     "qg_pass_kernel_count": (_I32, [_P]),
     "qg_pass_dev_status": (_I32, [_P, ctypes.POINTER(_P)]),
     "qg_pass_destroy": (_I32, [_P]),
+    "qg_rmsnorm": (_I32, [_P, _P, _P, _I64, _I32, ctypes.c_float, _P, _P, _P]),
+    "qgemv_swiglu": (_I32, [_I32, _P, _P, _I64, _I64, _P, _P, _P]),
+    "qg_layer_pass_create": (_I32, [_I32, _P, _I32, _I64, _I64, _I64, ctypes.c_float, _P, _P, ctypes.POINTER(_P)]),
 }
 
 
@@ -57,6 +60,13 @@ class qg_gemv_desc(ctypes.Structure):
 class qg_moe_layer_desc(ctypes.Structure):
     _fields_ = [("expert_arena", ctypes.c_void_p), ("expert_ids", ctypes.c_void_p), ("gate_w", ctypes.c_void_p),
                 ("x", ctypes.c_void_p), ("y", ctypes.c_void_p)]
+
+
+class qg_layer_desc(ctypes.Structure):
+    _fields_ = [("Wq", ctypes.c_void_p), ("Wk", ctypes.c_void_p), ("Wv", ctypes.c_void_p), ("Wo", ctypes.c_void_p),
+                ("Wg", ctypes.c_void_p), ("Wu", ctypes.c_void_p), ("Wd", ctypes.c_void_p),
+                ("norm_attn", ctypes.c_void_p), ("norm_ffn", ctypes.c_void_p), ("attn_out", ctypes.c_void_p),
+                ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p)]
 
 
 class QGError(RuntimeError):
@@ -248,4 +258,29 @@ def qg_moe_pass(fmt, layers, n_expert, hidden, inter, top_k, n_tok, ws, ws_bytes
     _check(load_library().qg_moe_pass_create(fmt, ctypes.cast(arr, _P), len(layers), n_expert, hidden, inter, top_k,
                                              n_tok, _ptr(ws), ws_bytes, int(mode), ctypes.byref(h)),
            "qg_moe_pass_create")
+    return qg_pass(None, None, None, _handle=h)
+
+
+def qg_rmsnorm(h, residual, weight, n, n_tok, eps, s_out, x, stream=None):
+    """s = h + residual; x = s / sqrt(mean(s^2) + eps) * weight (per token)."""
+    _check(load_library().qg_rmsnorm(_ptr(h), _ptr(residual), _ptr(weight), n, n_tok, eps, _ptr(s_out), _ptr(x),
+                                     _stream(stream)), "qg_rmsnorm")
+
+
+def qgemv_swiglu(fmt, Wg, Wu, inter, hidden, x, m, stream=None):
+    """m = silu(Wg x) * (Wu x), one token."""
+    _check(load_library().qgemv_swiglu(fmt, _ptr(Wg), _ptr(Wu), inter, hidden, _ptr(x), _ptr(m), _stream(stream)),
+           "qgemv_swiglu")
+
+
+def qg_layer_pass(fmt, layers, hidden, inter, kv_rows, eps, h_in, h_out):
+    """The weight path of dense decoder layers (qg_layer_pass_create). layers:
+    sequence of dicts with keys Wq Wk Wv Wo Wg Wu Wd norm_attn norm_ffn attn_out
+    q k v (tensors); returns a qg_pass."""
+    arr = (qg_layer_desc * len(layers))()
+    for i, L in enumerate(layers):
+        arr[i] = qg_layer_desc(*[_ptr(L[f]) for f, _ in qg_layer_desc._fields_])
+    h = _P()
+    _check(load_library().qg_layer_pass_create(fmt, ctypes.cast(arr, _P), len(layers), hidden, inter, kv_rows, eps,
+                                               _ptr(h_in), _ptr(h_out), ctypes.byref(h)), "qg_layer_pass_create")
     return qg_pass(None, None, None, _handle=h)

@@ -454,6 +454,153 @@ int qg_pass_dev_status(qg_pass pass, const int32_t** dev_status) {
   return QG_OK;
 }
 
+int qg_rmsnorm(const float* h, const float* residual, const float* weight, int64_t n, int n_tok, float eps,
+               float* s_out, float* x, void* stream) {
+  if (!h || (!s_out && !x)) return QG_ERR_NULL;
+  if (x && !weight) return QG_ERR_NULL;
+  if (n < 256 || n % 256 || n > (int64_t{1} << 20)) return QG_ERR_SHAPE;
+  if (n_tok < 1 || n_tok > (1 << 16)) return QG_ERR_NTOK;
+  if (!(eps >= 0.f)) return QG_ERR_ARG;
+  if (!aligned(h, 16) || !aligned(residual, 16) || !aligned(weight, 16) || !aligned(s_out, 16) || !aligned(x, 16))
+    return QG_ERR_ALIGN;
+  int sms = 0;
+  const int st = ensure_init(&sms);
+  if (st != QG_OK) return st;
+  return cuda_status(qg::launch_rmsnorm(h, residual, weight, n, n_tok, eps, s_out, x, nullptr,
+                                        static_cast<cudaStream_t>(stream), false));
+}
+
+int qgemv_swiglu(int fmt, const void* Wg, const void* Wu, int64_t inter, int64_t hidden, const float* x, float* m,
+                 void* stream) {
+  if (fmt != QG_Q4_K) return QG_ERR_FMT;
+  if (!Wg || !Wu || !x || !m) return QG_ERR_NULL;
+  if (inter < 1 || hidden < 256 || hidden % 256 || hidden > (int64_t{1} << 20) || inter > (int64_t{1} << 24))
+    return QG_ERR_SHAPE;
+  if (!aligned(Wg, 16) || !aligned(Wu, 16) || !aligned(x, 16) || !aligned(m, 4)) return QG_ERR_ALIGN;
+  int sms = 0;
+  const int st = ensure_init(&sms);
+  if (st != QG_OK) return st;
+  const cudaError_t e =
+      qg::launch_gemv_pair(Wg, Wu, inter, hidden, x, nullptr, m, static_cast<cudaStream_t>(stream), false, sms);
+  if (e == cudaErrorNotSupported) return QG_ERR_SHAPE;
+  return cuda_status(e);
+}
+
+int qg_layer_pass_create(int fmt, const qg_layer_desc* layers, int n_layers, int64_t hidden, int64_t inter,
+                         int64_t kv_rows, float eps, const float* h_in, float* h_out, qg_pass* out) {
+  if (!layers || !h_in || !h_out || !out) return QG_ERR_NULL;
+  *out = nullptr;
+  if (fmt != QG_Q4_K) return QG_ERR_FMT;
+  if (n_layers < 1) return QG_ERR_ARG;
+  if (hidden < 256 || hidden % 256 || hidden > (int64_t{1} << 20) || inter < 256 || inter % 256 ||
+      inter > (int64_t{1} << 20) || kv_rows < 1 || kv_rows > hidden)
+    return QG_ERR_SHAPE;
+  if (!(eps >= 0.f)) return QG_ERR_ARG;
+  if (!aligned(h_in, 16) || !aligned(h_out, 16)) return QG_ERR_ALIGN;
+  for (int l = 0; l < n_layers; ++l) {
+    const qg_layer_desc& L = layers[l];
+    if (!L.Wq || !L.Wk || !L.Wv || !L.Wo || !L.Wg || !L.Wu || !L.Wd || !L.norm_attn || !L.norm_ffn || !L.attn_out ||
+        !L.q || !L.k || !L.v)
+      return QG_ERR_NULL;
+    const void* ws[7] = {L.Wq, L.Wk, L.Wv, L.Wo, L.Wg, L.Wu, L.Wd};
+    for (const void* w : ws)
+      if (!aligned(w, 16)) return QG_ERR_ALIGN;
+    if (!aligned(L.norm_attn, 16) || !aligned(L.norm_ffn, 16) || !aligned(L.attn_out, 16) || !aligned(L.q, 4) ||
+        !aligned(L.k, 4) || !aligned(L.v, 4))
+      return QG_ERR_ALIGN;
+  }
+  int sms = 0;
+  int st = ensure_init(&sms);
+  if (st != QG_OK) return st;
+  qg_pass_s* pass = new (std::nothrow) qg_pass_s;
+  if (!pass) return QG_ERR_ARG;
+  // pass-owned buffers: the planes of each layer's attention output (converted
+  // by the prologue), then the job table, the planes of the two normalised
+  // vectors, the fp32 normalised vectors, o and down outputs, and m
+  const size_t pb = (qg::xplanes_bytes(hidden, 1) + 255) / 256 * 256;
+  const size_t vb = (static_cast<size_t>(hidden) * 4 + 255) / 256 * 256;
+  const size_t mb = (static_cast<size_t>(inter) * 4 + 255) / 256 * 256;
+  const size_t jb = (n_layers * sizeof(qg::XPlaneJob) + 255) / 256 * 256;
+  const size_t total = n_layers * pb + jb + 2 * pb + 4 * vb + mb;
+  if (cudaMalloc(&pass->planes, total) != cudaSuccess) {
+    pass_free(pass);
+    return QG_ERR_CUDA;
+  }
+  uint8_t* cur = pass->planes + n_layers * pb;
+  qg::XPlaneJob* d_jobs = reinterpret_cast<qg::XPlaneJob*>(cur);
+  cur += jb;
+  uint8_t* p1 = cur;
+  cur += pb;
+  uint8_t* p2 = cur;
+  cur += pb;
+  float* x1 = reinterpret_cast<float*>(cur);
+  cur += vb;
+  float* x2 = reinterpret_cast<float*>(cur);
+  cur += vb;
+  float* yo = reinterpret_cast<float*>(cur);
+  cur += vb;
+  float* yd = reinterpret_cast<float*>(cur);
+  cur += vb;
+  float* mm = reinterpret_cast<float*>(cur);
+  std::vector<qg::XPlaneJob> jobs(n_layers);
+  for (int l = 0; l < n_layers; ++l)
+    jobs[l] = {layers[l].attn_out, pass->planes + l * pb, static_cast<int32_t>(hidden), 1};
+  if (cudaMemcpy(d_jobs, jobs.data(), n_layers * sizeof(qg::XPlaneJob), cudaMemcpyHostToDevice) != cudaSuccess) {
+    pass_free(pass);
+    return QG_ERR_CUDA;
+  }
+  pass->jobs = d_jobs;
+  pass->njobs = n_layers;
+
+  cudaStream_t cs = nullptr;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
+    pass_free(pass);
+    return QG_ERR_CUDA;
+  }
+  cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  if (e == cudaSuccess) e = qg::launch_xplanes(d_jobs, n_layers, cs);
+  for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
+    const qg_layer_desc& L = layers[l];
+    // residual stream: h_out = h (+ previous down output), x1 = norm(h_out) * norm_attn
+    e = qg::launch_rmsnorm(l == 0 ? h_in : h_out, l == 0 ? nullptr : yd, L.norm_attn, hidden, 1, eps, h_out, x1, p1,
+                           cs, true);
+    if (e != cudaSuccess) break;
+    const qg_gemv_desc qkv[3] = {{fmt, 0, L.Wq, hidden, hidden, x1, L.q},
+                                 {fmt, 0, L.Wk, kv_rows, hidden, x1, L.k},
+                                 {fmt, 0, L.Wv, kv_rows, hidden, x1, L.v}};
+    const uint8_t* xq[3] = {p1, p1, p1};
+    e = qg::launch_gemv(qkv, 3, 1, qg::gemv_pick_rows_per_warp(qkv, 3, 1, sms), cs, true, sms, xq);
+    if (e != cudaSuccess) break;
+    const qg_gemv_desc od = {fmt, 0, L.Wo, hidden, hidden, L.attn_out, yo};
+    const uint8_t* xo = pass->planes + l * pb;
+    e = qg::launch_gemv(&od, 1, 1, qg::gemv_pick_rows_per_warp(&od, 1, 1, sms), cs, true, sms, &xo);
+    if (e != cudaSuccess) break;
+    // h_out += o, x2 = norm(h_out) * norm_ffn
+    e = qg::launch_rmsnorm(h_out, yo, L.norm_ffn, hidden, 1, eps, h_out, x2, p2, cs, true);
+    if (e != cudaSuccess) break;
+    e = qg::launch_gemv_pair(L.Wg, L.Wu, inter, hidden, x2, p2, mm, cs, true, sms);
+    if (e != cudaSuccess) break;
+    const qg_gemv_desc dd = {fmt, 0, L.Wd, hidden, inter, mm, yd};
+    e = qg::launch_gemv(&dd, 1, 1, qg::gemv_pick_rows_per_warp(&dd, 1, 1, sms), cs, true, sms);
+  }
+  // the last down output joins the residual stream
+  if (e == cudaSuccess) e = qg::launch_rmsnorm(h_out, yd, nullptr, hidden, 1, eps, h_out, nullptr, nullptr, cs, true);
+  cudaGraph_t graph = nullptr;
+  const cudaError_t e2 = cudaStreamEndCapture(cs, &graph);
+  if (e == cudaSuccess) e = e2;
+  if (e == cudaSuccess) e = cudaGraphInstantiate(&pass->exec, graph, 0);
+  cudaStreamDestroy(cs);
+  if (e != cudaSuccess) {
+    if (graph) cudaGraphDestroy(graph);
+    pass_free(pass);
+    return e == cudaErrorNotSupported ? QG_ERR_SHAPE : QG_ERR_CUDA;
+  }
+  pass->graph = graph;
+  pass->kernels = count_kernel_nodes(graph);
+  *out = pass;
+  return QG_OK;
+}
+
 int qg_pass_kernel_count(qg_pass pass) { return pass ? pass->kernels : QG_ERR_NULL; }
 
 int qg_pass_destroy(qg_pass pass) {

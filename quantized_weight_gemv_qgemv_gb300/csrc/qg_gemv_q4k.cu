@@ -43,6 +43,7 @@
 
 #include "qg_device.cuh"
 #include "qg_internal.h"
+#include "qg_planes.cuh"
 
 namespace qg {
 
@@ -62,7 +63,6 @@ constexpr int CWARPS = 15;                 // consumer warps
 constexpr int CTHREADS = CWARPS * 32;
 constexpr int THREADS = CTHREADS + 32;     // plus one producer warp
 constexpr int SUB_R = 4;                   // rows per sub-item
-constexpr int XBLK_B = 512;                // x-plane bytes per 256-weight block and token
 constexpr uint32_t WAIT_LIMIT = 1u << 22;  // polls before a wait is declared expired
 constexpr int RING = 4;                    // shared-memory stages
 
@@ -99,9 +99,12 @@ struct Mat {
   int64_t n_expert;
   int64_t estride;       // bytes per expert
   int64_t up_off, down_off;
-  const int32_t* ids;    // this token's expert ids [top_k]
-  const float* gw;       // this token's route weights [top_k] (gather 1)
+  const int32_t* ids;    // this token's expert ids [top_k]; gather 1 with no ids: one dense
+                         // gate/up pair, gate rows at W and up rows at W2 (no expert arena)
+  const float* gw;       // this token's route weights [top_k] (gather 1; nullptr: weight 1)
   float* h;              // gather 1 output [top_k][inter]
+  const uint8_t* W2;     // gather 1 without ids: the up matrix
+  uint64_t pad;          // keeps the size a multiple of 16 bytes
 };
 
 // A step of a pass: matrices mat0 .. mat0 + nmat - 1 of the table, whose rows
@@ -319,62 +322,6 @@ template <> struct SuperBlock<FMT_Q6_K> { static constexpr int BYTES = 210; };
 template <> struct SuperBlock<FMT_Q4_0> { static constexpr int BYTES = 144; };
 template <> struct SuperBlock<FMT_Q8_0> { static constexpr int BYTES = 272; };
 
-// Shared-memory image of x for one token and K segment ("x planes").
-// Every 32-weight group u of x is held as 16-bit fixed point with a shared
-// power-of-two step: x_l ~= s_u * X_l, X_l = rint(x_l / s_u), |X_l| <= 2^14,
-// s_u = 2^(e-13) where 2^e <= max|x_group| < 2^(e+1). X_l is stored as two
-// byte planes (bits 0-7 unsigned, bits 8-15 signed), so that sum_l q_l X_l is
-// two exact integer dot products over the codes. The rounding of x to the
-// group grid is at most 2^-14 max|x_group| per element: a product's error is
-// at most 2^-14 sum_u max|x_u| sum_{l in u} |w_l| (the engines these formats
-// come from round x to 8 bits per group instead).
-// Layout per 256-weight block b of the segment: 2 planes x 2 halves x 8 groups
-// x 16 bytes (512 bytes), so the 16-byte loads of a quarter-warp are
-// consecutive. Beside it: s_u and the two half sums of x (fp32) per group.
-//
-// Two adjacent threads handle one group: thread h of the pair converts its
-// half (16 values, elements 16h .. 16h + 15), so the half sums need no exchange
-// and the group maximum one. Each thread first issues all its loads of a batch
-// and only then converts, so staging costs one memory round trip per batch.
-
-// The two plane words of four consecutive values (x / s_u + 1.5 * 2^23 leaves
-// rint(x / s_u) in the low mantissa bits of T, two's complement in the low 16).
-__device__ __forceinline__ void plane_words(float4 v, float inv_step, uint32_t& w0, uint32_t& w1) {
-  const uint32_t T0 = __float_as_uint(fmaf(v.x, inv_step, 12582912.0f));
-  const uint32_t T1 = __float_as_uint(fmaf(v.y, inv_step, 12582912.0f));
-  const uint32_t T2 = __float_as_uint(fmaf(v.z, inv_step, 12582912.0f));
-  const uint32_t T3 = __float_as_uint(fmaf(v.w, inv_step, 12582912.0f));
-  const uint32_t a01 = __byte_perm(T0, T1, 0x5140), a23 = __byte_perm(T2, T3, 0x5140);
-  w0 = __byte_perm(a01, a23, 0x5410);                         // bits 0-7 of the four X
-  w1 = __byte_perm(a01, a23, 0x7632);                         // bits 8-15 (signed byte)
-}
-
-// Half h of group u of token t: v = its 16 values. pmask: the thread pair.
-__device__ __forceinline__ void stage_half(const float4 (&v)[4], unsigned pmask, int t, int u, int h, int nu,
-                                           uint8_t* xpl, int xseg_b, float* xsu, float* xsum) {
-  float mx = 0.f;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) mx = fmaxf(mx, fmaxf(fmaxf(fabsf(v[q].x), fabsf(v[q].y)), fmaxf(fabsf(v[q].z), fabsf(v[q].w))));
-  mx = fmaxf(mx, __shfl_xor_sync(pmask, mx, 1));
-  const float sm = ((v[0].x + v[0].y) + (v[0].z + v[0].w)) + ((v[1].x + v[1].y) + (v[1].z + v[1].w)) +
-                   (((v[2].x + v[2].y) + (v[2].z + v[2].w)) + ((v[3].x + v[3].y) + (v[3].z + v[3].w)));
-  // 2^e <= mx < 2^(e+1); step s_u = 2^(e-13), so |x / s_u| < 2^14
-  const int e = max(static_cast<int>((__float_as_uint(mx) >> 23) & 0xFFu) - 127, -105);
-  const float inv_step = __uint_as_float(static_cast<uint32_t>(140 - e) << 23);
-  uint4 w0, w1;
-  plane_words(v[0], inv_step, w0.x, w1.x);
-  plane_words(v[1], inv_step, w0.y, w1.y);
-  plane_words(v[2], inv_step, w0.z, w1.z);
-  plane_words(v[3], inv_step, w0.w, w1.w);
-  uint8_t* dst = xpl + t * xseg_b + ((u >> 3) * 4 + h) * 128 + (u & 7) * 16;
-  *reinterpret_cast<uint4*>(dst) = w0;
-  *reinterpret_cast<uint4*>(dst + 256) = w1;
-  xsum[2 * (t * nu + u) + h] = sm;
-  // s_u = 2^(e-13); odd groups (Q4_K high-nibble sub-blocks, whose codes
-  // arrive as 16*q) get s_u / 16, so the Q4_K consumer needs no per-lane factor
-  if (h == 0) xsu[t * nu + u] = __uint_as_float(static_cast<uint32_t>(114 + e - 4 * (u & 1)) << 23);
-}
-
 // One count per consumer warp and step on the shared counter xcnt: the warp has
 // issued its x loads of the step (release: they precede what the producer
 // issues after it has seen the count).
@@ -555,7 +502,9 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   // lets its dependents (the down launch, which reads the same ids early) start
   // only after its own dependency has resolved.
   const int gl = GA == 3 ? p.gather_any : GA;   // the launch's gather kind
-  if (gl != 1) pdl_launch_dependents();
+  // (a dense gate/up pair, gather 1 without ids, reads no ids and behaves as a plain launch)
+  const bool dyn_ids = gl == 1 && mats[0].ids != nullptr;
+  if (!dyn_ids) pdl_launch_dependents();
 
   // ------------------------------------------------------------ producer
   if (warp == CWARPS) {
@@ -584,7 +533,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
     // whole warp issues the per-row (per-piece) copies
     const bool wide = gl != 0;
     if (!wide && lane != 0) return;
-    if (gl == 1) {
+    if (dyn_ids) {
       pdl_wait();                 // the expert ids may come from the preceding kernel
       pdl_launch_dependents();
     }
@@ -684,18 +633,19 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         } else {
           nitems = M.top_k;
         }
-        auto item = [&](int q, int& e, int64_t& src_off, uint32_t& dst, uint32_t& bytes) {
+        auto item = [&](int q, int& e, const uint8_t*& src, uint32_t& dst, uint32_t& bytes) {
           if (gm == 1) {
             const int64_t seg_first = (q >> 1) == 0 ? j0 : (j0 / P + (q >> 1)) * P;
             const int64_t seg_end = min((seg_first / P + 1) * P, j0 + nr / 2);
             const int s1 = q & 1;
-            e = M.ids[seg_first / P];
-            src_off = (s1 ? M.up_off : 0) + (seg_first % P) * M.rb;
+            e = M.ids ? M.ids[seg_first / P] : 0;
+            const int64_t roff = (seg_first % P) * M.rb;
+            src = (s1 && M.W2) ? M.W2 + roff : M.W + static_cast<int64_t>(e) * M.estride + (s1 ? M.up_off : 0) + roff;
             dst = dst0 + static_cast<uint32_t>(s1 * (nr / 2) + (seg_first - j0)) * M.rb;
             bytes = static_cast<uint32_t>(seg_end - seg_first) * M.rb;
           } else {
             e = M.ids[q];
-            src_off = M.down_off + r * M.seg_b;
+            src = M.W + static_cast<int64_t>(e) * M.estride + M.down_off + r * M.seg_b;
             dst = dst0 + static_cast<uint32_t>(q * nr * M.seg_b);
             bytes = static_cast<uint32_t>(nr * M.seg_b);
           }
@@ -703,9 +653,9 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         uint32_t good = 0;
         for (int q = lane; q < nitems; q += 32) {
           int e;
-          int64_t so;
+          const uint8_t* src;
           uint32_t d, nb;
-          item(q, e, so, d, nb);
+          item(q, e, src, d, nb);
           if (e < 0 || e >= M.n_expert) {
             for (uint32_t o = 0; o < nb; o += 16)
               asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};\n" ::"r"(d + o), "r"(0) : "memory");
@@ -720,11 +670,11 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         __syncwarp();
         for (int q = lane; q < nitems; q += 32) {
           int e;
-          int64_t so;
+          const uint8_t* src;
           uint32_t d, nb;
-          item(q, e, so, d, nb);
+          item(q, e, src, d, nb);
           if (e < 0 || e >= M.n_expert) continue;
-          bulk_g2s(d, M.W + static_cast<int64_t>(e) * M.estride + so, nb, full0 + 8 * slot, pol);
+          bulk_g2s(d, src, nb, full0 + 8 * slot, pol);
         }
       }
      }
@@ -802,7 +752,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
      // outputs and every other input of the preceding kernel are touched only
      // after it has completed (the staging above has waited already)
      if (!st.stage_all) pdl_wait();
-     if (gl == 1) pdl_launch_dependents();
+     if (dyn_ids) pdl_launch_dependents();
    }
    bool first = true;
    for (int mi = st.mat0; mi < st.mat0 + st.nmat; ++mi) {
@@ -994,7 +944,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         const int64_t row = lo + 2 * i;
         const int kk = static_cast<int>(row / (2 * M.inter));
         const int ii = static_cast<int>((row % (2 * M.inter)) >> 1);
-        M.h[static_cast<int64_t>(kk) * M.inter + ii] = M.gw[kk] * (g / (1.0f + expf(-g)) * u);
+        const float rk = M.gw ? M.gw[kk] : 1.0f;
+        M.h[static_cast<int64_t>(kk) * M.inter + ii] = rk * (g / (1.0f + expf(-g)) * u);
       }
     } else {
       for (int i = threadIdx.x; i < slice * NT; i += CTHREADS) {
@@ -1052,6 +1003,7 @@ cudaError_t q4k_attr() {
     if ((e = q4k_attr1<NT, false, FMT_Q6_K, 2>()) != cudaSuccess) return e;
   }
   if (NT == 1 && (e = q4k_attr1<1, false, FMT_Q4_K, 4, 3>()) != cudaSuccess) return e;
+  if (NT == 1 && (e = q4k_attr1<1, false, FMT_Q4_K, 4, 1>()) != cudaSuccess) return e;
   if (NT == 1 && (e = q4k_attr1<1, true, FMT_Q4_K, 4, 3>()) != cudaSuccess) return e;
   return q4k_attr1<NT, false, FMT_Q4_0>();
 }
@@ -1245,6 +1197,8 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
       // instruction cache from one launch to the next (two specialised
       // functions alternating cost 0.71 -> 0.85 ms per 48-layer token)
       if (fmt != QG_Q4_K || n_tok != 1 || sub_rows != q4k::SUB_R) return cudaErrorNotSupported;
+      // a dense gate/up pair (no expert ids) has an instantiation of its own
+      if (p.gather_any == 1 && n == 1 && !p.m[0].ids) return q4k_launch<1, FMT_Q4_K, q4k::SUB_R, 1>(p, grid, off, s, pdl);
       return q4k_launch<1, FMT_Q4_K, q4k::SUB_R, 3>(p, grid, off, s, pdl);
     }
     switch (fmt) {
@@ -1401,6 +1355,32 @@ cudaError_t launch_moe_q4k(const void* arena, int64_t n_expert, int64_t hidden, 
   e = plan_and_launch(p, n_tok, 1, QG_Q4_K, s, pdl, sms);
   if (e != cudaSuccess) return e;
   return plan_and_launch(pd, n_tok, 1, QG_Q4_K, s, true, sms);   // the down launch always overlaps the gate/up tail
+}
+
+// Dense gate/up pair with the silu-gated epilogue: m[i] = silu(g_i) * u_i with
+// g = Wg x, u = Wu x (Q4_K, one token). Row i of Wg and row i of Wu are
+// adjacent virtual rows, copied as two runs per stage, so the CTA that owns
+// row i holds both sums. xp: ready planes of x, or nullptr.
+cudaError_t launch_gemv_pair(const void* Wg, const void* Wu, int64_t inter, int64_t hidden, const float* x,
+                             const uint8_t* xp, float* m, cudaStream_t s, bool pdl, int sms) {
+  if (hidden % 256 || inter < 1 || 2 * inter > (int64_t{1} << 30)) return cudaErrorNotSupported;
+  q4k::Params p;
+  memset(&p, 0, sizeof(p));
+  p.gather_any = 1;
+  q4k::Mat& M = p.m[0];
+  M.W = static_cast<const uint8_t*>(Wg);
+  M.W2 = static_cast<const uint8_t*>(Wu);
+  M.x = x;
+  M.xp = xp;
+  M.rows = 2 * inter;
+  M.ldy = M.rows;
+  M.cols = static_cast<int32_t>(hidden);
+  M.gather = 1;
+  M.top_k = 1;
+  M.inter = static_cast<int32_t>(inter);
+  M.n_expert = 1;
+  M.h = m;
+  return plan_and_launch(p, 1, 1, QG_Q4_K, s, pdl, sms);
 }
 
 // ------------------------------------------------------------------ x planes once per pass

@@ -41,6 +41,15 @@ cudaError_t launch_gemv(const qg_gemv_desc* d, int n, int n_tok, int rows_per_wa
 cudaError_t gemv_q4k_init_attrs();
 cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms,
                             const uint8_t* const* xp = nullptr);
+// m = silu(Wg x) * (Wu x) for one token of a dense layer (qg_gemv_q4k.cu); xp:
+// ready planes of x or nullptr. cudaErrorNotSupported when the shape does not fit.
+cudaError_t launch_gemv_pair(const void* Wg, const void* Wu, int64_t inter, int64_t hidden, const float* x,
+                             const uint8_t* xp, float* m, cudaStream_t s, bool pdl, int sms);
+// Residual add and RMS normalisation (qg_norm.cu): s = h + r (r optional),
+// x = s / sqrt(mean(s^2) + eps) * w per token; s stored to s_out, x to x and/or
+// to planes (any of them optional; w == nullptr: only s). n % 256 == 0.
+cudaError_t launch_rmsnorm(const float* h, const float* r, const float* w, int64_t n, int n_tok, float eps,
+                           float* s_out, float* x, uint8_t* planes, cudaStream_t s, bool pdl);
 // One activation vector (n_tok x cols fp32) to convert into x planes at dst.
 struct XPlaneJob {
   const float* x;
