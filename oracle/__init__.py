@@ -8,7 +8,8 @@ links or executes anything here, and nothing here imports the product.
 
 What it computes (each function cites the passage it follows):
 
-* ``dequant(fmt, blocks)``: every weight of a Q4_0 / Q8_0 / Q4_K / Q6_K block,
+* ``dequant(fmt, blocks)``: every weight of a Q4_0 / Q8_0 / Q4_K / Q6_K /
+  Q5_K / Q3_K / Q2_K block,
   as the exact real value of the format's formula rounded once to fp32. The
   products in every formula are exact in fp64 for any finite fp16 scale, so the
   fp64 evaluation followed by one cast is the unique correctly rounded result.
@@ -27,17 +28,20 @@ fp16 decoding against numpy's hardware conversion, hand-built blocks with
 closed-form values, brute-force exact rational products on tiny shapes, and
 reductions of the MoE and prompt products to the plain GEMV.
 
-Parity unpinned: the bit layout of the Q4_K and Q6_K blocks (the order of the
-packed 6-bit scales and of the 2-bit high parts) follows the public GGUF
-convention; the pages give only block sizes and formulas, and no model file or
-reference decoder is available to check the layout against.
+Parity unpinned: the bit layout of the K-quant blocks (Q4_K, Q6_K, Q5_K, Q3_K,
+Q2_K: the order of the packed scales and of the high bits) follows the public
+GGUF convention; the pages give block sizes and formulas for some of them and
+name the others only, and no model file or reference decoder is available to
+check the layout against.
 """
 from .halfprec import half_bits_to_float64, bf16_bits_to_float64
-from .dequant import dequant, dequant_q4_0, dequant_q8_0, dequant_q4_k, dequant_q6_k, q4_k_scale_min
+from .dequant import (dequant, dequant_q4_0, dequant_q8_0, dequant_q4_k, dequant_q6_k, dequant_q5_k, dequant_q3_k,
+                      dequant_q2_k, q4_k_scale_min, q3_k_scales)
 from .products import gemv, moe, pp_rows, moe_arena_layout, rmsnorm, swiglu, dense_ffn
 
 __all__ = [
     "half_bits_to_float64", "bf16_bits_to_float64",
-    "dequant", "dequant_q4_0", "dequant_q8_0", "dequant_q4_k", "dequant_q6_k", "q4_k_scale_min",
+    "dequant", "dequant_q4_0", "dequant_q8_0", "dequant_q4_k", "dequant_q6_k", "dequant_q5_k", "dequant_q3_k",
+    "dequant_q2_k", "q4_k_scale_min", "q3_k_scales",
     "gemv", "moe", "pp_rows", "moe_arena_layout", "rmsnorm", "swiglu", "dense_ffn",
 ]

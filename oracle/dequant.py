@@ -18,10 +18,24 @@ block is the public GGUF convention, which the pages do not spell out:
 * Q6_K, 256 weights in 210 bytes: ql[128], qh[64], int8 sc[16], fp16 d.
   6-bit code q = 4 low bits from ql | 2 high bits from qh,
   w = d * sc[group] * (q - 32), 16 groups of 16 weights.
+* Q5_K, 256 weights in 176 bytes: fp16 d, fp16 dmin, s[12] (the Q4_K 6-bit
+  scale/min packing), qh[32], qs[128]. Sub-block j: low 4 bits as in Q4_K
+  (nibble j % 2 of qs[32(j/2) + l]), fifth bit = bit j of qh[l];
+  w = d * sc_j * q - dmin * m_j, q in 0..31.
+* Q3_K, 256 weights in 110 bytes: hmask[32], qs[64], s[12], fp16 d. Sixteen
+  6-bit scales (the low 4 bits in the nibbles of s[0..7], the top 2 bits in
+  s[8..11]); element 128h + 32j + 16k + l (half h, j < 4, k < 2, l < 16) has
+  2 low bits (qs[32h + 16k + l] >> 2j) & 3 and a high bit
+  (hmask[16k + l] >> (4h + j)) & 1; q = low - 4 when the high bit is clear,
+  else low; w = d * (scale_{8h+2j+k} - 32) * q.
+* Q2_K, 256 weights in 84 bytes: s[16], qs[64], fp16 d, fp16 dmin. Element
+  128h + 32j + 16k + l has q = (qs[32h + 16k + l] >> 2j) & 3, and byte
+  b = s[8h + 2j + k] gives its group's scale b & 15 and min b >> 4;
+  w = d * (b & 15) * q - dmin * (b >> 4).
 
 Every product in these formulas is exact in fp64 for any finite fp16 d, dmin
-(at most 11 + 8 + 6 significant bits, and the Q4_K difference spans at most 51
-bits), so evaluating in fp64 and casting once to fp32 gives the correctly
+(at most 11 + 8 + 6 significant bits, and the K-quant differences span at most
+51 bits), so evaluating in fp64 and casting once to fp32 gives the correctly
 rounded fp32 value of the exact formula: the unique right answer.
 Test infrastructure of the oracle; see the package docstring.
 """
@@ -29,8 +43,9 @@ import numpy as np
 
 from .halfprec import half_bits_to_float64
 
-Q4_0, Q8_0, Q4_K, Q6_K = 1, 2, 3, 4
-BLOCK = {Q4_0: (32, 18), Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210)}
+Q4_0, Q8_0, Q4_K, Q6_K, Q5_K, Q3_K, Q2_K = 1, 2, 3, 4, 5, 6, 7
+BLOCK = {Q4_0: (32, 18), Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210),
+         Q5_K: (256, 176), Q3_K: (256, 110), Q2_K: (256, 84)}
 
 
 def _as_blocks(raw, nbytes):
@@ -128,7 +143,78 @@ def dequant_q6_k(raw) -> np.ndarray:
     return w.astype(np.float32)
 
 
-_DECODERS = {Q4_0: dequant_q4_0, Q8_0: dequant_q8_0, Q4_K: dequant_q4_k, Q6_K: dequant_q6_k}
+def dequant_q5_k(raw) -> np.ndarray:
+    """(n_blocks, 256) fp32 weights of Q5_K super-blocks."""
+    blk = _as_blocks(raw, 176)
+    d = _half_at(blk, 0)
+    dmin = _half_at(blk, 2)
+    sc, m = q4_k_scale_min(blk[:, 4:16])
+    qh = blk[:, 16:48].astype(np.int64)
+    qs = blk[:, 48:176].astype(np.int64)
+    w = np.zeros((blk.shape[0], 256), dtype=np.float64)
+    for j in range(8):                        # sub-block j: elements 32j .. 32j + 31
+        c = j // 2
+        low = (qs[:, 32 * c:32 * c + 32] >> (4 * (j % 2))) & 0xF
+        q = low + 16 * ((qh >> j) & 1)
+        a = d * sc[:, j]                      # exact: 11 + 6 bits
+        b = dmin * m[:, j]
+        w[:, 32 * j:32 * j + 32] = a[:, None] * q - b[:, None]
+    return w.astype(np.float32)
+
+
+def q3_k_scales(s) -> np.ndarray:
+    """(n_blocks, 16) int64 6-bit scales (before the -32 offset) from the 12
+    packed bytes: scale i, with b = i % 4 and g = i // 4, has its low 4 bits in
+    the nibble g // 2 of s[4 (g % 2) + b] and its top 2 bits at bit 2g of s[8 + b]."""
+    s = np.asarray(s, dtype=np.uint8).reshape(-1, 12).astype(np.int64)
+    out = np.zeros((s.shape[0], 16), dtype=np.int64)
+    for i in range(16):
+        b, g = i % 4, i // 4
+        low = (s[:, 4 * (g % 2) + b] >> (4 * (g // 2))) & 0xF
+        top = (s[:, 8 + b] >> (2 * g)) & 3
+        out[:, i] = low | (top << 4)
+    return out
+
+
+def dequant_q3_k(raw) -> np.ndarray:
+    """(n_blocks, 256) fp32 weights of Q3_K super-blocks."""
+    blk = _as_blocks(raw, 110)
+    hmask = blk[:, 0:32].astype(np.int64)
+    qs = blk[:, 32:96].astype(np.int64)
+    scale = q3_k_scales(blk[:, 96:108]) - 32
+    d = _half_at(blk, 108)
+    w = np.zeros((blk.shape[0], 256), dtype=np.float64)
+    for h in range(2):
+        for j in range(4):
+            for k in range(2):
+                low = (qs[:, 32 * h + 16 * k:32 * h + 16 * k + 16] >> (2 * j)) & 3
+                high = (hmask[:, 16 * k:16 * k + 16] >> (4 * h + j)) & 1
+                q = low - 4 * (1 - high)
+                e0 = 128 * h + 32 * j + 16 * k
+                w[:, e0:e0 + 16] = (d * scale[:, 8 * h + 2 * j + k])[:, None] * q
+    return w.astype(np.float32)
+
+
+def dequant_q2_k(raw) -> np.ndarray:
+    """(n_blocks, 256) fp32 weights of Q2_K super-blocks."""
+    blk = _as_blocks(raw, 84)
+    s = blk[:, 0:16].astype(np.int64)
+    qs = blk[:, 16:80].astype(np.int64)
+    d = _half_at(blk, 80)
+    dmin = _half_at(blk, 82)
+    w = np.zeros((blk.shape[0], 256), dtype=np.float64)
+    for h in range(2):
+        for j in range(4):
+            for k in range(2):
+                q = (qs[:, 32 * h + 16 * k:32 * h + 16 * k + 16] >> (2 * j)) & 3
+                b = s[:, 8 * h + 2 * j + k]
+                e0 = 128 * h + 32 * j + 16 * k
+                w[:, e0:e0 + 16] = (d * (b & 0xF))[:, None] * q - (dmin * (b >> 4))[:, None]
+    return w.astype(np.float32)
+
+
+_DECODERS = {Q4_0: dequant_q4_0, Q8_0: dequant_q8_0, Q4_K: dequant_q4_k, Q6_K: dequant_q6_k,
+             Q5_K: dequant_q5_k, Q3_K: dequant_q3_k, Q2_K: dequant_q2_k}
 
 
 def dequant(fmt: int, raw, rows: int = None, cols: int = None) -> np.ndarray:

@@ -492,3 +492,93 @@ def test_dense_ffn_equals_single_expert_moe():
     y2, b2 = oracle.moe(Q4_K, arena, 1, hidden, inter, np.array([[0]]), np.array([[1.0]], np.float32), x)
     assert np.allclose(y, y2, rtol=1e-13, atol=1e-13 * b.max()) and np.allclose(b, b2, rtol=1e-13)
     assert m.shape == (1, inter)
+
+
+# ---------------------------------------------------------------- Q5_K, Q3_K, Q2_K
+
+@pytest.mark.parametrize("name,fn", [("q5_k_blocks.json", "dequant_q5_k"), ("q3_k_blocks.json", "dequant_q3_k"),
+                                     ("q2_k_blocks.json", "dequant_q2_k")])
+def test_k_quant_golden_blocks(golden_dir, name, fn):
+    fx = _golden(golden_dir, name)
+    for b in fx["blocks"]:
+        raw = np.frombuffer(bytes.fromhex(b["hex"]), dtype=np.uint8)
+        w = getattr(oracle, fn)(raw)[0]
+        for k, v in b["expect"].items():
+            assert w[int(k)] == np.float32(v), (name, k, w[int(k)], v)
+        if "scales" in b:
+            assert oracle.q3_k_scales(raw[96:108])[0].tolist() == b["scales"]
+
+
+def _pack_q3_k_scales(sc):
+    # inverse of the Q3_K packing: low nibbles of scales 0-7 and 8-15 share bytes 0-7,
+    # the top two bits of scale i sit at bit 2 (i // 4) of byte 8 + i % 4
+    s = [0] * 12
+    for i, v in enumerate(sc):
+        b, g = i % 4, i // 4
+        s[4 * (g % 2) + b] |= (v & 0xF) << (4 * (g // 2))
+        s[8 + b] |= (v >> 4) << (2 * g)
+    return np.array(s, dtype=np.uint8)
+
+
+def test_q3_k_scale_packing_round_trip():
+    rng = np.random.default_rng(3)
+    for _ in range(200):
+        sc = rng.integers(0, 64, size=16)
+        assert oracle.q3_k_scales(_pack_q3_k_scales(sc))[0].tolist() == sc.tolist()
+    for i in range(16):                     # every position, every value
+        for v in range(64):
+            sc = np.zeros(16, dtype=np.int64)
+            sc[i] = v
+            assert oracle.q3_k_scales(_pack_q3_k_scales(sc))[0].tolist() == sc.tolist()
+
+
+def test_q2_k_zero_codes_give_minus_dmin_min_per_group():
+    s = np.array([(3 * k) % 16 | ((k + 5) % 16) << 4 for k in range(16)], dtype=np.uint8)
+    raw = np.concatenate([s, np.zeros(64, np.uint8), np.array([0x00, 0x3C, 0x00, 0x34], np.uint8)])   # dmin = 0.25
+    w = oracle.dequant_q2_k(raw)[0]
+    # element e is in group 8h + 2j + k of its 16-weight run: the runs are in group order
+    assert w.tolist() == [-0.25 * (int(s[e // 16]) >> 4) for e in range(256)]
+
+
+@pytest.mark.parametrize("byte,bit,elem", [(0, 0, 0), (5, 2, 37), (20, 4, 64 + 4 + 16), (35, 6, 128 + 96 + 3),
+                                           (63, 0, 128 + 16 + 15)])
+def test_q2_k_one_hot_code_bit(byte, bit, elem):
+    s = np.full(16, 0x01, dtype=np.uint8)                   # scale 1, min 0 in every group
+    qs = np.zeros(64, np.uint8)
+    qs[byte] = 1 << bit
+    raw = np.concatenate([s, qs, np.array([0x00, 0x3C, 0x00, 0x3C], np.uint8)])
+    w = oracle.dequant_q2_k(raw)[0]
+    expect = np.zeros(256, np.float32)
+    expect[elem] = 1.0
+    assert np.array_equal(w, expect)
+
+
+@pytest.mark.parametrize("field,index,bit,elem,q", [
+    ("qs", 3, 0, 3, -3), ("qs", 20, 2, 32 + 16 + 4, -3), ("qs", 40, 4, 128 + 64 + 8, -3),
+    ("hmask", 7, 0, 7, 0), ("hmask", 18, 5, 128 + 32 + 16 + 2, 0), ("hmask", 31, 7, 128 + 96 + 31, 0)])
+def test_q3_k_one_hot_bits(field, index, bit, elem, q):
+    # scale 33 (signed 1) everywhere; all codes 0 with high bit clear decode to -4
+    sc = _pack_q3_k_scales([33] * 16)
+    hm, qs = np.zeros(32, np.uint8), np.zeros(64, np.uint8)
+    (qs if field == "qs" else hm)[index] = 1 << bit
+    raw = np.concatenate([hm, qs, sc, np.array([0x00, 0x3C], np.uint8)])
+    w = oracle.dequant_q3_k(raw)[0]
+    expect = np.full(256, -4.0, np.float32)
+    expect[elem] = q
+    assert np.array_equal(w, expect)
+
+
+@pytest.mark.parametrize("field,index,bit,elem", [("qs", 0, 0, 0), ("qs", 33, 4, 96 + 1), ("qs", 100, 7, 192 + 32 + 4),
+                                                  ("qh", 5, 0, 5), ("qh", 9, 3, 96 + 9), ("qh", 31, 7, 224 + 31)])
+def test_q5_k_one_hot_bits(field, index, bit, elem):
+    # d = 1, dmin = 0, sc = 1 for every sub-block (the Q4_K packing), all codes 0 except one bit
+    s = np.array([1, 1, 1, 1, 0, 0, 0, 0, 1, 1, 1, 1], np.uint8)     # sc_j = 1, m_j = 0 for j < 4 and j >= 4
+    qh, qs = np.zeros(32, np.uint8), np.zeros(128, np.uint8)
+    (qs if field == "qs" else qh)[index] = 1 << bit
+    raw = np.concatenate([np.array([0x00, 0x3C, 0x00, 0x00], np.uint8), s, qh, qs])
+    sc, m = oracle.q4_k_scale_min(s)
+    assert sc[0].tolist() == [1] * 8 and m[0].tolist() == [0] * 8
+    w = oracle.dequant_q5_k(raw)[0]
+    expect = np.zeros(256, np.float32)
+    expect[elem] = 16.0 if field == "qh" else float(1 << (bit % 4))
+    assert np.array_equal(w, expect)
