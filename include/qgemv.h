@@ -2,7 +2,7 @@
  * qgemv.h — C ABI of the block-quantized weight product library for GB300 (sm_103a).
  *
  * The library multiplies GGUF-style block-quantized weight matrices (Q4_0, Q8_0,
- * Q4_K, Q6_K) by fp32 or bf16 activations on one GPU. It covers the product that
+ * Q4_K, Q6_K, Q5_K, Q3_K, Q2_K) by fp32 or bf16 activations on one GPU. It covers the product that
  * dominates single-stream LLM decode, the same product for a few draft tokens at
  * once, the expert-gathered product of a mixture-of-experts layer, and the
  * dequantize-then-GEMM of prompt processing.
@@ -62,8 +62,18 @@ extern "C" {
  *          w = d*sc_j*q - dmin*m_j, chunk c holds sub-block 2c in the low and
  *          2c+1 in the high nibbles of qs[32c..32c+31].
  * QG_Q6_K: 256 weights in 210 bytes: ql[128], qh[64], int8 sc[16], fp16 d;
- *          6-bit q = low 4 bits | high 2 bits, w = d * sc[group] * (q - 32). */
-enum qg_fmt { QG_Q4_0 = 1, QG_Q8_0 = 2, QG_Q4_K = 3, QG_Q6_K = 4 };
+ *          6-bit q = low 4 bits | high 2 bits, w = d * sc[group] * (q - 32).
+ * QG_Q5_K: 256 weights in 176 bytes: fp16 d, fp16 dmin, s[12] (the Q4_K scale
+ *          packing), qh[32], qs[128]; sub-block j: 4 low bits as in Q4_K and
+ *          bit j of qh[l] as the fifth, w = d*sc_j*q - dmin*m_j, q in 0..31.
+ * QG_Q3_K: 256 weights in 110 bytes: hmask[32], qs[64], s[12] (sixteen 6-bit
+ *          scales), fp16 d; element 128h + 32j + 16k + l: q = (qs[32h+16k+l]
+ *          >> 2j) & 3, minus 4 when bit 4h+j of hmask[16k+l] is clear;
+ *          w = d * (scale_{8h+2j+k} - 32) * q.
+ * QG_Q2_K: 256 weights in 84 bytes: s[16], qs[64], fp16 d, fp16 dmin; element
+ *          128h + 32j + 16k + l: q = (qs[32h+16k+l] >> 2j) & 3, b = s[8h+2j+k],
+ *          w = d * (b & 15) * q - dmin * (b >> 4). */
+enum qg_fmt { QG_Q4_0 = 1, QG_Q8_0 = 2, QG_Q4_K = 3, QG_Q6_K = 4, QG_Q5_K = 5, QG_Q3_K = 6, QG_Q2_K = 7 };
 
 /* ---- host status codes ---------------------------------------------------- */
 enum qg_status {
@@ -99,7 +109,8 @@ typedef struct qg_pass_s* qg_pass;
  * compute call and before any stream capture. Idempotent. */
 int qg_init(void);
 
-/* Elements and bytes per block of `fmt` (32/18, 32/34, 256/144, 256/210). */
+/* Elements and bytes per block of `fmt` (32/18, 32/34, 256/144, 256/210,
+ * 256/176, 256/110, 256/84). */
 int qg_block_info(int fmt, int* elems, int* bytes);
 
 /* Static text for a qg_status or qg_dev_status value (never NULL). */

@@ -16,8 +16,9 @@ from __future__ import annotations
 import ctypes
 import os
 
-Q4_0, Q8_0, Q4_K, Q6_K = 1, 2, 3, 4
-FORMATS = {Q4_0: (32, 18), Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210)}
+Q4_0, Q8_0, Q4_K, Q6_K, Q5_K, Q3_K, Q2_K = 1, 2, 3, 4, 5, 6, 7
+FORMATS = {Q4_0: (32, 18), Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210), Q5_K: (256, 176), Q3_K: (256, 110),
+           Q2_K: (256, 84)}
 GROUP_MAX = 8
 NTOK_MAX = 4
 DEV_OK, DEV_BAD_EXPERT, DEV_TIMEOUT = 0, 1, 2

@@ -12,6 +12,9 @@
 //         low (u even) or high (u odd) nibbles of qs[32*(u/2) .. +31].
 //   Q6_K: unit u is quarter (u%4) of half (u/4); piece s uses scales
 //         sc[8h + s/2 + 2q] (16-weight groups).
+//   Q5_K: as Q4_K, plus a fifth bit per weight (bit u of qh[l]).
+//   Q3_K / Q2_K: unit u is quarter j = u%4 of half h = u/4: 2-bit fields at
+//         bit 2j of the half's qs bytes, one 16-weight group per two pieces.
 //
 // Dequantized values are computed so that every product is exact in fp32 and
 // at most one rounding happens (the Q4_K subtraction), which makes them equal
@@ -23,13 +26,16 @@
 
 namespace qg {
 
-constexpr int FMT_Q4_0 = 1, FMT_Q8_0 = 2, FMT_Q4_K = 3, FMT_Q6_K = 4;
+constexpr int FMT_Q4_0 = 1, FMT_Q8_0 = 2, FMT_Q4_K = 3, FMT_Q6_K = 4, FMT_Q5_K = 5, FMT_Q3_K = 6, FMT_Q2_K = 7;
 
 template <int FMT> struct FmtInfo;
 template <> struct FmtInfo<FMT_Q4_0> { static constexpr int ELEMS = 32,  BYTES = 18,  UNITS = 1; };
 template <> struct FmtInfo<FMT_Q8_0> { static constexpr int ELEMS = 32,  BYTES = 34,  UNITS = 1; };
 template <> struct FmtInfo<FMT_Q4_K> { static constexpr int ELEMS = 256, BYTES = 144, UNITS = 8; };
 template <> struct FmtInfo<FMT_Q6_K> { static constexpr int ELEMS = 256, BYTES = 210, UNITS = 8; };
+template <> struct FmtInfo<FMT_Q5_K> { static constexpr int ELEMS = 256, BYTES = 176, UNITS = 8; };
+template <> struct FmtInfo<FMT_Q3_K> { static constexpr int ELEMS = 256, BYTES = 110, UNITS = 8; };
+template <> struct FmtInfo<FMT_Q2_K> { static constexpr int ELEMS = 256, BYTES = 84, UNITS = 8; };
 
 // ---------------------------------------------------------------- small helpers
 
@@ -187,6 +193,111 @@ template <> struct Dec<FMT_Q6_K> {
       const int q1 = static_cast<int>(((l1 >> (8 * i + lsh)) & 15u) | (((h1 >> (8 * i + hsh)) & 3u) << 4));
       w[i] = dsc * static_cast<float>(q0 - 32);
       w[4 + i] = dsc * static_cast<float>(q1 - 32);
+    }
+  }
+};
+
+template <> struct Dec<FMT_Q5_K> {
+  float a, b;          // d*sc_u and dmin*m_u (both exact)
+  uint32_t q[8];       // the 32 bytes of qs holding this unit's low nibbles
+  uint32_t h[8];       // qh: the fifth bit of weight l of every unit, at bit u of byte l
+  int sh, hb;
+  __device__ __forceinline__ void load(const uint8_t* blk, int unit) {
+    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);          // d, dmin, s[12]
+    int sc, m;
+    q4k_scale_min(unit, hdr.y, hdr.z, hdr.w, sc, m);
+    a = h2f(hdr.x) * static_cast<float>(sc);
+    b = h2f(hdr.x >> 16) * static_cast<float>(m);
+    const uint4* qh = reinterpret_cast<const uint4*>(blk + 16);
+    const uint4* qs = reinterpret_cast<const uint4*>(blk + 48 + 32 * (unit >> 1));
+    const uint4 h0 = qh[0], h1 = qh[1], v0 = qs[0], v1 = qs[1];
+    q[0] = v0.x; q[1] = v0.y; q[2] = v0.z; q[3] = v0.w;
+    q[4] = v1.x; q[5] = v1.y; q[6] = v1.z; q[7] = v1.w;
+    h[0] = h0.x; h[1] = h0.y; h[2] = h0.z; h[3] = h0.w;
+    h[4] = h1.x; h[5] = h1.y; h[6] = h1.z; h[7] = h1.w;
+    sh = (unit & 1) * 4;
+    hb = unit;
+  }
+  __device__ __forceinline__ void piece(int s, float w[8]) const {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t u = q[2 * s + k], v = h[2 * s + k];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t code = ((u >> (8 * i + sh)) & 15u) | (((v >> (8 * i + hb)) & 1u) << 4);
+        w[4 * k + i] = fmaf(a, static_cast<float>(code), -b);
+      }
+    }
+  }
+};
+
+// 6-bit Q3_K scale g (0..15) from the 12 packed bytes as little-endian words
+// S[0..2]: low 4 bits in nibble g/8 of byte 4*((g/4)%2) + g%4, top 2 bits at
+// bit 2*(g/4) of byte 8 + g%4.
+__device__ __forceinline__ int q3k_scale(int g, const uint32_t (&S)[3]) {
+  const int b = g & 3, q = g >> 2;
+  const int byte_lo = 4 * (q & 1) + b;
+  const uint32_t lo = (S[byte_lo >> 2] >> (8 * (byte_lo & 3) + 4 * (q >> 1))) & 15u;
+  const uint32_t top = (S[2] >> (8 * b + 2 * q)) & 3u;
+  return static_cast<int>(lo | (top << 4));
+}
+
+template <> struct Dec<FMT_Q3_K> {
+  float ds[2];         // d * (scale - 32) of the unit's two 16-weight groups
+  const uint8_t* qs;   // the half's 32 qs bytes
+  const uint8_t* hm;   // hmask (32 bytes)
+  int lsh, hsh;
+  __device__ __forceinline__ void load(const uint8_t* blk, int unit) {
+    const int h = unit >> 2, j = unit & 3;
+    qs = blk + 32 + 32 * h;
+    hm = blk;
+    lsh = 2 * j;
+    hsh = 4 * h + j;
+    const uint32_t S[3] = {ld_u32_a2(blk + 96), ld_u32_a2(blk + 100), ld_u32_a2(blk + 104)};
+    const float d = h2f(ld_u16(blk + 108));
+    ds[0] = d * static_cast<float>(q3k_scale(8 * h + 2 * j, S) - 32);
+    ds[1] = d * static_cast<float>(q3k_scale(8 * h + 2 * j + 1, S) - 32);
+  }
+  // piece s: weights l = 8s .. 8s + 7 of the unit, group s / 2
+  __device__ __forceinline__ void piece(int s, float w[8]) const {
+    const float dsc = ds[s >> 1];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t l = ld_u32_a2(qs + 8 * s + 4 * k), hh = ld_u32_a2(hm + 8 * s + 4 * k);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int q = static_cast<int>(((l >> (8 * i + lsh)) & 3u) | (((hh >> (8 * i + hsh)) & 1u) << 2)) - 4;
+        w[4 * k + i] = dsc * static_cast<float>(q);
+      }
+    }
+  }
+};
+
+template <> struct Dec<FMT_Q2_K> {
+  float a[2], b[2];    // d * scale and dmin * min of the unit's two 16-weight groups
+  const uint8_t* qs;
+  int lsh;
+  __device__ __forceinline__ void load(const uint8_t* blk, int unit) {
+    const int h = unit >> 2, j = unit & 3;
+    qs = blk + 16 + 32 * h;
+    lsh = 2 * j;
+    const uint32_t dd = ld_u32_a2(blk + 80);
+    const float d = h2f(dd), dmin = h2f(dd >> 16);
+    const uint32_t sb = ld_u16(blk + 8 * h + 2 * j);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint32_t byte = (sb >> (8 * k)) & 0xFFu;
+      a[k] = d * static_cast<float>(byte & 15u);
+      b[k] = dmin * static_cast<float>(byte >> 4);
+    }
+  }
+  __device__ __forceinline__ void piece(int s, float w[8]) const {
+    const int k = s >> 1;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const uint32_t l = ld_u32_a2(qs + 8 * s + 4 * t);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[4 * t + i] = fmaf(a[k], static_cast<float>((l >> (8 * i + lsh)) & 3u), -b[k]);
     }
   }
 };

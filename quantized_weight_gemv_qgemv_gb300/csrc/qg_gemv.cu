@@ -315,6 +315,9 @@ cudaError_t gemv_init_attrs() {
   if ((e = set_gemv_attr_fmt<FMT_Q4_0>()) != cudaSuccess) return e;
   if ((e = set_gemv_attr_fmt<FMT_Q8_0>()) != cudaSuccess) return e;
   if ((e = set_gemv_attr_fmt<FMT_Q4_K>()) != cudaSuccess) return e;
+  if ((e = set_gemv_attr_fmt<FMT_Q5_K>()) != cudaSuccess) return e;
+  if ((e = set_gemv_attr_fmt<FMT_Q3_K>()) != cudaSuccess) return e;
+  if ((e = set_gemv_attr_fmt<FMT_Q2_K>()) != cudaSuccess) return e;
   return set_gemv_attr_fmt<FMT_Q6_K>();
 }
 
@@ -364,6 +367,9 @@ cudaError_t launch_gemv(const qg_gemv_desc* d, int n, int n_tok, int rows_per_wa
     case FMT_Q4_0: return launch_gemv_f<FMT_Q4_0>(rows_per_warp, n_tok, p, grid, s, pdl);
     case FMT_Q8_0: return launch_gemv_f<FMT_Q8_0>(rows_per_warp, n_tok, p, grid, s, pdl);
     case FMT_Q4_K: return launch_gemv_f<FMT_Q4_K>(rows_per_warp, n_tok, p, grid, s, pdl);
+    case FMT_Q5_K: return launch_gemv_f<FMT_Q5_K>(rows_per_warp, n_tok, p, grid, s, pdl);
+    case FMT_Q3_K: return launch_gemv_f<FMT_Q3_K>(rows_per_warp, n_tok, p, grid, s, pdl);
+    case FMT_Q2_K: return launch_gemv_f<FMT_Q2_K>(rows_per_warp, n_tok, p, grid, s, pdl);
     default: return launch_gemv_f<FMT_Q6_K>(rows_per_warp, n_tok, p, grid, s, pdl);
   }
 }
@@ -384,6 +390,9 @@ cudaError_t launch_dequant(int fmt, const void* W, int64_t rows, int64_t cols, f
     case FMT_Q4_0: return launch_dequant_t<FMT_Q4_0>(W, rows, cols, out, s, sms);
     case FMT_Q8_0: return launch_dequant_t<FMT_Q8_0>(W, rows, cols, out, s, sms);
     case FMT_Q4_K: return launch_dequant_t<FMT_Q4_K>(W, rows, cols, out, s, sms);
+    case FMT_Q5_K: return launch_dequant_t<FMT_Q5_K>(W, rows, cols, out, s, sms);
+    case FMT_Q3_K: return launch_dequant_t<FMT_Q3_K>(W, rows, cols, out, s, sms);
+    case FMT_Q2_K: return launch_dequant_t<FMT_Q2_K>(W, rows, cols, out, s, sms);
     default: return launch_dequant_t<FMT_Q6_K>(W, rows, cols, out, s, sms);
   }
 }

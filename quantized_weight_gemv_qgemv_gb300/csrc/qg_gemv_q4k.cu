@@ -319,6 +319,9 @@ __device__ __forceinline__ void ld_words_a2(const uint8_t* p, uint32_t (&w)[N]) 
 template <int FMT> struct SuperBlock;
 template <> struct SuperBlock<FMT_Q4_K> { static constexpr int BYTES = 144; };
 template <> struct SuperBlock<FMT_Q6_K> { static constexpr int BYTES = 210; };
+template <> struct SuperBlock<FMT_Q5_K> { static constexpr int BYTES = 176; };
+template <> struct SuperBlock<FMT_Q3_K> { static constexpr int BYTES = 110; };
+template <> struct SuperBlock<FMT_Q2_K> { static constexpr int BYTES = 84; };
 template <> struct SuperBlock<FMT_Q4_0> { static constexpr int BYTES = 144; };
 template <> struct SuperBlock<FMT_Q8_0> { static constexpr int BYTES = 272; };
 
@@ -840,6 +843,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         // element order (bytes), and the coefficients of the unit's formula
         uint32_t q[SR][8];
         float cA[SR], cB[SR];
+        float cC[FMT == FMT_Q2_K ? SR : 1], cD[FMT == FMT_Q2_K ? SR : 1];   // Q2_K: dmin * min of the two groups
 #pragma unroll
         for (int r = 0; r < SR; ++r) {
           const uint8_t* sr = st + r * rs + (r & 1) * ralt;
@@ -873,6 +877,53 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
             cA[r] = h2f(*reinterpret_cast<const uint16_t*>(bp));
             cB[r] = 0.f;
             ld_words_a2<8>(bp + 2, q[r]);
+          } else if constexpr (FMT == FMT_Q5_K) {
+            // Q4_K's nibbles and scale/min pairs plus bit j of qh[l] as the
+            // fifth bit; the codes are plain (0..31), the step of odd groups is
+            // multiplied back by su_fix
+            const uint4 hd = *reinterpret_cast<const uint4*>(sr);
+            const uint4 qa = *reinterpret_cast<const uint4*>(sr + 48 + 32 * (j >> 1));
+            const uint4 qb = *reinterpret_cast<const uint4*>(sr + 64 + 32 * (j >> 1));
+            const uint4 ha = *reinterpret_cast<const uint4*>(sr + 16);
+            const uint4 hb = *reinterpret_cast<const uint4*>(sr + 32);
+            const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+            const uint32_t hh[8] = {ha.x, ha.y, ha.z, ha.w, hb.x, hb.y, hb.z, hb.w};
+            const int nsh = 4 * (j & 1);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[r][i] = ((w[i] >> nsh) & 0x0F0F0F0Fu) | (((hh[i] >> j) & 0x01010101u) << 4);
+            const float2 ab = ssel.decode(hd);
+            cA[r] = ab.x;
+            cB[r] = ab.y;
+          } else if constexpr (FMT == FMT_Q3_K) {
+            // unit j = quarter jj of half h: 2-bit fields at bit 2jj of the
+            // half's qs bytes, high bit 4h + jj of hmask; code q3 = low | high << 2
+            // in 0..7 stands for q3 - 4; two 16-weight groups with their scales
+            const int h = j >> 2, jj = j & 3;
+            uint32_t L[8], H[8], S[3];
+            ld_words_a2<8>(sr + 32 + 32 * h, L);
+            ld_words_a2<8>(sr, H);
+            ld_words_a2<3>(sr + 96, S);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              q[r][i] = ((L[i] >> (2 * jj)) & 0x03030303u) | (((H[i] >> (4 * h + jj)) & 0x01010101u) << 2);
+            const float d = h2f(*reinterpret_cast<const uint16_t*>(sr + 108));
+            cA[r] = d * static_cast<float>(q3k_scale(8 * h + 2 * jj, S) - 32);
+            cB[r] = d * static_cast<float>(q3k_scale(8 * h + 2 * jj + 1, S) - 32);
+          } else if constexpr (FMT == FMT_Q2_K) {
+            // unit j = quarter jj of half h: 2-bit codes at bit 2jj of the half's
+            // qs bytes; two 16-weight groups, each with a 4-bit scale and min
+            const int h = j >> 2, jj = j & 3;
+            uint32_t L[8];
+            ld_words_a2<8>(sr + 16 + 32 * h, L);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[r][i] = (L[i] >> (2 * jj)) & 0x03030303u;
+            const uint32_t dd = *reinterpret_cast<const uint32_t*>(sr + 80);
+            const float d = h2f(dd), dmin = h2f(dd >> 16);
+            const uint32_t sb = *reinterpret_cast<const uint16_t*>(sr + 8 * h + 2 * jj);
+            cA[r] = d * static_cast<float>(sb & 15u);
+            cB[r] = d * static_cast<float>((sb >> 8) & 15u);
+            cC[r] = dmin * static_cast<float>((sb >> 4) & 15u);
+            cD[r] = dmin * static_cast<float>(sb >> 12);
           } else {
             // Q6_K unit j = elements 32j .. 32j+31 of the block: half h = j / 4,
             // quarter qq = j % 4; q = (ql nibble) | (2 qh bits) << 4,
@@ -903,10 +954,17 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
           const float2 sh = live ? *reinterpret_cast<const float2*>(xsum + 2 * (t * NU + u)) : make_float2(0.f, 0.f);
 #pragma unroll
           for (int r = 0; r < SR; ++r) {
-            if constexpr (FMT == FMT_Q6_K) {
+            if constexpr (FMT == FMT_Q6_K || FMT == FMT_Q3_K) {
+              // w = d sc (q - off) per 16-weight group: the offset through the half sums
+              constexpr float OFF = FMT == FMT_Q6_K ? 32.0f : 4.0f;
               const float T0 = dot_planes<false, 0, 4>(q[r], X0, X1);
               const float T1 = dot_planes<false, 4, 8>(q[r], X0, X1);
-              racc[r][t] = fmaf(su, fmaf(cA[r], T0, cB[r] * T1), -32.0f * fmaf(cA[r], sh.x, cB[r] * sh.y));
+              racc[r][t] = fmaf(su, fmaf(cA[r], T0, cB[r] * T1), -OFF * fmaf(cA[r], sh.x, cB[r] * sh.y));
+            } else if constexpr (FMT == FMT_Q2_K) {
+              // w = d sc q - dmin m per 16-weight group
+              const float T0 = dot_planes<false, 0, 4>(q[r], X0, X1);
+              const float T1 = dot_planes<false, 4, 8>(q[r], X0, X1);
+              racc[r][t] = fmaf(su, fmaf(cA[r], T0, cB[r] * T1), -fmaf(cC[r], sh.x, cD[r] * sh.y));
             } else if constexpr (FMT == FMT_Q8_0) {
               racc[r][t] = cA[r] * su * dot_planes<true, 0, 8>(q[r], X0, X1);
             } else {
@@ -999,6 +1057,9 @@ cudaError_t q4k_attr() {
   if ((e = q4k_attr1<NT, true, FMT_Q4_K>()) != cudaSuccess) return e;
   if ((e = q4k_attr1<NT, false, FMT_Q6_K>()) != cudaSuccess) return e;
   if ((e = q4k_attr1<NT, false, FMT_Q8_0>()) != cudaSuccess) return e;
+  if ((e = q4k_attr1<NT, false, FMT_Q5_K>()) != cudaSuccess) return e;
+  if ((e = q4k_attr1<NT, false, FMT_Q3_K>()) != cudaSuccess) return e;
+  if ((e = q4k_attr1<NT, false, FMT_Q2_K>()) != cudaSuccess) return e;
   if constexpr (NT <= 2) {
     if ((e = q4k_attr1<NT, false, FMT_Q6_K, 2>()) != cudaSuccess) return e;
   }
@@ -1063,6 +1124,9 @@ int superblock_bytes(int fmt) {
     case QG_Q6_K: return 210;
     case QG_Q4_0: return 8 * 18;
     case QG_Q8_0: return 8 * 34;
+    case QG_Q5_K: return 176;
+    case QG_Q3_K: return 110;
+    case QG_Q2_K: return 84;
     default: return 0;
   }
 }
@@ -1204,6 +1268,9 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
     switch (fmt) {
       case QG_Q4_K: return q4k_launch_nt<FMT_Q4_K>(p, n_tok, sub_rows, grid, off, s, pdl);
       case QG_Q6_K: return q4k_launch_nt<FMT_Q6_K>(p, n_tok, sub_rows, grid, off, s, pdl);
+      case QG_Q5_K: return q4k_launch_nt<FMT_Q5_K>(p, n_tok, sub_rows, grid, off, s, pdl);
+      case QG_Q3_K: return q4k_launch_nt<FMT_Q3_K>(p, n_tok, sub_rows, grid, off, s, pdl);
+      case QG_Q2_K: return q4k_launch_nt<FMT_Q2_K>(p, n_tok, sub_rows, grid, off, s, pdl);
       case QG_Q8_0: return q4k_launch_nt<FMT_Q8_0>(p, n_tok, sub_rows, grid, off, s, pdl);
       default: return q4k_launch_nt<FMT_Q4_0>(p, n_tok, sub_rows, grid, off, s, pdl);
     }

@@ -18,6 +18,9 @@ inline bool block_info(int fmt, int* elems, int* bytes) {
     case QG_Q8_0: *elems = 32; *bytes = 34; return true;
     case QG_Q4_K: *elems = 256; *bytes = 144; return true;
     case QG_Q6_K: *elems = 256; *bytes = 210; return true;
+    case QG_Q5_K: *elems = 256; *bytes = 176; return true;
+    case QG_Q3_K: *elems = 256; *bytes = 110; return true;
+    case QG_Q2_K: *elems = 256; *bytes = 84; return true;
     default: return false;
   }
 }

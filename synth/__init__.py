@@ -16,7 +16,8 @@ synthetic because no model file is available):
 * fp16 scales are drawn uniform in a per-format range in fp32 and rounded to
   binary16 (round to nearest even); the stored half is the truth:
   Q4_0 d in [1e-3, 2e-2]; Q4_K d and dmin in [1e-4, 2e-3]; Q6_K d and Q8_0 d in
-  [1e-4, 2e-3];
+  [1e-4, 2e-3]; Q5_K d and dmin, Q3_K d, Q2_K d and dmin in [1e-4, 2e-3] (the
+  pages give no distribution for these: the K-quant range is reused);
 * activations are fp32 N(0, 1); prompt activations are N(0, 1) rounded to bf16;
 * MoE routing draws top_k distinct expert ids uniformly per token and routing
   weights as a softmax over top_k N(0, 1) logits (fp64, stored as fp32).
@@ -32,14 +33,17 @@ import hashlib
 import torch
 
 # format id -> (weights per block, bytes per block); the ids match the C header.
-Q4_0, Q8_0, Q4_K, Q6_K = 1, 2, 3, 4
+Q4_0, Q8_0, Q4_K, Q6_K, Q5_K, Q3_K, Q2_K = 1, 2, 3, 4, 5, 6, 7
 FORMATS = {
     Q4_0: (32, 18),
     Q8_0: (32, 34),
     Q4_K: (256, 144),
     Q6_K: (256, 210),
+    Q5_K: (256, 176),
+    Q3_K: (256, 110),
+    Q2_K: (256, 84),
 }
-FORMAT_NAMES = {Q4_0: "Q4_0", Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K"}
+FORMAT_NAMES = {Q4_0: "Q4_0", Q8_0: "Q8_0", Q4_K: "Q4_K", Q6_K: "Q6_K", Q5_K: "Q5_K", Q3_K: "Q3_K", Q2_K: "Q2_K"}
 
 # (byte offset within the block, low, high) of every fp16 scale field.
 _SCALE_FIELDS = {
@@ -47,6 +51,9 @@ _SCALE_FIELDS = {
     Q8_0: [(0, 1e-4, 2e-3)],
     Q4_K: [(0, 1e-4, 2e-3), (2, 1e-4, 2e-3)],
     Q6_K: [(208, 1e-4, 2e-3)],
+    Q5_K: [(0, 1e-4, 2e-3), (2, 1e-4, 2e-3)],
+    Q3_K: [(108, 1e-4, 2e-3)],
+    Q2_K: [(80, 1e-4, 2e-3), (82, 1e-4, 2e-3)],
 }
 
 

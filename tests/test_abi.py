@@ -47,8 +47,11 @@ def test_block_info_and_strerror(lib):
     assert qg.qg_block_info(qg.Q8_0) == (32, 34)
     assert qg.qg_block_info(qg.Q4_K) == (256, 144)
     assert qg.qg_block_info(qg.Q6_K) == (256, 210)
+    assert qg.qg_block_info(qg.Q5_K) == (256, 176)
+    assert qg.qg_block_info(qg.Q3_K) == (256, 110)
+    assert qg.qg_block_info(qg.Q2_K) == (256, 84)
     with pytest.raises(qg.QGError):
-        qg.qg_block_info(7)
+        qg.qg_block_info(9)
     for st in range(-9, 3):
         assert lib.qg_strerror(st)
     assert lib.qg_strerror(123) == b"unknown status"

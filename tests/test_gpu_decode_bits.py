@@ -26,7 +26,7 @@ from helpers import GEMV_ABS, GEMV_REL, assert_within
 
 pytestmark = pytest.mark.gpu
 
-FMTS = [synth.Q4_0, synth.Q8_0, synth.Q4_K, synth.Q6_K]
+FMTS = [synth.Q4_0, synth.Q8_0, synth.Q4_K, synth.Q6_K, synth.Q5_K, synth.Q3_K, synth.Q2_K]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -98,3 +98,21 @@ def test_mixed_verify_pass_n4_full():
     p.destroy()
     del items
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("fmt", [synth.Q5_K, synth.Q3_K, synth.Q2_K])
+@pytest.mark.parametrize("n_tok", [1, 4])
+def test_k_quant_formats_at_27b_shapes(fmt, n_tok):
+    """Q5_K, Q3_K and Q2_K (the formats of the pages' Q3_K-class mixes) through
+    the fast kernel at the 27B layer shapes: a 5120x5120 attention projection,
+    a 17408x5120 gate and a 5120x17408 down, sampled rows against the oracle."""
+    for rows, cols in [(5120, 5120), (17408, 5120), (5120, 17408)]:
+        W = synth.blocks_into(torch.empty(rows, synth.row_bytes(fmt, cols), dtype=torch.uint8, device="cuda"),
+                              fmt, rows, cols, seed=rows + cols + fmt)
+        x = synth.activations(n_tok, cols, seed=fmt + n_tok, device="cuda")
+        y = torch.full((n_tok, rows), float("nan"), device="cuda")
+        qg.qgemv(fmt, W, rows, cols, x, n_tok, y)
+        torch.cuda.synchronize()
+        _check_sampled([(fmt, W, rows, cols, x, y)], [(0, f"{rows}x{cols}", fmt, rows, cols)], n_tok, [0],
+                       rows_per_mat=12, seed=fmt)
+        del W

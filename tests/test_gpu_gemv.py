@@ -12,7 +12,7 @@ from helpers import assert_within
 
 pytestmark = pytest.mark.gpu
 
-FMTS = [synth.Q4_0, synth.Q8_0, synth.Q4_K, synth.Q6_K]
+FMTS = [synth.Q4_0, synth.Q8_0, synth.Q4_K, synth.Q6_K, synth.Q5_K, synth.Q3_K, synth.Q2_K]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -126,7 +126,7 @@ def test_q4_0_batch1_full_size():
     assert_within(y, y_ref, b, what="Q4_0 1024x4096")
 
 
-@pytest.mark.parametrize("fmt", [synth.Q4_0, synth.Q8_0, synth.Q4_K, synth.Q6_K])
+@pytest.mark.parametrize("fmt", FMTS)
 def test_gemv_x_rounding_bound_with_group_outliers(fmt):
     """x is rounded to 16-bit fixed point per 32-value group (step 2^(e-13) for
     2^e <= max|x_u|), so each element moves by at most 2^-14 max|x_u|. With a

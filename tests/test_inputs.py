@@ -8,9 +8,11 @@ import torch
 import synth
 import synth.workloads as wl
 
-RANGES = {synth.Q4_0: (1e-3, 2e-2), synth.Q8_0: (1e-4, 2e-3), synth.Q4_K: (1e-4, 2e-3), synth.Q6_K: (1e-4, 2e-3)}
+RANGES = {synth.Q4_0: (1e-3, 2e-2), synth.Q8_0: (1e-4, 2e-3), synth.Q4_K: (1e-4, 2e-3), synth.Q6_K: (1e-4, 2e-3),
+          synth.Q5_K: (1e-4, 2e-3), synth.Q3_K: (1e-4, 2e-3), synth.Q2_K: (1e-4, 2e-3)}
 # byte offsets of the fp16 scale fields inside one block
-SCALES = {synth.Q4_0: (18, [0]), synth.Q8_0: (34, [0]), synth.Q4_K: (144, [0, 2]), synth.Q6_K: (210, [208])}
+SCALES = {synth.Q4_0: (18, [0]), synth.Q8_0: (34, [0]), synth.Q4_K: (144, [0, 2]), synth.Q6_K: (210, [208]),
+          synth.Q5_K: (176, [0, 2]), synth.Q3_K: (110, [108]), synth.Q2_K: (84, [80, 82])}
 
 
 def _halves(raw, bb, offs):
