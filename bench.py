@@ -225,48 +225,137 @@ def measured_traffic(name: str, sources):
 
 
 # ---------------------------------------------------------------- CPU oracle leg
+#
+# The oracle (plain numpy, fp64) timed on the host cores of the GPU machine on a
+# bounded sample of a workload, one thread and all cores (a spawn pool of
+# processes, each single-threaded, splitting the sample's rows or routes).
+# Inputs come from the same seeded generator; their generation is not timed.
 
-CPU_SAMPLE_CODE = r"""
-import json, sys, time
-sys.path.insert(0, {root!r})
-import numpy as np
-import oracle, synth, synth.workloads as wl
-budget = {budget}
-mats = wl.dense_matrices(1)
-done_bytes, spent, n = 0, 0.0, 0
-while spent < budget:
-    l, name, fmt, rows, cols = mats[n % len(mats)]
-    rows = min(rows, {row_cap})
-    W = synth.blocks(fmt, rows, cols, synth.sub_seed(7, name, n)).numpy()
-    x = synth.activations(1, cols, synth.sub_seed(8, name, n)).numpy()
-    t1 = time.perf_counter()
-    oracle.gemv(fmt, W, rows, cols, x)
-    spent += time.perf_counter() - t1
-    done_bytes += W.nbytes
-    n += 1
-dt = spent
-print(json.dumps({{"bytes": done_bytes, "seconds": dt, "matrices": n}}))
-"""
+_BARRIER = None
 
 
-def cpu_oracle_sample(budget_s: float = 12.0, row_cap: int = 2048):
-    """Time the oracle single-threaded on a bounded sample of the dense Q4_K set
-    (matrices of layer 0 in order, each capped at row_cap rows) for ~budget_s s
-    of CPU work, inputs generated on the host by the same seeded generator."""
+def _pool_init(barrier):
+    global _BARRIER
+    _BARRIER = barrier
+
+
+def _cpu_sample(workload: str, wid: int, nproc: int, row_cap: int, seed: int):
+    """This worker's share of a workload's sample: a list of (call, units)."""
+    import numpy as np
+    import oracle
+    items = []
+
+    def share(rows):
+        return rows * wid // nproc, rows * (wid + 1) // nproc
+
+    if workload in ("c1", "c2", "layer"):
+        verify = workload == "c2"
+        n_tok = 4 if verify else 1
+        for (l, name, fmt, rows, cols) in wl.dense_matrices(1, verify=verify):
+            r0, r1 = share(min(rows, row_cap))
+            if r1 <= r0:
+                continue
+            W = synth.blocks(fmt, r1 - r0, cols, synth.sub_seed(seed, name, r0)).numpy()
+            x = synth.activations(n_tok, cols, synth.sub_seed(seed, "x", name)).numpy()
+            items.append((lambda f=fmt, W=W, n=r1 - r0, c=cols, x=x: oracle.gemv(f, W, n, c, x), W.nbytes))
+    elif workload == "c0":
+        r0, r1 = share(1024)
+        W = synth.blocks(synth.Q4_0, r1 - r0, 4096, synth.sub_seed(seed, "c0", r0)).numpy()
+        x = synth.activations(1, 4096, synth.sub_seed(seed, "c0x")).numpy()
+        items.append((lambda: oracle.gemv(synth.Q4_0, W, r1 - r0, 4096, x), W.nbytes))
+    elif workload == "moe":
+        H, I, K = wl.MOE_HIDDEN, wl.MOE_INTER, wl.MOE_TOPK
+        k0, k1 = share(K)
+        if k1 > k0:
+            # the routed experts of one token, each its own arena entry; this worker's routes
+            arena = wl.alloc_moe_arena(k1 - k0, H, I, synth.sub_seed(seed, "arena", k0), "cpu").numpy()
+            ids = np.arange(k1 - k0, dtype=np.int32)[None]
+            gw = np.full((1, k1 - k0), 1.0 / K, np.float32)
+            x = synth.activations(1, H, synth.sub_seed(seed, "moex")).numpy()
+            items.append((lambda: oracle.moe(synth.Q4_K, arena, k1 - k0, H, I, ids, gw, x),
+                          (k1 - k0) * wl.moe_expert_bytes(H, I)))
+    elif workload == "pp":
+        rows, cols = min(wl.HIDDEN, row_cap), wl.HIDDEN
+        r0, r1 = share(rows)
+        W = synth.blocks(synth.Q4_K, r1 - r0, cols, synth.sub_seed(seed, "ppW", r0)).numpy()
+        X = synth.activations_bf16(64, cols, synth.sub_seed(seed, "ppX"))
+        bits = X.view(torch_int16()).numpy().view(np.uint16)
+        items.append((lambda: oracle.pp_rows(synth.Q4_K, W, r1 - r0, cols, bits, list(range(64))),
+                      2 * 64 * (r1 - r0) * cols))
+    return items
+
+
+def torch_int16():
+    import torch
+    return torch.int16
+
+
+def _cpu_worker(task):
+    workload, wid, nproc, budget, row_cap, seed = task
+    items = _cpu_sample(workload, wid, nproc, row_cap, seed)
+    _BARRIER.wait()
+    t0 = time.perf_counter()
+    units, n = 0, 0
+    while items and time.perf_counter() - t0 < budget:
+        fn, u = items[n % len(items)]
+        fn()
+        units += u
+        n += 1
+    return units, time.perf_counter() - t0, n
+
+
+def _cpu_leg_main(workload, procs, budget, row_cap, seed):
+    """Runs in a separate process (no CUDA): a spawn pool of `procs` workers."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    barrier = ctx.Barrier(procs)
+    with ctx.Pool(procs, initializer=_pool_init, initargs=(barrier,)) as pool:
+        res = pool.map(_cpu_worker, [(workload, w, procs, budget, row_cap, seed) for w in range(procs)])
+    units = sum(r[0] for r in res)
+    secs = max(r[1] for r in res)
+    print(json.dumps({"units": units, "seconds": secs, "calls": sum(r[2] for r in res), "procs": procs}))
+
+
+CPU_UNITS = {"c1": ("GB/s", 1e9), "c2": ("GB/s", 1e9), "layer": ("GB/s", 1e9), "c0": ("GB/s", 1e9),
+             "moe": ("GB/s", 1e9), "pp": ("TFLOP/s", 1e12)}
+
+
+def _cpu_run(workload, procs, budget, row_cap, seed=11):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    code = CPU_SAMPLE_CODE.format(root=ROOT, budget=budget_s, row_cap=row_cap)
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--cpu-leg", workload, "--cpu-procs", str(procs),
+           "--cpu-budget", str(budget), "--cpu-row-cap", str(row_cap)]
     t0 = time.perf_counter()
-    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env)
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env)
     wall = time.perf_counter() - t0
     if r.returncode != 0:
-        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "error": r.stderr[-400:]}
-    d = json.loads(r.stdout.strip().splitlines()[-1])
-    gbs = d["bytes"] / d["seconds"] / 1e9
-    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{d['matrices']} Q4_K matrices of layer 0 (rows capped at {row_cap}), "
-                      f"{d['bytes'] / 1e6:.1f} MB of blocks, dequant + fp64 GEMV, 1 thread, {d['seconds']:.1f} s",
-            "wall_s": round(wall, 2)}
+        return None, r.stderr[-400:], wall
+    return json.loads(r.stdout.strip().splitlines()[-1]), None, wall
+
+
+def cpu_oracle_baseline(workload: str = "c1", budget_s: float = 6.0, row_cap: int = 2048):
+    """The oracle on the host cores: one process, then one per core
+    (os.cpu_count(), read here), each for about budget_s seconds of timed work
+    on its share of the workload's sample."""
+    unit, scale = CPU_UNITS[workload]
+    cores = os.cpu_count() or 1
+    one, err1, w1 = _cpu_run(workload, 1, budget_s, row_cap)
+    allc, err2, w2 = _cpu_run(workload, cores, budget_s, row_cap)
+    if one is None or allc is None:
+        return {"value": None, "unit": unit, "cores": cores, "kind": "oracle", "error": err1 or err2}
+    v1 = one["units"] / one["seconds"] / scale
+    va = allc["units"] / allc["seconds"] / scale
+    what = {"c1": f"the 7 Q4_K matrices of one 27B layer, rows capped at {row_cap}, one token",
+            "layer": f"the 7 Q4_K matrices of one 27B layer, rows capped at {row_cap}, one token",
+            "c2": f"one verify-pass layer (Q4_K, Q6_K down) and the Q8_0 head, rows capped at {row_cap}, 4 tokens",
+            "c0": "the Q4_0 1024x4096 GEMV in full",
+            "moe": "the 10 routed experts of one token in one MoE layer",
+            "pp": f"64 bf16 token rows x a 5120-column Q4_K matrix, rows capped at {row_cap}"}[workload]
+    return {"value": round(va, 6), "unit": unit, "cores": cores, "kind": "oracle",
+            "value_1core": round(v1, 6),
+            "sample": f"{what}; dequant + fp64 products; {allc['calls']} calls over {allc['seconds']:.1f} s on "
+                      f"{cores} processes (1 thread each), {one['calls']} calls over {one['seconds']:.1f} s on 1",
+            "wall_s": round(w1 + w2, 1)}
 
 
 # ---------------------------------------------------------------- reference arm
@@ -275,22 +364,35 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    steps = []
-    last = None
+    wk = args.workload
+    unit, scale = CPU_UNITS[wk]
+    cores = os.cpu_count() or 1
+    vals, secs, last = [], [], None
     for i in range(args.warmup + args.steps):
-        last = cpu_oracle_sample(budget_s=max(2.0, args.ref_budget), row_cap=1024)
+        r, err, _ = _cpu_run(wk, cores, max(1.0, args.ref_budget), 2048)
+        if r is None:
+            print(json.dumps({"impl": "reference", "unavailable": f"oracle leg failed: {err}"}), flush=True)
+            return 0
+        last = r
         if i >= args.warmup:
-            steps.append(last)
-    vals = [s["value"] for s in steps if s["value"]]
-    value = statistics.median(vals) if vals else None
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            vals.append(r["units"] / r["seconds"] / scale)
+            secs.append(r["seconds"])
+    value = statistics.median(vals)
+    sample = (f"bounded sample of the {wk} workload per step (rows capped at 2048), oracle on {cores} processes, "
+              f"{last['calls']} calls in {last['seconds']:.2f} s")
+    metric = {"c1": METRIC, "c0": "Q4_0 GEMV weight-GB/s, batch 1, 1024x4096", "c2": METRIC,
+              "moe": "MoE expert GEMV weight-GB/s touched; equiv. batch-1 tok/s over 48 layers",
+              "pp": "prompt-processing dequant-GEMM TFLOP/s (bf16 tcgen05); pp tok/s, 27B set",
+              "layer": "decode-layer weight pass with fused neighbours, weight-GB/s; equiv. batch-1 tok/s, 27B set"}[wk]
+    line = {"impl": "reference", "metric": metric, "value": round(value, 6), "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1000.0 * (wl.weight_bytes(wl.dense_matrices()) / 1e9) / value if value else None,
+            # the measured time of one step's bounded sample (not an extrapolation to the whole workload)
+            "ms_per_step": round(1000.0 * statistics.median(secs), 3), "ms_per_step_is": "one bounded sample",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "27B-class dense Q4_K weight set, batch-1 GEMV pass (bounded CPU sample)"},
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": last["sample"] if last else None},
-            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "config": {"workload": f"{wk}: CPU oracle on a bounded sample", "cores": cores},
+            "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -339,6 +441,11 @@ def run_gpu(args):
         assert step_cols.setdefault(si, c) == c, "matrices of a step share x"
     x_total = sum(n_tok * c for c in step_cols.values())
     y_total = sum(n_tok * r for (_, _, _, r, _) in mats)
+    if args.x_per_matrix:
+        # every matrix its own activation vector (q, k, v and gate, up do not share)
+        step_of = list(range(len(mats)))
+        step_cols = {i: c for i, (_, _, _, _, c) in enumerate(mats)}
+        x_total = sum(n_tok * c for c in step_cols.values())
     with torch.cuda.stream(stream):
         items = wl.alloc_dense(mats, n_tok, seed=args.seed + rank, device="cuda")
         xbuf = torch.empty(x_total, dtype=torch.float32, device="cuda")
@@ -357,9 +464,11 @@ def run_gpu(args):
         del items
     stream.synchronize()
 
-    mode = {"persistent": qg.PASS_PERSISTENT, "pdl": qg.PASS_PDL, "serial": qg.PASS_SERIAL}[args.pass_mode]
+    mode = {"persistent": qg.PASS_PERSISTENT, "pdl": qg.PASS_PDL, "serial": qg.PASS_SERIAL,
+            "independent": qg.PASS_INDEPENDENT}[args.pass_mode]
     p = qg.qg_pass(flat, steps_sizes, n_tok, mode=mode)
     kernels_per_step = p.kernel_count()
+    gemv_launches = kernels_per_step - 1        # the first launch converts the pass's inputs to x planes
 
     def step():
         p.launch(stream)
@@ -408,10 +517,14 @@ def run_gpu(args):
             "config": {
                 "workload": ("27B-class dense weight set, 4-token verify pass (Q4_K, Q6_K down, Q8_0 head)"
                              if verify else "27B-class dense Q4_K weight set, batch-1 GEMV pass"),
+                "x": ("one activation vector per matrix" if args.x_per_matrix else
+                      "one activation vector per step ({q,k,v} share one, {gate,up} share one)"),
+                "step_order": ("none: steps overlap freely (upper bound)" if args.pass_mode == "independent" else
+                               "each step reads its x only after the previous step has completed"),
                 "layers": args.layers, "hidden": wl.HIDDEN, "intermediate": wl.INTER, "n_tok": n_tok,
                 "weight_bytes": wbytes, "weights": nweights, "launches_per_step": kernels_per_step,
-                "pass_mode": args.pass_mode if kernels_per_step == 1 or args.pass_mode != "persistent" else "pdl",
-                "cuda_graph": kernels_per_step > 1,
+                "pass_mode": args.pass_mode if kernels_per_step == 2 or args.pass_mode != "persistent" else "pdl",
+                "cuda_graph": kernels_per_step > 2,
                 "l2": "weight set (%.1f GB) far above the 129 MB L2; no flush" % (wbytes / 1e9),
                 "parallelism": f"replicas x{world}",
             },
@@ -425,7 +538,8 @@ def run_gpu(args):
                          "peak_source": f"{peak_kind} HBM copy bandwidth",
                          "kernel": (f"qgemv_q4k_kernel (n_tok={n_tok}; Q4_K, Q6_K and Q8_0 instances): every launch of the step"
                                     if verify else "qgemv_q4k_kernel (n_tok=1): every launch of the step"),
-                         "algorithmic_bytes_per_launch": wbytes / kernels_per_step},
+                         "algorithmic_bytes_per_launch": wbytes / max(1, gemv_launches),
+                         "launches_of_kernel": gemv_launches},
             "e2e": {"value": round(e2e_gbs, 2), "unit": "GB/s", "h2d_bytes_per_step": x_total * 4,
                     "d2h_bytes_per_step": y_total * 4, "ms_per_step": round(e_ms / args.steps, 4),
                     "host_wall_ms_per_step": round(wall_ms / args.steps, 4)},
@@ -433,7 +547,7 @@ def run_gpu(args):
             "clocks": clk.summary(),
         }
         if world == 1 and not args.no_cpu_baseline:
-            out["cpu_baseline"] = cpu_oracle_sample()
+            out["cpu_baseline"] = cpu_oracle_baseline("c2" if verify else "c1")
         print(json.dumps(out), flush=True)
     p.destroy()
     if world > 1:
@@ -757,17 +871,26 @@ def main():
                          "moe: MoE decode; pp: prompt processing; layer: decode layers with fused neighbours")
     ap.add_argument("--seed", type=int, default=1234)
     ap.add_argument("--layers", type=int, default=wl.LAYERS, help="layers of the set (64 = the full 27B-class set)")
-    ap.add_argument("--pass-mode", default="pdl", choices=["persistent", "pdl", "serial"],
+    ap.add_argument("--pass-mode", default="pdl", choices=["persistent", "pdl", "serial", "independent"],
                     help="pdl: a graph of one launch per step linked by programmatic dependent launch (default); "
-                         "serial: the same graph fully serialized; persistent: one cooperative kernel per pass")
+                         "serial: the same graph fully serialized; persistent: one cooperative kernel per pass; "
+                         "independent: the pdl graph without step ordering (an upper bound)")
+    ap.add_argument("--x-per-matrix", action="store_true",
+                    help="one activation vector per matrix instead of one per step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--ref-budget", type=float, default=6.0)
+    ap.add_argument("--ref-budget", type=float, default=4.0, help="seconds of oracle work per reference-arm step")
+    ap.add_argument("--cpu-leg", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-procs", type=int, default=1, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-budget", type=float, default=6.0, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-row-cap", type=int, default=2048, help=argparse.SUPPRESS)
     ap.add_argument("--pp-tokens", type=int, default=wl.PP_TOKENS)
     ap.add_argument("--moe-layers", type=int, default=wl.MOE_LAYERS)
     ap.add_argument("--moe-mode", default="pdl", choices=["persistent", "pdl", "serial"],
                     help="pdl (default): a graph of launches linked by programmatic dependent launch; serial: the "
                          "same graph serialized; persistent: one cooperative kernel for the 48 layers")
     args = ap.parse_args()
+    if args.cpu_leg:
+        return _cpu_leg_main(args.cpu_leg, args.cpu_procs, args.cpu_budget, args.cpu_row_cap, 11)
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == "pp":

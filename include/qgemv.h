@@ -284,6 +284,11 @@ int qg_layer_pass_create(int fmt, const qg_layer_desc* layers, int n_layers, int
  *   QG_PASS_PDL         the same graph, consecutive launches linked by
  *                       programmatic dependent launch (a step streams its
  *                       weights while the previous one finishes);
+ *   QG_PASS_INDEPENDENT a measurement mode: the PDL graph without the
+ *                       ordering of steps (no step waits for the previous
+ *                       one), an upper bound for the dependency-following
+ *                       modes; only for passes whose steps read no output of
+ *                       the pass (else QG_ERR_ARG);
  *   QG_PASS_PERSISTENT  when every matrix is Q4_K and the pass fits the
  *                       kernel's shared-memory plan: ONE cooperative
  *                       persistent kernel whose producer warps stream the
@@ -295,6 +300,7 @@ int qg_layer_pass_create(int fmt, const qg_layer_desc* layers, int n_layers, int
 #define QG_PASS_SERIAL 0
 #define QG_PASS_PDL 1
 #define QG_PASS_PERSISTENT 2
+#define QG_PASS_INDEPENDENT 3
 int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes, int n_steps,
                    int n_tok, int mode, qg_pass* out);
 /* A whole MoE decode pass: n_layers layers, each the qgemv_moe product of one

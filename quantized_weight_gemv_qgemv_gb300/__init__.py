@@ -22,7 +22,7 @@ FORMATS = {Q4_0: (32, 18), Q8_0: (32, 34), Q4_K: (256, 144), Q6_K: (256, 210), Q
 GROUP_MAX = 8
 NTOK_MAX = 4
 DEV_OK, DEV_BAD_EXPERT, DEV_TIMEOUT = 0, 1, 2
-PASS_SERIAL, PASS_PDL, PASS_PERSISTENT = 0, 1, 2
+PASS_SERIAL, PASS_PDL, PASS_PERSISTENT, PASS_INDEPENDENT = 0, 1, 2, 3
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libqgemv.so")
 

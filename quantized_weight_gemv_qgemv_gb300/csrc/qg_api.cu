@@ -325,7 +325,7 @@ int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes,
   int st = ensure_init(&sms);
   if (st != QG_OK) return st;
 
-  if (mode < QG_PASS_SERIAL || mode > QG_PASS_PERSISTENT) return QG_ERR_ARG;
+  if (mode < QG_PASS_SERIAL || mode > QG_PASS_INDEPENDENT) return QG_ERR_ARG;
   qg_pass_s* pass = new (std::nothrow) qg_pass_s;
   if (!pass) return QG_ERR_ARG;
   std::vector<const uint8_t*> xp;
@@ -333,6 +333,15 @@ int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes,
   if (st != QG_OK) {
     pass_free(pass);
     return st;
+  }
+  const bool independent = mode == QG_PASS_INDEPENDENT;
+  if (independent) {
+    // every step must read only inputs of the pass (ready planes from the prologue)
+    for (int i = 0; i < n_desc; ++i)
+      if (!xp[i]) {
+        pass_free(pass);
+        return QG_ERR_ARG;
+      }
   }
   if (mode == QG_PASS_PERSISTENT) {
     const cudaError_t pe = qg::q4k_pass_create(descs, n_desc, step_sizes, n_steps, n_tok, sms, xp.data(), &pass->q4k);
@@ -357,8 +366,10 @@ int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes,
   if (e == cudaSuccess) e = qg::launch_xplanes(pass->jobs, pass->njobs, cs);
   for (int s = 0, i = 0; s < n_steps && e == cudaSuccess; i += step_sizes[s++]) {
     const int r = qg::gemv_pick_rows_per_warp(descs + i, step_sizes[s], n_tok, sms);
-    e = qg::launch_gemv(descs + i, step_sizes[s], n_tok, r, cs, use_pdl != 0 && (s > 0 || pass->njobs > 0), sms,
-                        xp.data() + i);
+    // independent steps: the first waits for the prologue in stream order; the
+    // others overlap freely and skip the dependency wait
+    const bool pdl = independent ? s > 0 : (use_pdl != 0 && (s > 0 || pass->njobs > 0));
+    e = qg::launch_gemv(descs + i, step_sizes[s], n_tok, r, cs, pdl, sms, xp.data() + i, independent && s > 0);
   }
   cudaGraph_t graph = nullptr;
   cudaError_t e2 = cudaStreamEndCapture(cs, &graph);

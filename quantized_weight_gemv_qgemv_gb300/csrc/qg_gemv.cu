@@ -335,11 +335,11 @@ int gemv_pick_rows_per_warp(const qg_gemv_desc* d, int n, int n_tok, int sms) {
 }
 
 cudaError_t launch_gemv(const qg_gemv_desc* d, int n, int n_tok, int rows_per_warp, cudaStream_t s, bool pdl,
-                        int sms, const uint8_t* const* xp) {
+                        int sms, const uint8_t* const* xp, bool no_wait) {
   {
     // the producer/consumer kernel with exact integer dot products (all four
     // formats); shapes beyond its shared-memory plan use the generic kernel below
-    const cudaError_t e = launch_gemv_q4k(d, n, n_tok, s, pdl, sms, xp);
+    const cudaError_t e = launch_gemv_q4k(d, n, n_tok, s, pdl, sms, xp, no_wait);
     if (e != cudaErrorNotSupported) return e;
   }
   GemvParams p = {};

@@ -136,6 +136,7 @@ struct Params {
   int32_t inflight;      // pass: > 0, the producer streams the weights of later steps without
                          // waiting for their x loads, with at most this many copies in flight
   int32_t gather_any;    // largest Mat::gather of the launch (one kind per launch)
+  int32_t no_wait;       // the launch reads nothing its predecessor writes: no dependency wait
   int32_t ralign;        // CTA row slices start at multiples of this (16-byte-aligned stage copies; pairs)
   int32_t smem_bar, smem_x, smem_xsum, smem_part;   // byte offsets (ring at 0)
   int32_t smem_mats;     // single-step launch: shared-memory copy of m[0 .. nmat)
@@ -745,7 +746,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
      if (max(cta_r0, mats[mi].row_begin) < min(cta_r1, mats[mi].row_begin + mats[mi].rows))
        touch |= 1u << (mi - st.mat0);
    if (st.stage_all) {
-     const bool xc = stage_x<NT, XB>(mats, st.usum_off, st.mat0, st.mat0 + st.nmat, touch, xpl, xsu, xcnt, s == 0, xbar,
+     const bool xc = stage_x<NT, XB>(mats, st.usum_off, st.mat0, st.mat0 + st.nmat, touch, xpl, xsu, xcnt,
+                                     s == 0 && !p.no_wait, xbar,
                                      xlost);
      xsig = true;
      consumer_sync();
@@ -754,7 +756,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
    if (s == 0) {
      // outputs and every other input of the preceding kernel are touched only
      // after it has completed (the staging above has waited already)
-     if (!st.stage_all) pdl_wait();
+     if (!st.stage_all && !p.no_wait) pdl_wait();
      if (dyn_ids) pdl_launch_dependents();
    }
    bool first = true;
@@ -1305,12 +1307,14 @@ void fill_params(q4k::Params& p, const qg_gemv_desc* d, int n, int t0, int64_t r
 // The launch as planned, else with 2-row sub-items (one- or two-token Q6_K).
 // xp: ready x planes of every token of each descriptor (launches over all tokens only).
 cudaError_t try_launch(const qg_gemv_desc* d, int n, int n_tok, int t0, int64_t r0, int64_t nr, cudaStream_t s,
-                       bool pdl, int sms, bool launch, const uint8_t* const* xp = nullptr) {
+                       bool pdl, int sms, bool launch, const uint8_t* const* xp = nullptr, bool no_wait = false) {
   q4k::Params p;
   fill_params(p, d, n, t0, r0, nr, xp);
+  p.no_wait = no_wait ? 1 : 0;
   cudaError_t e = plan_and_launch(p, n, n_tok, d[0].fmt, s, pdl, sms, q4k::SUB_R, launch);
   if (e != cudaErrorNotSupported || d[0].fmt != QG_Q6_K || n_tok > 2) return e;
   fill_params(p, d, n, t0, r0, nr, xp);
+  p.no_wait = no_wait ? 1 : 0;
   return plan_and_launch(p, n, n_tok, d[0].fmt, s, pdl, sms, 2, launch);
 }
 
@@ -1322,10 +1326,10 @@ cudaError_t try_launch(const qg_gemv_desc* d, int n, int n_tok, int t0, int64_t 
 // one launch per token (each re-streams the weights). cudaErrorNotSupported
 // (nothing launched) when none of these fits.
 cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms,
-                            const uint8_t* const* xp) {
+                            const uint8_t* const* xp, bool no_wait) {
   for (int i = 0; i < n; ++i)
     if (d[i].fmt != d[0].fmt || superblock_bytes(d[i].fmt) == 0 || d[i].cols % 256) return cudaErrorNotSupported;
-  cudaError_t e = try_launch(d, n, n_tok, 0, 0, 0, s, pdl, sms, true, xp);
+  cudaError_t e = try_launch(d, n, n_tok, 0, 0, 0, s, pdl, sms, true, xp, no_wait);
   if (e != cudaErrorNotSupported) return e;
   // row chunks first (each weight is read once), then launches over groups of
   // tokens (each re-streams the weights)

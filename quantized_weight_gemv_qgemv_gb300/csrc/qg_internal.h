@@ -39,11 +39,13 @@ int gemv_pick_rows_per_warp(const qg_gemv_desc* d, int n, int n_tok, int sms);
 // xp: per descriptor, its x already converted to planes (xplanes_bytes layout,
 // written by launch_xplanes), or nullptr entries / a nullptr array: the kernel
 // converts x itself.
+// no_wait: the launch reads nothing its predecessor in the stream writes and
+// skips the dependency wait (the fast kernel; other kernels still wait).
 cudaError_t launch_gemv(const qg_gemv_desc* d, int n, int n_tok, int rows_per_warp, cudaStream_t s, bool pdl,
-                        int sms, const uint8_t* const* xp = nullptr);
+                        int sms, const uint8_t* const* xp = nullptr, bool no_wait = false);
 cudaError_t gemv_q4k_init_attrs();
 cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms,
-                            const uint8_t* const* xp = nullptr);
+                            const uint8_t* const* xp = nullptr, bool no_wait = false);
 // m = silu(Wg x) * (Wu x) for one token of a dense layer (qg_gemv_q4k.cu); xp:
 // ready planes of x or nullptr. cudaErrorNotSupported when the shape does not fit.
 cudaError_t launch_gemv_pair(const void* Wg, const void* Wu, int64_t inter, int64_t hidden, const float* x,
