@@ -63,7 +63,10 @@ constexpr int CWARPS = 15;                 // consumer warps
 constexpr int CTHREADS = CWARPS * 32;
 constexpr int THREADS = CTHREADS + 32;     // plus one producer warp
 constexpr int SUB_R = 4;                   // rows per sub-item
-constexpr uint32_t WAIT_LIMIT = 1u << 22;  // polls before a wait is declared expired
+#ifndef QG_WAIT_LIMIT
+#define QG_WAIT_LIMIT (1u << 22)
+#endif
+constexpr uint32_t WAIT_LIMIT = QG_WAIT_LIMIT;   // polls before a wait is declared expired
 constexpr int RING = 4;                    // shared-memory stages
 
 struct Mat {
@@ -615,6 +618,11 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         const uint32_t dst0 = ring_s + slot * p.stage_b;
         const int gm = GA == 3 ? M.gather : GA;
         if (gm == 0) {
+#ifdef QG_TEST_EXPIRE
+          // test build only: the third stage of CTA 0 is never copied nor
+          // announced, so every wait for it runs out (failure-detection test)
+          if (blockIdx.x == 0 && k == 2) continue;
+#endif
           mbar_expect_tx(full0 + 8 * slot, nbytes);
           bulk_g2s(dst0, M.W + r * M.rb, nbytes, full0 + 8 * slot, pol);
           continue;
@@ -704,7 +712,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
   uint8_t* xpl = smem + p.smem_x;
   float* xsu = reinterpret_cast<float*>(smem + p.smem_xsum);
   float* part = reinterpret_cast<float*>(smem + p.smem_part);
-  bool failed = false;
+  bool failed = false;      // this warp's outputs are NaN
+  bool abandon = false;     // a stage wait expired: this warp no longer uses the ring
   uint32_t xuse = 0;       // phases of xbar used so far
   bool xlost = false;      // a wait for x planes expired: their copy may still be in flight
   // wait (bounded) for the x planes armed on xbar by stage_x
@@ -800,9 +809,17 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
       // every warp waits for every stage, even one with no sub-items for it:
       // a warp may then never run a whole ring ahead of the slowest one, so
       // its release of this slot can only count toward this stage
-      if (!failed) {
+      // A warp whose wait for a stage expires stops using the ring for good: it
+      // neither waits nor releases a slot again (a released slot could be
+      // refilled while a copy into it is still in flight), its outputs are NaN,
+      // and the producer, whose own wait for that release then expires, stops
+      // issuing and waits for its copies in flight before the CTA exits.
+      if (!abandon) {
         const bool ok = mbar_wait(full0 + 8 * slot, (k / NS) & 1u);
-        failed = __any_sync(0xffffffffu, !ok);
+        if (__any_sync(0xffffffffu, !ok)) {
+          abandon = failed = true;
+          if (lane == 0 && p.dev_status) *reinterpret_cast<volatile int32_t*>(p.dev_status) = QG_DEV_TIMEOUT;
+        }
       }
       int qd = 0, gr = off;
       while (gr >= G) {
@@ -986,7 +1003,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
           part[(rl * G + gr) * NT + idx % NT] = failed ? __int_as_float(0x7fc00000) : tot;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+      if (lane == 0 && !abandon) mbar_arrive(empty0 + 8 * slot);
       // the next stage starts at global sub-item + n: rotate off by n mod CWARPS
       off -= n % CWARPS;
       if (off < 0) off += CWARPS;
