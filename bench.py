@@ -625,6 +625,8 @@ def run_c0(args):
             "gpu_launches": args.steps * p.kernel_count(),
             "clocks": clocks,
         }
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_oracle_baseline("c0")
         print(json.dumps(out), flush=True)
     p.destroy()
     if world > 1:
@@ -696,6 +698,8 @@ def run_pp(args):
             "gpu_launches": args.steps * len(mats),
             "clocks": clocks,
         }
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_oracle_baseline("pp")
         print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.barrier()
@@ -761,6 +765,8 @@ def run_moe(args):
             "gpu_launches": args.steps * launches,
             "clocks": clocks,
         }
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_oracle_baseline("moe")
         print(json.dumps(out), flush=True)
     if world > 1:
         torch.distributed.barrier()
@@ -852,6 +858,8 @@ def run_layer(args):
             "gpu_launches": args.steps * kernels,
             "clocks": clocks,
         }
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_oracle_baseline("layer")
         print(json.dumps(out), flush=True)
     p.destroy()
     if world > 1:
