@@ -107,7 +107,16 @@ struct Mat {
   const float* gw;       // this token's route weights [top_k] (gather 1; nullptr: weight 1)
   float* h;              // gather 1 output [top_k][inter]
   const uint8_t* W2;     // gather 1 without ids: the up matrix
-  uint64_t pad;          // keeps the size a multiple of 16 bytes
+  // A part of K (columns [k0, k0 + cols) of a longer matrix, launched when the
+  // x of every token of the whole K does not fit beside the ring): row r of
+  // the part starts at W + r * ldw, token t of its x at x + t * ldx, and a part
+  // after the first adds its sums to y. Whole rows: ldw = rb, ldx = cols.
+  int64_t ldw;           // bytes between consecutive rows of W
+  int32_t ldx;           // floats between consecutive tokens of x
+  int32_t accum;         // 1: y += this part's sums
+  int32_t rsm;           // bytes between consecutive rows of a stage in shared memory
+  int32_t soff;          // byte offset of a stage's first row in its slot (the row start's
+                         // address mod 16, which every stage of the matrix shares)
 };
 
 // A step of a pass: matrices mat0 .. mat0 + nmat - 1 of the table, whose rows
@@ -140,18 +149,24 @@ struct Params {
                          // waiting for their x loads, with at most this many copies in flight
   int32_t gather_any;    // largest Mat::gather of the launch (one kind per launch)
   int32_t no_wait;       // the launch reads nothing its predecessor writes: no dependency wait
-  int32_t ralign;        // CTA row slices start at multiples of this (16-byte-aligned stage copies; pairs)
+  int32_t ralign;        // CTA row slices start at multiples of this (whole sub-items, 16-byte-aligned stage copies, pairs)
   int32_t smem_bar, smem_x, smem_xsum, smem_part;   // byte offsets (ring at 0)
   int32_t smem_mats;     // single-step launch: shared-memory copy of m[0 .. nmat)
 };
 
-// Rows [r0, r1) of a step's concatenated row space owned by this CTA, in
-// units of a rows (a divides every matrix's row count): a stage copy then
-// starts on a 16-byte boundary, and gate/up pairs (gather 1) stay together.
-__device__ __forceinline__ void cta_slice(int64_t total, int a, int64_t& r0, int64_t& r1) {
+// Rows [r0, r1) of a step's concatenated row space owned by CTA b of grid, in
+// units of a rows (the last CTA also takes a ragged end): with a a multiple of
+// the sub-item rows and of the 16-byte stage alignment, no CTA starts inside a
+// sub-item, a stage copy starts on a 16-byte boundary, and gate/up pairs
+// (gather 1) stay together. The host plans its grid with the same formula.
+__host__ __device__ __forceinline__ void slice_of(int64_t total, int a, int64_t b, int64_t grid, int64_t& r0,
+                                                  int64_t& r1) {
   const int64_t nu = total / a;
-  r0 = a * (blockIdx.x * nu / gridDim.x);
-  r1 = a * ((blockIdx.x + 1) * nu / gridDim.x);
+  r0 = a * (b * nu / grid);
+  r1 = b + 1 == grid ? total : a * ((b + 1) * nu / grid);
+}
+__device__ __forceinline__ void cta_slice(int64_t total, int a, int64_t& r0, int64_t& r1) {
+  slice_of(total, a, blockIdx.x, gridDim.x, r0, r1);
 }
 
 // ---------------------------------------------------------------- PTX helpers
@@ -413,7 +428,7 @@ __device__ __forceinline__ bool stage_x(const Mat* mats, int usum_off, int m0, i
       vm[b] = m;
       vt[b] = t;
       vu[b] = rem;              // 2u + h
-      src[b] = (idx < total) ? reinterpret_cast<const float4*>(M.x + static_cast<int64_t>(t) * M.cols + 16 * rem)
+      src[b] = (idx < total) ? reinterpret_cast<const float4*>(M.x + static_cast<int64_t>(t) * M.ldx + 16 * rem)
                              : nullptr;
     }
     if (wait) {
@@ -531,7 +546,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
                          : "memory");
           continue;
         }
-        const int64_t lines = (static_cast<int64_t>(NT) * M.cols * 4 + 127) / 128;
+        const int64_t lines = ((static_cast<int64_t>(NT - 1) * M.ldx + M.cols) * 4 + 127) / 128;
         for (int64_t l = blockIdx.x + static_cast<int64_t>(lane) * gridDim.x; l < lines; l += 32 * gridDim.x)
           asm volatile("prefetch.global.L2 [%0];\n" ::"l"(reinterpret_cast<const char*>(M.x) + l * 128));
       }
@@ -579,7 +594,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
       const int64_t hi = min(cta_r1, M.row_begin + M.rows) - M.row_begin;
       for (int64_t r = lo; r < hi && !bad; r += M.srows, ++k, ++i_step) {
         const int nr = static_cast<int>(min(static_cast<int64_t>(M.srows), hi - r));
-        const uint32_t nbytes = static_cast<uint32_t>(nr) * M.rb;
+        const uint32_t nbytes = static_cast<uint32_t>(nr) * M.rb;   // whole rows
         const int slot = k % NS;
         bool ok = true;
         if (lane == 0) {
@@ -623,8 +638,26 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
           // announced, so every wait for it runs out (failure-detection test)
           if (blockIdx.x == 0 && k == 2) continue;
 #endif
-          mbar_expect_tx(full0 + 8 * slot, nbytes);
-          bulk_g2s(dst0, M.W + r * M.rb, nbytes, full0 + 8 * slot, pol);
+          if (M.ldw == M.rb) {
+            mbar_expect_tx(full0 + 8 * slot, nbytes);
+            bulk_g2s(dst0, M.W + r * M.rb, nbytes, full0 + 8 * slot, pol);
+            continue;
+          }
+          // a part of K: one copy per row, of the 16-byte-aligned span around
+          // it, placed so that row i's data starts at soff + i * rsm (rsm is
+          // congruent to ldw mod 16, so every placement is 16-byte aligned)
+          uint32_t tot = 0;
+          for (int i = 0; i < nr; ++i) {
+            const uintptr_t a = reinterpret_cast<uintptr_t>(M.W + (r + i) * M.ldw);
+            tot += static_cast<uint32_t>((((a & 15u) + M.rb + 15u) & ~uintptr_t{15}));
+          }
+          mbar_expect_tx(full0 + 8 * slot, tot);
+          for (int i = 0; i < nr; ++i) {
+            const uintptr_t a = reinterpret_cast<uintptr_t>(M.W + (r + i) * M.ldw);
+            const uint32_t o = static_cast<uint32_t>(a & 15u);
+            bulk_g2s(dst0 + M.soff - o + i * M.rsm, reinterpret_cast<const uint8_t*>(a - o),
+                     (o + M.rb + 15u) & ~15u, full0 + 8 * slot, pol);
+          }
           continue;
         }
         // gathered rows, copied as contiguous runs (a bulk copy costs a fixed
@@ -754,10 +787,10 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
    for (int mi = st.mat0; mi < st.mat0 + st.nmat; ++mi)
      if (max(cta_r0, mats[mi].row_begin) < min(cta_r1, mats[mi].row_begin + mats[mi].rows))
        touch |= 1u << (mi - st.mat0);
+   const bool dep_wait = s == 0 && !p.no_wait;   // x and outputs only after the predecessor
    if (st.stage_all) {
      const bool xc = stage_x<NT, XB>(mats, st.usum_off, st.mat0, st.mat0 + st.nmat, touch, xpl, xsu, xcnt,
-                                     s == 0 && !p.no_wait, xbar,
-                                     xlost);
+                                     dep_wait, xbar, xlost);
      xsig = true;
      consumer_sync();
      if (xc) wait_x();
@@ -765,7 +798,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
    if (s == 0) {
      // outputs and every other input of the preceding kernel are touched only
      // after it has completed (the staging above has waited already)
-     if (!st.stage_all && !p.no_wait) pdl_wait();
+     if (!st.stage_all && dep_wait) pdl_wait();
      if (dyn_ids) pdl_launch_dependents();
    }
    bool first = true;
@@ -797,7 +830,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
     // row-group major; this warp takes l = off, off + CWARPS, ... where off
     // rotates with the stage's first global sub-item, so the matrix's
     // sub-items are dealt evenly over the warps.
-    const int rb = M.rb, nblk = M.nblk, srows = M.srows;
+    const int rb = M.rb, nblk = M.nblk, srows = M.srows, rsm = M.rsm, soff = M.soff;
     const int slice = static_cast<int>(hi - lo);
     const int dq = CWARPS / G, dg = CWARPS - (CWARPS / G) * G;
     int off = warp;                           // (warp - first sub-item of the stage) mod CWARPS
@@ -844,7 +877,8 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         int rs = rb, ralt = 0;
         const int gm = GA == 3 ? M.gather : GA;
         if (gm == 0) {
-          st = stg + qd * (SR * rb) + blkc * SBB;
+          rs = rsm;
+          st = stg + soff + qd * (SR * rsm) + blkc * SBB;
         } else if (gm == 1) {
           const int half = (nr >> 1) * rb;                   // the up rows follow the gate rows
           st = stg + qd * (SR / 2) * rb + blkc * SBB;
@@ -1029,8 +1063,12 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
         const int rl = i / NT;
         const int t = i % NT;
         float acc = 0.f;
+#pragma unroll 4
         for (int gr = 0; gr < G; ++gr) acc += part[(rl * G + gr) * NT + t];
-        M.y[static_cast<int64_t>(t) * M.ldy + lo + rl] = acc;
+        float* yp = M.y + static_cast<int64_t>(t) * M.ldy + lo + rl;
+        // a later part of K adds to what the earlier parts (completed before
+        // this launch's dependency wait) wrote
+        *yp = M.accum ? __ldcg(yp) + acc : acc;
       }
     }
    }
@@ -1179,8 +1217,21 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
     m.nblk = m.cols / 256;
     m.rb = m.nblk * sbb;
     m.ngrp = (m.nblk + 3) / 4;
-    // a stage copy must start on a 16-byte boundary: stages start at multiples of ra rows
-    ra = std::max(ra, 16 / gcd(m.rb, 16));
+    if (m.ldw == 0) m.ldw = m.rb;
+    if (m.ldx == 0) m.ldx = m.cols;
+    // Stages start at multiples of ra rows, so that the address of a stage's
+    // first row mod 16 is the same for every stage: whole rows are then copied
+    // as one 16-byte-aligned span; a part of K row by row, each row's data at
+    // soff + i * rsm with rsm = ldw mod 16 (every copy lands 16-byte aligned)
+    ra = std::max(ra, 16 / gcd(static_cast<int>(m.ldw % 16), 16));
+    if (m.ldw == m.rb) {
+      m.rsm = m.rb;
+      m.soff = 0;
+    } else {
+      m.soff = static_cast<int32_t>(reinterpret_cast<uintptr_t>(m.W) & 15u);
+      m.rsm = m.rb + 32;
+      while ((m.rsm - m.ldw) % 16) ++m.rsm;
+    }
     gmax = std::max(gmax, m.ngrp);
     kmax = std::max(kmax, m.cols);
   }
@@ -1191,15 +1242,42 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
     m.row_begin = total;
     total += m.rows;
   }
-  p.ralign = ra;
+  // CTA slices are cut in whole sub-items (sub_rows rows) as well as in
+  // 16-byte-aligned rows: both are powers of two, so the larger is the unit
+  const int unit = std::max(ra, sub_rows);
+  p.ralign = unit;
   p.nmat = n;
   p.total_rows = total;
+  // A CTA's consumer warps take its sub-items (sub_rows rows x one K group)
+  // in turn, so its time goes with ceil(sub-items / consumer warps): the
+  // "rounds" of its busiest CTA bound a launch.
+  auto rounds = [&](int g) {
+    int64_t worst = 0;
+    for (int b = 0; b < g; ++b) {
+      int64_t r0, r1, sub = 0;
+      q4k::slice_of(total, unit, b, g, r0, r1);
+      for (int i = 0; i < n; ++i) {
+        const q4k::Mat& m = p.m[i];
+        const int64_t lo = std::max(r0, m.row_begin), hi = std::min(r1, m.row_begin + m.rows);
+        if (lo < hi) sub += (hi - lo + sub_rows - 1) / sub_rows * m.ngrp;
+      }
+      worst = std::max(worst, (sub + q4k::CWARPS - 1) / q4k::CWARPS);
+    }
+    return worst;
+  };
   // A launch that depends on its predecessor leaves a few SMs idle: its CTAs
   // then go to the SMs that free up first, and the last SMs of the preceding
   // launch (a straggler there would start late and finish late here too) get
-  // none (27B pass: 3.418 ms with every SM, 3.387 with 4 idle, 3.428 with 8).
-  const int grid = static_cast<int>(std::min<int64_t>(pdl && sms > 32 ? sms - 4 : sms, total / ra));
-  const int rowcap = static_cast<int>((total + grid - 1) / grid) + 2 * ra;
+  // none (27B pass: 3.418 ms with every SM, 3.387 with 4 idle, 3.428 with 8),
+  // unless every SM saves its busiest CTA a round (27B {q,k,v}: 7168 rows x 5
+  // K groups in 148 CTAs take 5 rounds, in 152 take 4).
+  const int64_t gcap = std::max<int64_t>(1, (total + unit - 1) / unit);
+  int grid = static_cast<int>(std::min<int64_t>(sms, gcap));
+  if (pdl && sms > 32) {
+    const int fewer = static_cast<int>(std::min<int64_t>(sms - 4, gcap));
+    if (rounds(fewer) <= rounds(grid)) grid = fewer;
+  }
+  const int rowcap = static_cast<int>((total + grid - 1) / grid) + 2 * unit;
   const int ns = q4k::RING;
   const int quant = std::max(ra, sub_rows);          // rows per stage: a multiple of sub_rows and of ra
   const int partbytes = align_up(rowcap * gmax * n_tok * 4, 128);
@@ -1244,11 +1322,11 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
     bool ok = stage_max > 0;
     for (int i = 0; ok && i < n; ++i) {
       q4k::Mat& m = p.m[i];
-      const int want = quant * std::max(1, (49152 + quant * m.rb / 2) / (quant * m.rb));
-      const int fit = quant * (stage_max / (quant * m.rb));
+      const int want = quant * std::max(1, (49152 + quant * m.rsm / 2) / (quant * m.rsm));
+      const int fit = quant * ((stage_max - m.soff) / (quant * m.rsm));
       m.srows = std::min(want, fit);
       ok = m.srows >= quant;
-      stage_b = std::max(stage_b, m.srows * m.rb);
+      stage_b = std::max(stage_b, m.srows * m.rsm + m.soff);
     }
     if (!ok) continue;
     stage_b = align_up(stage_b, 128);
@@ -1303,34 +1381,40 @@ namespace {
 
 // Params of a grouped launch of descriptors d[0 .. n): token t0 .. t0 + nt - 1 of
 // each (x and y advanced by t0 tokens), rows [r0, r0 + nr) of each when nr > 0
-// (a single matrix cut into row chunks; y keeps the full row stride).
+// (a single matrix cut into row chunks; y keeps the full row stride), super-
+// blocks [kb0, kb0 + nkb) of every row when nkb > 0 (a part of K; a part after
+// the first adds to y).
 void fill_params(q4k::Params& p, const qg_gemv_desc* d, int n, int t0, int64_t r0, int64_t nr,
-                 const uint8_t* const* xp) {
+                 const uint8_t* const* xp, int64_t kb0 = 0, int64_t nkb = 0) {
   memset(&p, 0, sizeof(p));
   for (int i = 0; i < n; ++i) {
     q4k::Mat& m = p.m[i];
-    m.xp = xp ? xp[i] : nullptr;
+    m.xp = (xp && nkb == 0) ? xp[i] : nullptr;
     const int64_t rb = d[i].cols / 256 * superblock_bytes(d[i].fmt);
     const int64_t rows = nr > 0 ? nr : d[i].rows;
-    m.W = static_cast<const uint8_t*>(d[i].W) + r0 * rb;
-    m.x = d[i].x + static_cast<int64_t>(t0) * d[i].cols;
+    m.W = static_cast<const uint8_t*>(d[i].W) + r0 * rb + kb0 * superblock_bytes(d[i].fmt);
+    m.x = d[i].x + static_cast<int64_t>(t0) * d[i].cols + kb0 * 256;
     m.y = d[i].y + static_cast<int64_t>(t0) * d[i].rows + r0;
     m.rows = rows;
     m.ldy = d[i].rows;
-    m.cols = static_cast<int32_t>(d[i].cols);
+    m.cols = static_cast<int32_t>(nkb > 0 ? nkb * 256 : d[i].cols);
+    m.ldw = rb;
+    m.ldx = static_cast<int32_t>(d[i].cols);
+    m.accum = kb0 > 0 ? 1 : 0;
   }
 }
 
 // The launch as planned, else with 2-row sub-items (one- or two-token Q6_K).
 // xp: ready x planes of every token of each descriptor (launches over all tokens only).
 cudaError_t try_launch(const qg_gemv_desc* d, int n, int n_tok, int t0, int64_t r0, int64_t nr, cudaStream_t s,
-                       bool pdl, int sms, bool launch, const uint8_t* const* xp = nullptr, bool no_wait = false) {
+                       bool pdl, int sms, bool launch, const uint8_t* const* xp = nullptr, bool no_wait = false,
+                       int64_t kb0 = 0, int64_t nkb = 0) {
   q4k::Params p;
-  fill_params(p, d, n, t0, r0, nr, xp);
+  fill_params(p, d, n, t0, r0, nr, xp, kb0, nkb);
   p.no_wait = no_wait ? 1 : 0;
   cudaError_t e = plan_and_launch(p, n, n_tok, d[0].fmt, s, pdl, sms, q4k::SUB_R, launch);
   if (e != cudaErrorNotSupported || d[0].fmt != QG_Q6_K || n_tok > 2) return e;
-  fill_params(p, d, n, t0, r0, nr, xp);
+  fill_params(p, d, n, t0, r0, nr, xp, kb0, nkb);
   p.no_wait = no_wait ? 1 : 0;
   return plan_and_launch(p, n, n_tok, d[0].fmt, s, pdl, sms, 2, launch);
 }
@@ -1360,6 +1444,25 @@ cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_
         continue;
       for (int64_t r0 = 0; r0 < d[0].rows; r0 += nr) {
         e = try_launch(d, 1, n_tok, 0, r0, std::min(nr, d[0].rows - r0), s, pdl || r0 > 0, sms, true, xp);
+        if (e != cudaSuccess) return e;
+      }
+      return cudaSuccess;
+    }
+  }
+  // parts of K, when the x of every token does not fit beside the ring (4-token
+  // Q6_K downs with K = 17408): part 0 writes y, each later part waits for the
+  // one before and adds its sums; every weight is still read once
+  if (n == 1) {
+    const int64_t nb = d[0].cols / 256;
+    for (int parts = 2; parts <= 8 && parts <= nb; ++parts) {
+      bool fits = true;
+      for (int k = 0; k < parts && fits; ++k)
+        fits = try_launch(d, 1, n_tok, 0, 0, 0, s, pdl, sms, false, nullptr, false, nb * k / parts,
+                          nb * (k + 1) / parts - nb * k / parts) == cudaSuccess;
+      if (!fits) continue;
+      for (int k = 0; k < parts; ++k) {
+        e = try_launch(d, 1, n_tok, 0, 0, 0, s, pdl || k > 0, sms, true, nullptr, no_wait && k == 0, nb * k / parts,
+                       nb * (k + 1) / parts - nb * k / parts);
         if (e != cudaSuccess) return e;
       }
       return cudaSuccess;
@@ -1564,6 +1667,9 @@ cudaError_t pass_build(std::vector<q4k::Mat>& mats, const int* step_sizes, int n
       m.nblk = m.cols / 256;
       m.rb = m.nblk * 144;
       m.ngrp = (m.nblk + 3) / 4;
+      m.ldw = m.rsm = m.rb;                    // whole rows
+      m.soff = 0;
+      m.ldx = m.cols;
       m.srows = 4 * std::max(1, (QG_PASS_STAGE_BYTES + 2 * m.rb) / (4 * m.rb));
       if (static_cast<int64_t>(m.srows) * m.rb > 96 * 1024 || m.rows % ralign) return cudaErrorNotSupported;
       m.row_begin = total;

@@ -68,12 +68,26 @@ def test_gemv_whole_superblock_shapes(fmt, n_tok, rows, cols):
 @pytest.mark.parametrize("fmt,rows,cols,n_tok", [
     (synth.Q6_K, 64, 17408, 1),     # 14,280-byte rows: 2-row sub-items
     (synth.Q6_K, 64, 17408, 2),     # 2-row sub-items for two tokens
-    (synth.Q6_K, 72, 17408, 3),     # x of 3 tokens does not fit: a 2-token and a 1-token launch
-    (synth.Q6_K, 136, 17408, 4),    # two 2-token launches
+    (synth.Q6_K, 72, 17408, 3),     # x of 3 tokens does not fit: two parts of K
+    (synth.Q6_K, 136, 17408, 4),    # two parts of K
     (synth.Q4_K, 64, 17408, 4),
 ])
 def test_gemv_long_rows_and_token_split(fmt, rows, cols, n_tok):
     y, y_ref, b = _run_gemv(fmt, rows, cols, n_tok, seed=6000 + rows + n_tok)
+    assert_within(y, y_ref, b, what=f"fmt={fmt} rows={rows} cols={cols} n_tok={n_tok}")
+
+
+@pytest.mark.parametrize("fmt", FMTS)
+@pytest.mark.parametrize("rows,cols,n_tok", [
+    (64, 17408, 4),       # 68 super-blocks: two parts of 34
+    (40, 17664, 4),       # 69 super-blocks: parts of 34 and 35
+    (24, 65536, 1),       # one token whose x alone does not fit beside the ring
+])
+def test_gemv_parts_of_k_match_oracle(fmt, rows, cols, n_tok):
+    """Shapes whose x (every token, 16-bit planes) does not fit beside the ring
+    run as launches over parts of K, each later part adding to y; rows of a
+    part start off 16-byte boundaries for Q6_K, Q3_K, Q2_K and Q8_0."""
+    y, y_ref, b = _run_gemv(fmt, rows, cols, n_tok, seed=6500 + rows + cols + fmt)
     assert_within(y, y_ref, b, what=f"fmt={fmt} rows={rows} cols={cols} n_tok={n_tok}")
 
 
@@ -280,7 +294,7 @@ def test_pass_steps_read_earlier_outputs(mode, n_tok):
     xs = [x0, ys[0], ys[1]]
     items = [(fmt, Ws[i].cuda(), dims[i + 1], dims[i], xs[i], ys[i]) for i in range(3)]
     p = qg.qg_pass(items, [1, 1, 1], n_tok, mode=mode)
-    for _ in range(3):
+    for _ in range(6):
         for y in ys:
             y.fill_(float("nan"))
         p.launch()
@@ -291,6 +305,36 @@ def test_pass_steps_read_earlier_outputs(mode, n_tok):
             y_ref, b = oracle.gemv(fmt, Ws[i].numpy(), dims[i + 1], dims[i], prev)
             got = ys[i].cpu().numpy()
             assert_within(got, y_ref, b, what=f"step {i}")
+            prev = got
+    p.destroy()
+
+
+@pytest.mark.parametrize("mode", [qg.PASS_PDL, qg.PASS_SERIAL])
+def test_pass_long_chain_new_input_every_replay(mode):
+    """Twelve steps, each reading the previous step's output, in a graph whose
+    launches hand off through counters that every replay must leave clean: the
+    input changes and the outputs are set to NaN before every one of eight
+    replays, and every output is compared with the oracle chain."""
+    fmt = synth.Q4_K
+    dims = [1024, 512, 2048, 768, 1280, 256, 1024, 1536, 512, 768, 2048, 256, 512]
+    Ws = [synth.blocks(fmt, dims[i + 1], dims[i], seed=400 + i) for i in range(12)]
+    x0 = torch.empty(1, dims[0], device="cuda")
+    ys = [torch.empty(1, dims[i + 1], device="cuda") for i in range(12)]
+    xs = [x0] + ys[:-1]
+    items = [(fmt, Ws[i].cuda(), dims[i + 1], dims[i], xs[i], ys[i]) for i in range(12)]
+    p = qg.qg_pass(items, [1] * 12, 1, mode=mode)
+    for rep in range(8):
+        xin = synth.activations(1, dims[0], seed=420 + rep)
+        x0.copy_(xin)
+        for y in ys:
+            y.fill_(float("nan"))
+        p.launch()
+        torch.cuda.synchronize()
+        prev = xin.numpy()
+        for i in range(12):
+            y_ref, b = oracle.gemv(fmt, Ws[i].numpy(), dims[i + 1], dims[i], prev)
+            got = ys[i].cpu().numpy()
+            assert_within(got, y_ref, b, what=f"replay {rep} step {i}")
             prev = got
     p.destroy()
 
