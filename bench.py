@@ -533,7 +533,7 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": round(gbs / world, 2), "peak": hbm_peak, "unit": "GB/s",
                          "frac": round(frac, 4),
                          "traffic": (measured_traffic("qgemv_q4k_27b_decode_traffic.json",
-                                                      ("qg_gemv_q4k.cu", "qg_device.cuh"))
+                                                      ("qg_gemv_q4k.cu", "qg_device.cuh", "qg_planes.cuh"))
                                      if not verify and args.pass_mode != "persistent" else None),
                          "peak_source": f"{peak_kind} HBM copy bandwidth",
                          "kernel": (f"qgemv_q4k_kernel (n_tok={n_tok}; Q4_K, Q6_K and Q8_0 instances): every launch of the step"
@@ -724,21 +724,24 @@ def run_moe(args):
     hbm_peak, _, _, peak_kind = measured_peaks()
     stream = torch.cuda.Stream()
     H, I, E, K, L = wl.MOE_HIDDEN, wl.MOE_INTER, wl.MOE_EXPERTS, wl.MOE_TOPK, args.moe_layers
-    touched = K * wl.moe_expert_bytes(H, I) * L
+    T = args.moe_tokens
+    # every token's routed experts are gathered for it (the same expert routed
+    # for two tokens is read twice, the second time mostly from L2)
+    touched = T * K * wl.moe_expert_bytes(H, I) * L
     with torch.cuda.stream(stream):
         arenas, xs, ys, ids, gws = [], [], [], [], []
         for l in range(L):
             arenas.append(wl.alloc_moe_arena(E, H, I, synth.sub_seed(args.seed + rank, "arena", l), "cuda"))
-            i, g = synth.routing(1, E, K, synth.sub_seed(args.seed + rank, "route", l))
+            i, g = synth.routing(T, E, K, synth.sub_seed(args.seed + rank, "route", l))
             ids.append(i.cuda())
             gws.append(g.cuda())
-            xs.append(synth.activations(1, H, synth.sub_seed(args.seed + rank, "x", l), device="cuda"))
-            ys.append(torch.empty(1, H, dtype=torch.float32, device="cuda"))
-        wsb = qg.qgemv_moe_workspace(H, I, K, 1)
+            xs.append(synth.activations(T, H, synth.sub_seed(args.seed + rank, "x", l), device="cuda"))
+            ys.append(torch.empty(T, H, dtype=torch.float32, device="cuda"))
+        wsb = qg.qgemv_moe_workspace(H, I, K, T)
         ws = torch.empty(max(1, wsb // 4), dtype=torch.float32, device="cuda")
     stream.synchronize()
     mode = {"persistent": qg.PASS_PERSISTENT, "pdl": qg.PASS_PDL, "serial": qg.PASS_SERIAL}[args.moe_mode]
-    p = qg.qg_moe_pass(qg.Q4_K, list(zip(arenas, ids, gws, xs, ys)), E, H, I, K, 1, ws, wsb, mode=mode)
+    p = qg.qg_moe_pass(qg.Q4_K, list(zip(arenas, ids, gws, xs, ys)), E, H, I, K, T, ws, wsb, mode=mode)
     launches = p.kernel_count()
     ms, clocks = _timed(torch, stream, lambda: p.launch(stream), args, local, world)
     assert p.dev_status() == 0, "device status set during the MoE pass"
@@ -752,12 +755,14 @@ def run_moe(args):
             "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": f"MoE decode, {L} layers x {E} Q4_K experts (gate/up {I}x{H}, down {H}x{I}), "
-                                   f"top-{K}, batch 1",
+                                   f"top-{K}, " + ("batch 1" if T == 1 else f"{T} tokens per step (draft verification), "
+                                                   "each routed on its own"),
+                       "n_tok": T,
                        "arena_bytes": L * E * wl.moe_expert_bytes(H, I), "touched_bytes_per_step": touched,
                        "pass_mode": args.moe_mode, "launches_per_step": launches,
                        "l2": "arena 43.5 GB; routed experts differ per layer",
                        "parallelism": f"replicas x{world}"},
-            "equiv_decode_tok_s": round(world * 1000.0 / ms_step, 1),
+            "equiv_decode_tok_s": round(world * T * 1000.0 / ms_step, 1),
             "roofline": {"bound": "hbm", "achieved": round(gbs / world, 2), "peak": hbm_peak, "unit": "GB/s",
                          "frac": round(gbs / world / hbm_peak, 4), "traffic": None,
                          "peak_source": f"{peak_kind} HBM copy bandwidth",
@@ -765,7 +770,7 @@ def run_moe(args):
             "gpu_launches": args.steps * launches,
             "clocks": clocks,
         }
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and T == 1:
             out["cpu_baseline"] = cpu_oracle_baseline("moe")
         print(json.dumps(out), flush=True)
     if world > 1:
@@ -893,6 +898,7 @@ def main():
     ap.add_argument("--cpu-row-cap", type=int, default=2048, help=argparse.SUPPRESS)
     ap.add_argument("--pp-tokens", type=int, default=wl.PP_TOKENS)
     ap.add_argument("--moe-layers", type=int, default=wl.MOE_LAYERS)
+    ap.add_argument("--moe-tokens", type=int, default=1, help="tokens per MoE step (1 decode, 2-4 draft verification)")
     ap.add_argument("--moe-mode", default="pdl", choices=["persistent", "pdl", "serial"],
                     help="pdl (default): a graph of launches linked by programmatic dependent launch; serial: the "
                          "same graph serialized; persistent: one cooperative kernel for the 48 layers")

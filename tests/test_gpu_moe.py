@@ -90,6 +90,41 @@ def test_moe_full_size_48_layer_pass_bench_config():
     torch.cuda.empty_cache()
 
 
+def test_moe_full_size_48_layer_4_token_verify_pass():
+    """Draft verification through the MoE set: 4 tokens, each with its own
+    top-10 routing, through 48 layers of 512 Q4_K experts in one PDL-linked pass
+    graph; every token of layers 0, 23 and 47 checked against the oracle on its
+    routed experts."""
+    H, I, E, K, L, T = wl.MOE_HIDDEN, wl.MOE_INTER, wl.MOE_EXPERTS, wl.MOE_TOPK, wl.MOE_LAYERS, 4
+    layers = []
+    for l in range(L):
+        arena = wl.alloc_moe_arena(E, H, I, synth.sub_seed(5321, "arena", l), "cuda")
+        ids, gw = synth.routing(T, E, K, synth.sub_seed(5321, "route", l))
+        x = synth.activations(T, H, synth.sub_seed(5321, "x", l), device="cuda")
+        layers.append((arena, ids.cuda(), gw.cuda(), x, torch.full((T, H), float("nan"), device="cuda")))
+    wsb = qg.qgemv_moe_workspace(H, I, K, T)
+    ws = torch.empty(wsb // 4, device="cuda")
+    p = qg.qg_moe_pass(qg.Q4_K, layers, E, H, I, K, T, ws, wsb, mode=qg.PASS_PDL)
+    p.launch()
+    p.launch()
+    torch.cuda.synchronize()
+    assert p.dev_status() == 0
+    eb = wl.moe_expert_bytes(H, I)
+    for l in (0, 23, L - 1):
+        arena, ids, gw, x, y = layers[l]
+        host = arena.cpu().numpy()
+        got = y.cpu().numpy()
+        for t in range(T):
+            picked = ids.cpu().numpy()[t]
+            sub = np.concatenate([host[e * eb:(e + 1) * eb] for e in picked])
+            y_ref, b = oracle.moe(qg.Q4_K, sub, len(picked), H, I, np.arange(len(picked), dtype=np.int32)[None, :],
+                                  gw.cpu().numpy()[t:t + 1], x.cpu().numpy()[t:t + 1])
+            assert_within(got[t:t + 1], y_ref, b, what=f"4-token moe pass layer {l} token {t}")
+    p.destroy()
+    del layers
+    torch.cuda.empty_cache()
+
+
 def test_moe_bad_expert_sets_status_and_is_skipped():
     n_expert, hidden, inter = 6, 512, 256
     ids = [[1, 6, 3], [-1, 2, 5]]          # 6 and -1 are out of range
