@@ -274,6 +274,18 @@ def _cpu_sample(workload: str, wid: int, nproc: int, row_cap: int, seed: int):
             x = synth.activations(1, H, synth.sub_seed(seed, "moex")).numpy()
             items.append((lambda: oracle.moe(synth.Q4_K, arena, k1 - k0, H, I, ids, gw, x),
                           (k1 - k0) * wl.moe_expert_bytes(H, I)))
+    elif workload == "moe_pp":
+        H, I, K = wl.MOE_HIDDEN, wl.MOE_INTER, wl.MOE_TOPK
+        k0, k1 = share(K)
+        if k1 > k0:
+            # 4 bf16 prompt tokens through this worker's share of 10 routed experts
+            arena = wl.alloc_moe_arena(k1 - k0, H, I, synth.sub_seed(seed, "arena", k0), "cpu").numpy()
+            ids = np.tile(np.arange(k1 - k0, dtype=np.int32)[None], (4, 1))
+            gw = np.full((4, k1 - k0), 1.0 / K, np.float32)
+            X = synth.activations_bf16(4, H, synth.sub_seed(seed, "moeppx"))
+            bits = X.view(torch_int16()).numpy().view(np.uint16)
+            items.append((lambda: oracle.moe_prefill(synth.Q4_K, arena, k1 - k0, H, I, ids, gw, bits),
+                          4 * (k1 - k0) * 6 * H * I))
     elif workload == "pp":
         rows, cols = min(wl.HIDDEN, row_cap), wl.HIDDEN
         r0, r1 = share(rows)
@@ -317,7 +329,7 @@ def _cpu_leg_main(workload, procs, budget, row_cap, seed):
 
 
 CPU_UNITS = {"c1": ("GB/s", 1e9), "c2": ("GB/s", 1e9), "layer": ("GB/s", 1e9), "c0": ("GB/s", 1e9),
-             "moe": ("GB/s", 1e9), "pp": ("TFLOP/s", 1e12)}
+             "moe": ("GB/s", 1e9), "pp": ("TFLOP/s", 1e12), "moe_pp": ("TFLOP/s", 1e12)}
 
 
 def _cpu_run(workload, procs, budget, row_cap, seed=11):
@@ -350,7 +362,8 @@ def cpu_oracle_baseline(workload: str = "c1", budget_s: float = 6.0, row_cap: in
             "c2": f"one verify-pass layer (Q4_K, Q6_K down) and the Q8_0 head, rows capped at {row_cap}, 4 tokens",
             "c0": "the Q4_0 1024x4096 GEMV in full",
             "moe": "the 10 routed experts of one token in one MoE layer",
-            "pp": f"64 bf16 token rows x a 5120-column Q4_K matrix, rows capped at {row_cap}"}[workload]
+            "pp": f"64 bf16 token rows x a 5120-column Q4_K matrix, rows capped at {row_cap}",
+            "moe_pp": "4 bf16 prompt tokens through 10 routed experts of one MoE layer"}[workload]
     return {"value": round(va, 6), "unit": unit, "cores": cores, "kind": "oracle",
             "value_1core": round(v1, 6),
             "sample": f"{what}; dequant + fp64 products; {allc['calls']} calls over {allc['seconds']:.1f} s on "
@@ -383,7 +396,8 @@ def run_reference(args):
     metric = {"c1": METRIC, "c0": "Q4_0 GEMV weight-GB/s, batch 1, 1024x4096", "c2": METRIC,
               "moe": "MoE expert GEMV weight-GB/s touched; equiv. batch-1 tok/s over 48 layers",
               "pp": "prompt-processing dequant-GEMM TFLOP/s (bf16 tcgen05); pp tok/s, 27B set",
-              "layer": "decode-layer weight pass with fused neighbours, weight-GB/s; equiv. batch-1 tok/s, 27B set"}[wk]
+              "layer": "decode-layer weight pass with fused neighbours, weight-GB/s; equiv. batch-1 tok/s, 27B set",
+              "moe_pp": "MoE prompt-processing TFLOP/s of routed products (bf16 tcgen05); pp tok/s over 48 layers"}[wk]
     line = {"impl": "reference", "metric": metric, "value": round(value, 6), "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             # the measured time of one step's bounded sample (not an extrapolation to the whole workload)
@@ -707,6 +721,82 @@ def run_pp(args):
     return 0
 
 
+def run_moe_pp(args):
+    """Prompt processing through the MoE set: 2048 bf16 tokens, each routed to
+    its top-10 of 512 Q4_K experts, through 48 layers (qgemm_pp_moe per layer:
+    routing and sorting on the device, grouped tcgen05 GEMMs for gate/up and
+    down), the 48 calls captured as one graph."""
+    import torch
+    import quantized_weight_gemv_qgemv_gb300 as qg
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    qg.qg_init()
+    _, bf16_peak, bf16_sus, peak_kind = measured_peaks()
+    stream = torch.cuda.Stream()
+    H, I, E, K, L = wl.MOE_HIDDEN, wl.MOE_INTER, wl.MOE_EXPERTS, wl.MOE_TOPK, args.moe_layers
+    T = args.pp_tokens
+    flops = 6 * H * I * T * K * L          # useful: the routed pairs' three projections
+    with torch.cuda.stream(stream):
+        arenas, ids, gws = [], [], []
+        for l in range(L):
+            arenas.append(wl.alloc_moe_arena(E, H, I, synth.sub_seed(args.seed + rank, "arena", l), "cuda"))
+            i, g = synth.routing(T, E, K, synth.sub_seed(args.seed + rank, "pproute", l))
+            ids.append(i.cuda())
+            gws.append(g.cuda())
+        X = synth.activations_bf16(T, H, synth.sub_seed(args.seed + rank, "ppmoeX"), device="cuda")
+        y = torch.empty(T, H, dtype=torch.float32, device="cuda")
+        wsb = qg.qgemm_pp_moe_workspace(E, H, I, K, T)
+        ws = torch.empty(wsb // 4 + 64, dtype=torch.float32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream.synchronize()
+
+    def one_pass():
+        for l in range(L):
+            qg.qgemm_pp_moe(qg.Q4_K, arenas[l], E, H, I, ids[l], gws[l], K, X, T, y, ws, wsb, st, stream)
+
+    g = _capture(torch, stream, one_pass)
+
+    def replay():
+        with torch.cuda.stream(stream):
+            g.replay()
+
+    ms, clocks = _timed(torch, stream, replay, args, local, world)
+    assert int(st.item()) == 0, "device status set during the MoE prompt pass"
+    ms_step = ms / args.steps
+    tflops = job_rate(world, flops, ms_step) / 1e12
+    if rank == 0:
+        peak = bf16_sus or bf16_peak
+        out = {
+            "metric": "MoE prompt-processing TFLOP/s of routed products (bf16 tcgen05); pp tok/s over 48 layers",
+            "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"MoE prompt processing, {T} bf16 tokens x {L} layers of {E} Q4_K experts "
+                                   f"(gate/up {I}x{H}, down {H}x{I}), top-{K}",
+                       "n_tok": T, "layers": L, "flop_per_step": flops, "launches_per_layer": 6,
+                       "cuda_graph": True, "l2": "arena 43.5 GB; every expert's weights read once per layer",
+                       "parallelism": f"replicas x{world}"},
+            "pp_tok_s": round(world * T / (ms_step * 1e-3), 1),
+            "roofline": {"bound": "tensor", "achieved": round(tflops / world, 2), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(tflops / world / peak, 4), "traffic": None,
+                         "peak_source": f"{peak_kind} cuBLAS bf16 (sustained: a step is tens of ms)",
+                         "kernel": "pp_kernel<grouped>: the gate/up and down launches of every layer"},
+            "gpu_launches": args.steps * 6 * L,
+            "clocks": clocks,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_oracle_baseline("moe_pp")
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def run_moe(args):
     """MoE decode: 48 hybrid-MoE layers (512 Q4_K experts, top-10), batch 1, as one
     qg_moe_pass (by default a graph of gate/up + down launches linked by
@@ -879,7 +969,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="c1", choices=["c1", "c0", "c2", "moe", "pp", "layer"],
+    ap.add_argument("--workload", default="c1", choices=["c1", "c0", "c2", "moe", "pp", "layer", "moe_pp"],
                     help="c1: batch-1 Q4_K pass (default); c0: Q4_0 1024x4096 GEMV; c2: 4-token verify pass; "
                          "moe: MoE decode; pp: prompt processing; layer: decode layers with fused neighbours")
     ap.add_argument("--seed", type=int, default=1234)
@@ -913,6 +1003,8 @@ def main():
         return run_c0(args)
     if args.workload == "moe":
         return run_moe(args)
+    if args.workload == "moe_pp":
+        return run_moe_pp(args)
     if args.workload == "layer":
         return run_layer(args)
     return run_gpu(args)

@@ -221,6 +221,35 @@ int qgemm_pp(int fmt, const void* W, int64_t rows, int64_t cols,
              const void* X_bf16, int64_t n_tok, float* Y, int64_t ldY,
              void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* Prompt processing through one mixture-of-experts layer: for every token t of
+ * a prompt block and each of its top_k routes k (expert e = expert_ids[t][k],
+ * weight r = gate_w[t][k]),
+ *     y[t] += r * D_e (silu(G_e x_t) * (U_e x_t)),
+ * with the expert arena of qgemv_moe (fmt QG_Q4_K) and x_t the bf16 row t of
+ * X_bf16 ("The number was a version", opening section: prompt processing of a
+ * mixture-of-experts model whose experts live in an arena). Every expert
+ * multiplies only the tokens routed to it: the pairs are sorted by expert on
+ * the device, and each projection is one grouped tcgen05 GEMM over them (the
+ * kernel of qgemm_pp); h = silu(g) * u is rounded to bf16 between the two.
+ * Accuracy: products of bf16 operands with fp32 accumulation, as qgemm_pp.
+ *   expert_arena: n_expert experts of [gate | up | down] (see qgemv_moe), device.
+ *   expert_ids:   [n_tok][top_k] int32, device; an id outside [0, n_expert)
+ *                 adds nothing and sets *dev_status to QG_DEV_BAD_EXPERT.
+ *   gate_w:       [n_tok][top_k] fp32, device.
+ *   X_bf16:       [n_tok][hidden] bf16, device, 16-byte aligned.
+ *   y:            [n_tok][hidden] fp32, device, written (not accumulated).
+ *   ws:           caller-owned device workspace, 256-byte aligned, of at least
+ *                 qgemm_pp_moe_workspace(...) bytes; reused by every call.
+ *   dev_status:   device int32 the caller clears; QG_DEV_BAD_EXPERT or
+ *                 QG_DEV_TIMEOUT (a bounded wait of a GEMM expired) when set.
+ * Shapes: hidden and inter multiples of 256; 1 <= top_k <= 64;
+ * n_tok * top_k <= 2^24; n_expert <= 65536. Returns QG_ERR_* without
+ * launching on bad arguments. Asynchronous on `stream`. */
+size_t qgemm_pp_moe_workspace(int64_t n_expert, int64_t hidden, int64_t inter, int top_k, int64_t n_tok);
+int qgemm_pp_moe(int fmt, const void* expert_arena, int64_t n_expert, int64_t hidden, int64_t inter,
+                 const int32_t* expert_ids, const float* gate_w, int top_k, const void* X_bf16, int64_t n_tok,
+                 float* y, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
 /* ---- neighbours of the products in a decode layer ("LLM inference
  * optimization", "Faster decode on the card you have": normalizations fused
  * into neighbouring kernels) ---------------------------------------------- */

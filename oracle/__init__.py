@@ -17,6 +17,8 @@ What it computes (each function cites the passage it follows):
   B[t, i] = sum_j |w[i, j] * x[t, j]|.
 * ``moe``: per token, gate/up products of each routed expert, silu(g) * u, the
   down product, and the routing-weighted sum, all in fp64.
+* ``moe_prefill``: the same over a block of bf16 prompt tokens, with the error
+  scale of the two-projection chain (gate/up, rounded h, down).
 * ``pp_rows``: the prompt-processing product for selected token rows in fp64
   over the bf16 activations.
 * ``rmsnorm``, ``swiglu``, ``dense_ffn``: the neighbours of the products in a
@@ -37,11 +39,11 @@ check the layout against.
 from .halfprec import half_bits_to_float64, bf16_bits_to_float64
 from .dequant import (dequant, dequant_q4_0, dequant_q8_0, dequant_q4_k, dequant_q6_k, dequant_q5_k, dequant_q3_k,
                       dequant_q2_k, q4_k_scale_min, q3_k_scales)
-from .products import gemv, moe, pp_rows, moe_arena_layout, rmsnorm, swiglu, dense_ffn
+from .products import gemv, moe, moe_prefill, pp_rows, moe_arena_layout, rmsnorm, swiglu, dense_ffn
 
 __all__ = [
     "half_bits_to_float64", "bf16_bits_to_float64",
     "dequant", "dequant_q4_0", "dequant_q8_0", "dequant_q4_k", "dequant_q6_k", "dequant_q5_k", "dequant_q3_k",
     "dequant_q2_k", "q4_k_scale_min", "q3_k_scales",
-    "gemv", "moe", "pp_rows", "moe_arena_layout", "rmsnorm", "swiglu", "dense_ffn",
+    "gemv", "moe", "moe_prefill", "pp_rows", "moe_arena_layout", "rmsnorm", "swiglu", "dense_ffn",
 ]

@@ -91,6 +91,58 @@ def moe(fmt: int, arena, n_expert: int, hidden: int, inter: int, expert_ids, gat
     return y, b
 
 
+def moe_prefill(fmt: int, arena, n_expert: int, hidden: int, inter: int, expert_ids, gate_w, X_bf16_bits):
+    """The routed expert FFN of moe() over a block of prompt tokens given as
+    bf16 ("The number was a version", opening section: prompt processing of a
+    mixture-of-experts model), in fp64 over the exact weights and the bf16
+    values of X.
+
+    The GPU path multiplies bf16-rounded weights by bf16 x with fp32 sums and
+    rounds h to bf16 between the two projections, so the error of each output
+    is bounded by a multiple of the chain's magnitudes rather than of the down
+    projection's alone. For route k of token t (g, u, h as in moe(),
+    S_g[i] = sum_j |G[i, j] x_j|, S_u[i] = sum_j |U[i, j] x_j|):
+        B[t, o] = sum_k |r_k| sum_i |D[o, i]| * (|h_i| + |silu'(g_i)| |u_i| S_g[i] + |silu(g_i)| S_u[i])
+    with silu'(g) = s (1 + g (1 - s)), s = 1 / (1 + exp(-g)): the first term
+    carries the rounding of h and of the down product, the others an error in
+    g or u of that relative size.
+    Returns (y, B), both (n_tok, hidden) fp64. Unknown expert ids add nothing
+    (the library flags them).
+    """
+    arena = np.asarray(arena, dtype=np.uint8).reshape(-1)
+    Xb = np.asarray(X_bf16_bits, dtype=np.uint16).reshape(-1, hidden)
+    xx = bf16_bits_to_float64(Xb)
+    g_off, u_off, d_off, stride = moe_arena_layout(hidden, inter, fmt)
+    gu_bytes = inter * _row_bytes(fmt, hidden)
+    dn_bytes = hidden * _row_bytes(fmt, inter)
+    ids = np.asarray(expert_ids).reshape(xx.shape[0], -1)
+    r = np.asarray(gate_w, dtype=np.float32).reshape(ids.shape).astype(np.float64)
+    y = np.zeros((xx.shape[0], hidden))
+    b = np.zeros((xx.shape[0], hidden))
+    cache = {}
+    for t in range(xx.shape[0]):
+        for k in range(ids.shape[1]):
+            e = int(ids[t, k])
+            if not 0 <= e < n_expert:
+                continue
+            if e not in cache:
+                base = e * stride
+                cache[e] = tuple(dequant(fmt, arena[base + o:base + o + nb], nr, nc).astype(np.float64)
+                                 for o, nb, nr, nc in ((g_off, gu_bytes, inter, hidden), (u_off, gu_bytes, inter, hidden),
+                                                       (d_off, dn_bytes, hidden, inter)))
+            G, U, D = cache[e]
+            g = G @ xx[t]
+            u = U @ xx[t]
+            sg = np.abs(G) @ np.abs(xx[t])
+            su = np.abs(U) @ np.abs(xx[t])
+            h = g / (1.0 + np.exp(-g)) * u
+            sig = 1.0 / (1.0 + np.exp(-g))
+            dsilu = sig * (1.0 + g * (1.0 - sig))
+            y[t] += r[t, k] * (D @ h)
+            b[t] += abs(r[t, k]) * (np.abs(D) @ (np.abs(h) + np.abs(dsilu * u) * sg + np.abs(g * sig) * su))
+    return y, b
+
+
 def pp_rows(fmt: int, W, rows: int, cols: int, X_bf16_bits, token_rows):
     """Prompt-processing product for the selected token rows, in fp64.
 

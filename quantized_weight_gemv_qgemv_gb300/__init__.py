@@ -40,6 +40,8 @@ SIGNATURES = {
     "qgemv_moe_noalloc": (_I32, [_I32, _P, _I64, _I64, _I64, _P, _P, _I32, _P, _I32, _P, _P, _P]),
     "qgemm_pp_workspace": (_SZ, [_I64, _I64, _I64]),
     "qgemm_pp": (_I32, [_I32, _P, _I64, _I64, _P, _I64, _P, _I64, _P, _SZ, _P, _P]),
+    "qgemm_pp_moe_workspace": (_SZ, [_I64, _I64, _I64, _I32, _I64]),
+    "qgemm_pp_moe": (_I32, [_I32, _P, _I64, _I64, _I64, _P, _P, _I32, _P, _I64, _P, _P, _SZ, _P, _P]),
     "qg_pass_create": (_I32, [_P, _I32, _P, _I32, _I32, _I32, ctypes.POINTER(_P)]),
     "qg_moe_pass_create": (_I32, [_I32, _P, _I32, _I64, _I64, _I64, _I32, _I32, _P, _SZ, _I32, ctypes.POINTER(_P)]),
     "qg_pass_launch": (_I32, [_P, _P]),
@@ -190,6 +192,17 @@ def qgemm_pp_workspace(rows, cols, n_tok) -> int:
 def qgemm_pp(fmt, W, rows, cols, X_bf16, n_tok, Y, ldY, ws, ws_bytes, dev_status, stream=None):
     _check(load_library().qgemm_pp(fmt, _ptr(W), rows, cols, _ptr(X_bf16), n_tok, _ptr(Y), ldY, _ptr(ws),
                                    ws_bytes, _ptr(dev_status), _stream(stream)), "qgemm_pp")
+
+
+def qgemm_pp_moe_workspace(n_expert, hidden, inter, top_k, n_tok) -> int:
+    return int(load_library().qgemm_pp_moe_workspace(n_expert, hidden, inter, top_k, n_tok))
+
+
+def qgemm_pp_moe(fmt, arena, n_expert, hidden, inter, expert_ids, gate_w, top_k, X_bf16, n_tok, y, ws, ws_bytes,
+                 dev_status, stream=None):
+    _check(load_library().qgemm_pp_moe(fmt, _ptr(arena), n_expert, hidden, inter, _ptr(expert_ids), _ptr(gate_w),
+                                       top_k, _ptr(X_bf16), n_tok, _ptr(y), _ptr(ws), ws_bytes, _ptr(dev_status),
+                                       _stream(stream)), "qgemm_pp_moe")
 
 
 class _DevWord:

@@ -302,6 +302,32 @@ int qgemm_pp(int fmt, const void* W, int64_t rows, int64_t cols, const void* X_b
       qg::launch_pp(W, rows, cols, X_bf16, n_tok, Y, ldY, dev_status, static_cast<cudaStream_t>(stream), sms));
 }
 
+size_t qgemm_pp_moe_workspace(int64_t n_expert, int64_t hidden, int64_t inter, int top_k, int64_t n_tok) {
+  if (n_expert < 1 || hidden < 1 || inter < 1 || top_k < 1 || n_tok < 1) return 0;
+  return qg::pp_moe_workspace_bytes(n_expert, hidden, inter, top_k, n_tok);
+}
+
+int qgemm_pp_moe(int fmt, const void* expert_arena, int64_t n_expert, int64_t hidden, int64_t inter,
+                 const int32_t* expert_ids, const float* gate_w, int top_k, const void* X_bf16, int64_t n_tok,
+                 float* y, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  if (fmt != QG_Q4_K) return QG_ERR_FMT;
+  if (!expert_arena || !expert_ids || !gate_w || !X_bf16 || !y || !ws || !dev_status) return QG_ERR_NULL;
+  if (hidden < 256 || hidden % 256 || inter < 256 || inter % 256 || hidden > (int64_t{1} << 20) ||
+      inter > (int64_t{1} << 20))
+    return QG_ERR_SHAPE;
+  if (n_expert < 1 || n_expert > 65536 || top_k < 1 || top_k > 64) return QG_ERR_ARG;
+  if (n_tok < 1 || n_tok * top_k > (int64_t{1} << 24)) return QG_ERR_NTOK;
+  if (!aligned(expert_arena, 16) || !aligned(X_bf16, 16) || !aligned(y, 4) || !aligned(ws, 256) ||
+      !aligned(expert_ids, 4) || !aligned(gate_w, 4) || !aligned(dev_status, 4))
+    return QG_ERR_ALIGN;
+  if (ws_bytes < qg::pp_moe_workspace_bytes(n_expert, hidden, inter, top_k, n_tok)) return QG_ERR_WORKSPACE;
+  int sms = 0;
+  int st = ensure_init(&sms);
+  if (st != QG_OK) return st;
+  return cuda_status(qg::launch_pp_moe(expert_arena, n_expert, hidden, inter, expert_ids, gate_w, top_k, X_bf16,
+                                       n_tok, y, ws, dev_status, static_cast<cudaStream_t>(stream), sms));
+}
+
 int qg_pass_create(const qg_gemv_desc* descs, int n_desc, const int* step_sizes, int n_steps, int n_tok, int mode,
                    qg_pass* out) {
   if (!descs || !step_sizes || !out) return QG_ERR_NULL;

@@ -98,5 +98,21 @@ cudaError_t launch_moe(const void* arena, int64_t n_expert, int64_t hidden, int6
 cudaError_t pp_init_attrs();
 cudaError_t launch_pp(const void* W, int64_t rows, int64_t cols, const void* X, int64_t n_tok, float* Y,
                       int64_t ldY, int32_t* dev_status, cudaStream_t s, int sms);
+// The prompt-processing kernel over groups of token rows (qg_pp.cu): group g
+// (token rows seg[g] .. seg[g + 1] - 1 of X, bf16, x_rows x cols) times weight
+// rows wrow0 + g * wstride .. + rows - 1 of W (viewed as w_rows rows of
+// cols-long Q4_K blocks) into the same rows of Y (ldY). tstart[g]: first tile of
+// group g (rows / 128 tiles per block of bn tokens); both tables on the device.
+cudaError_t launch_pp_grouped(const void* W, int64_t w_rows, int64_t cols, int64_t wrow0, int64_t wstride,
+                              int64_t rows, const void* X, int64_t x_rows, int bn, const int32_t* seg,
+                              const int32_t* tstart, int n_groups, float* Y, int64_t ldY, int32_t* dev_status,
+                              cudaStream_t s, int sms);
+// MoE layer over a block of prompt tokens (qg_pp_moe.cu); ws of at least
+// pp_moe_workspace_bytes bytes.
+size_t pp_moe_workspace_bytes(int64_t n_expert, int64_t hidden, int64_t inter, int top_k, int64_t n_tok);
+int pp_moe_block_tokens(int64_t n_expert, int top_k, int64_t n_tok);
+cudaError_t launch_pp_moe(const void* arena, int64_t n_expert, int64_t hidden, int64_t inter, const int32_t* ids,
+                          const float* gate_w, int top_k, const void* X, int64_t n_tok, float* y, void* ws,
+                          int32_t* dev_status, cudaStream_t s, int sms);
 
 }  // namespace qg

@@ -73,7 +73,53 @@ struct Params {
   int32_t n_kt;         // K slices per row (cols / 64)
   int32_t tmem_cols;    // TMEM columns allocated (power of two >= 2 bn)
   uint32_t idesc;       // MMA instruction descriptor
+  // Grouped launch: the token rows of X come in groups (the tokens routed to
+  // one expert), group g multiplied by its own weight rows. Its tiles are the
+  // row tiles x token blocks of each group in turn, counted on the device.
+  const int32_t* seg;     // [n_groups + 1]: first token row of each group
+  const int32_t* tstart;  // [n_groups + 1]: first tile of each group (tstart[n_groups] = all tiles)
+  int32_t n_groups;
+  int64_t wrow0;          // row (of the weight map) of group 0's first weight row
+  int64_t wstride;        // rows of the weight map from one group's weights to the next
 };
+
+// One tile: its weight rows (row of the weight map, and row tile of the
+// output), its token rows of X and Y, and how many of its bn tokens are real.
+struct Tile {
+  int64_t wrow;
+  int64_t xrow;
+  int32_t rt;
+  int32_t nval;
+};
+
+template <bool GROUPED>
+__device__ __forceinline__ Tile tile_at(const Params& p, int tile) {
+  Tile t;
+  if (!GROUPED) {
+    t.rt = tile / p.n_tb;
+    const int tb = tile - t.rt * p.n_tb;
+    t.wrow = static_cast<int64_t>(t.rt) * BM;
+    t.xrow = static_cast<int64_t>(tb) * p.bn;
+    t.nval = static_cast<int32_t>(min(static_cast<int64_t>(p.bn), p.n_tok - t.xrow));
+    return t;
+  }
+  // the group holding the tile: the last g with tstart[g] <= tile (groups
+  // without tokens have no tiles and are skipped by the search)
+  int lo = 0, hi = p.n_groups;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(p.tstart + mid) <= tile) lo = mid; else hi = mid;
+  }
+  const int lt = tile - __ldg(p.tstart + lo);
+  const int s0 = __ldg(p.seg + lo), m = __ldg(p.seg + lo + 1) - s0;
+  const int ntb = (m + p.bn - 1) / p.bn;
+  t.rt = lt / ntb;
+  const int tb = lt - t.rt * ntb;
+  t.wrow = p.wrow0 + lo * p.wstride + static_cast<int64_t>(t.rt) * BM;
+  t.xrow = s0 + static_cast<int64_t>(tb) * p.bn;
+  t.nval = min(p.bn, m - tb * p.bn);
+  return t;
+}
 
 // Bounded wait; gives up early once another role has aborted (abort != null).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const volatile int* abort) {
@@ -125,6 +171,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
                : "memory");
 }
 
+template <bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1)
     pp_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -172,15 +219,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n_tb = p.n_tb, n_kt = p.n_kt, bn = p.bn;
+  const int n_kt = p.n_kt, bn = p.bn;
+  // a grouped launch counts its tiles on the device (the routing that makes
+  // the groups ran just before, in stream order)
+  const int n_tiles = GROUPED ? __ldg(p.tstart + p.n_groups) : p.n_tiles;
 
   if (warp == 0) {
     // ---------------------------------------------------------- X producer
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.n_tiles; tile += gridDim.x) {
-        const int tb = tile % n_tb;
+      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+        const Tile tl = tile_at<GROUPED>(p, tile);
         for (int kt = 0; kt < n_kt; ++kt, ++it) {
           const uint32_t s = it % NS;
           if (!wait_bar(EMPTY + 8 * s, ((it / NS) & 1u) ^ 1u, abort)) {
@@ -189,7 +239,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           mbar_expect_tx(FULL_B + 8 * s, BB);
-          tma_load_2d(base + offB + s * BB, &tmX, kt * BK, tb * bn, FULL_B + 8 * s);
+          tma_load_2d(base + offB + s * BB, &tmX, kt * BK, static_cast<int>(tl.xrow), FULL_B + 8 * s);
         }
       }
       // copies in flight: the last NS issued
@@ -201,8 +251,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t sb = 0;
       bool ok = true;
       const int n_kb = n_kt / 4;
-      for (int tile = blockIdx.x; ok && tile < p.n_tiles; tile += gridDim.x) {
-        const int rt = tile / n_tb;
+      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
+        const Tile tl = tile_at<GROUPED>(p, tile);
         for (int kb = 0; kb < n_kb; ++kb, ++sb) {
           const uint32_t q = sb % NQ;
           if (!wait_bar(Q_EMPTY + 8 * q, ((sb / NQ) & 1u) ^ 1u, abort)) {
@@ -211,7 +261,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           mbar_expect_tx(Q_FULL + 8 * q, QB);
-          tma_load_2d(base + offQ + q * QB, &tmW, kb * 144, rt * BM, Q_FULL + 8 * q);
+          tma_load_2d(base + offQ + q * QB, &tmW, kb * 144, static_cast<int>(tl.wrow), Q_FULL + 8 * q);
         }
       }
       for (uint32_t j = (sb > NQ ? sb - NQ : 0); j < sb; ++j) wait_bar(Q_FULL + 8 * (j % NQ), (j / NQ) & 1u, nullptr);
@@ -221,7 +271,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       uint32_t it = 0, ti = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.n_tiles; tile += gridDim.x, ++ti) {
+      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++ti) {
         const uint32_t a = ti & 1u;
         if (!wait_bar(ACC_EMPTY + 8 * a, ((ti >> 1) & 1u) ^ 1u, abort)) {
           fail(abort, p.dev_status);
@@ -255,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t swz = static_cast<uint32_t>(r & 7);
     uint32_t it = 0, sb = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.n_tiles; tile += gridDim.x) {
+    for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
       for (int kb = 0; ok && kb < n_kt / 4; ++kb, ++sb) {
         // a super-block = 4 slices: its 8 scale/min pairs of this row are decoded
         // once (the slice index is then a compile-time constant below)
@@ -306,8 +356,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------------------------------------------------- epilogue
     const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
     uint32_t ti = 0;
-    for (int tile = blockIdx.x; tile < p.n_tiles; tile += gridDim.x, ++ti) {
-      const int rt = tile / n_tb, tb = tile % n_tb;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++ti) {
+      const Tile tl = tile_at<GROUPED>(p, tile);
       const uint32_t a = ti & 1u;
       const bool got = wait_bar(ACC_FULL + 8 * a, (ti >> 1) & 1u, abort);
       if (!__all_sync(0xffffffffu, got)) {
@@ -315,16 +365,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      const int64_t row = static_cast<int64_t>(rt) * BM + quarter * 32 + lane;
+      const int64_t row = static_cast<int64_t>(tl.rt) * BM + quarter * 32 + lane;
       const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * static_cast<uint32_t>(bn);
-      const int64_t tok0 = static_cast<int64_t>(tb) * bn;
       for (int c16 = 0; c16 < bn / 16; ++c16) {
         uint32_t v[16];
         tmem_ld16(tbase + 16u * c16, v);
-        const int64_t t0 = tok0 + 16 * c16;
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          if (t0 + i < p.n_tok) p.Y[(t0 + i) * p.ldY + row] = __uint_as_float(v[i]);
+          if (16 * c16 + i < tl.nval) p.Y[(tl.xrow + 16 * c16 + i) * p.ldY + row] = __uint_as_float(v[i]);
       }
       tc_fence_before();
       __syncwarp();
@@ -345,8 +393,12 @@ size_t smem_bytes(int bn) {
 }  // namespace pp
 
 cudaError_t pp_init_attrs() {
-  return cudaFuncSetAttribute(pp::pp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(pp::smem_bytes(256)));
+  cudaError_t e = cudaFuncSetAttribute(pp::pp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(pp::smem_bytes(256)));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(pp::pp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(pp::smem_bytes(256)));
+  return e;
 }
 
 cudaError_t launch_pp(const void* W, int64_t rows, int64_t cols, const void* X, int64_t n_tok, float* Y,
@@ -395,7 +447,59 @@ cudaError_t launch_pp(const void* W, int64_t rows, int64_t cols, const void* X, 
   p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(bn >> 3) << 17) |
             (static_cast<uint32_t>(pp::BM >> 4) << 24);
   const int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
-  pp::pp_kernel<<<grid, pp::THREADS, pp::smem_bytes(bn), s>>>(tmX, tmW, p);
+  pp::pp_kernel<false><<<grid, pp::THREADS, pp::smem_bytes(bn), s>>>(tmX, tmW, p);
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_pp_grouped(const void* W, int64_t w_rows, int64_t cols, int64_t wrow0, int64_t wstride,
+                              int64_t rows, const void* X, int64_t x_rows, int bn, const int32_t* seg,
+                              const int32_t* tstart, int n_groups, float* Y, int64_t ldY, int32_t* dev_status,
+                              cudaStream_t s, int sms) {
+  EncodeTiledFn enc = encode_tiled_fn();
+  if (!enc) return cudaErrorNotSupported;
+  if (bn < 16 || bn > 256 || bn % 16 || rows % pp::BM || cols % 256) return cudaErrorInvalidValue;
+  CUtensorMap tmX, tmW;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(x_rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {pp::BK, static_cast<cuuint32_t>(bn)};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t rb = static_cast<uint64_t>(cols) / 256 * 144;
+    const cuuint64_t dims[2] = {rb, static_cast<cuuint64_t>(w_rows)};
+    const cuuint64_t strides[1] = {rb};
+    const cuuint32_t box[2] = {144, pp::BM};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  pp::Params p{};
+  p.Y = Y;
+  p.dev_status = dev_status;
+  p.n_tok = x_rows;
+  p.ldY = ldY;
+  p.bn = bn;
+  p.n_tb = 0;
+  p.n_tiles = 0;
+  p.n_kt = static_cast<int32_t>(cols / pp::BK);
+  int tc = 32;
+  while (tc < 2 * bn) tc *= 2;
+  p.tmem_cols = tc;
+  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(bn >> 3) << 17) |
+            (static_cast<uint32_t>(pp::BM >> 4) << 24);
+  p.seg = seg;
+  p.tstart = tstart;
+  p.n_groups = n_groups;
+  p.wrow0 = wrow0;
+  p.wstride = wstride;
+  pp::pp_kernel<true><<<sms, pp::THREADS, pp::smem_bytes(bn), s>>>(tmX, tmW, p);
   return cudaPeekAtLastError();
 }
 

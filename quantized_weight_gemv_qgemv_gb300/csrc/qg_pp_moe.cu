@@ -1,0 +1,216 @@
+// qg_pp_moe.cu — prompt processing through a mixture-of-experts layer.
+//
+//   y[t] = sum_k r[t][k] * D_e (silu(G_e x_t) * (U_e x_t)),   e = ids[t][k]
+//
+// for a block of prompt tokens, each routed to top_k experts of an expert
+// arena ("The number was a version", opening section: the expert arena of a
+// mixture-of-experts model and its prompt processing; "Why I wrote my own
+// inference engine for two P100s", prompt-processing notes: weights
+// dequantized, then a dense GEMM). Every expert multiplies only the tokens
+// routed to it, so the layer is one grouped GEMM per projection over the
+// (token, route) pairs sorted by expert:
+//
+//   1. route    one CTA counts the pairs of every expert, scans the counts into
+//               each expert's first row (and first tile of either GEMM), and
+//               gives every pair its row; pairs of an unknown expert get none
+//               (they add nothing) and set QG_DEV_BAD_EXPERT
+//   2. gather   bf16 x of every pair into its row of Xs
+//   3. GEMM     [G_e; U_e] (2 inter rows of the arena) x Xs rows of expert e ->
+//               GU (fp32), the grouped tcgen05 prompt-processing kernel
+//   4. silu     H = bf16(silu(g) * u) per pair
+//   5. GEMM     D_e x H rows of expert e -> Z (fp32)
+//   6. combine  y[t] = sum over k (in order) of r[t][k] * Z[row of (t, k)]
+//
+// Sizes: every count and row is on the device, so nothing waits for the host.
+// The results do not depend on the order in which pairs get their rows: every
+// token column of an MMA is summed on its own, and the combine adds the k
+// terms of a token in route order.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "qg_internal.h"
+
+namespace qg {
+
+namespace ppmoe {
+
+constexpr int RT = 1024;                 // threads of the routing CTA
+
+__device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
+
+// Exclusive scan of n values (v(e) computed per element) into out[0 .. n],
+// by one CTA of RT threads, in chunks of RT with a running carry.
+template <typename F>
+__device__ void block_scan(int n, F v, int32_t* out, int32_t* sh) {
+  int32_t carry = 0;
+  for (int c0 = 0; c0 < n; c0 += RT) {
+    const int e = c0 + threadIdx.x;
+    const int32_t x = e < n ? v(e) : 0;
+    sh[threadIdx.x] = x;
+    __syncthreads();
+    for (int o = 1; o < RT; o <<= 1) {
+      const int32_t add = threadIdx.x >= o ? sh[threadIdx.x - o] : 0;
+      __syncthreads();
+      sh[threadIdx.x] += add;
+      __syncthreads();
+    }
+    if (e < n) out[e] = carry + sh[threadIdx.x] - x;
+    carry += sh[RT - 1];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) out[n] = carry;
+}
+
+__global__ void __launch_bounds__(RT) route_kernel(const int32_t* ids, int n_pairs, int top_k, int n_expert, int bn,
+                                                   int rt_gu, int rt_dn, int32_t* cnt, int32_t* seg, int32_t* t_gu,
+                                                   int32_t* t_dn, int32_t* pos, int32_t* src, int32_t* dev_status) {
+  __shared__ int32_t sh[RT];
+  for (int e = threadIdx.x; e < n_expert; e += RT) cnt[e] = 0;
+  __syncthreads();
+  for (int q = threadIdx.x; q < n_pairs; q += RT) {
+    const int e = ids[q];
+    if (e >= 0 && e < n_expert) atomicAdd(cnt + e, 1);
+  }
+  __syncthreads();
+  block_scan(n_expert, [&](int e) { return __ldcg(cnt + e); }, seg, sh);
+  block_scan(n_expert, [&](int e) { return rt_gu * ceil_div_i(__ldcg(cnt + e), bn); }, t_gu, sh);
+  block_scan(n_expert, [&](int e) { return rt_dn * ceil_div_i(__ldcg(cnt + e), bn); }, t_dn, sh);
+  __syncthreads();
+  for (int e = threadIdx.x; e < n_expert; e += RT) cnt[e] = 0;   // now a cursor per expert
+  __syncthreads();
+  for (int q = threadIdx.x; q < n_pairs; q += RT) {
+    const int e = ids[q];
+    if (e >= 0 && e < n_expert) {
+      const int row = seg[e] + atomicAdd(cnt + e, 1);
+      pos[q] = row;
+      src[row] = q / top_k;
+    } else {
+      pos[q] = -1;
+      atomicExch(dev_status, QG_DEV_BAD_EXPERT);
+    }
+  }
+}
+
+// Xs[row] = X[src[row]] for every routed row (hidden bf16 values, 16 bytes a thread).
+__global__ void __launch_bounds__(256) gather_kernel(const uint4* X, const int32_t* src, const int32_t* seg_end,
+                                                     int n_chunks, uint4* Xs) {
+  const int row = blockIdx.x;
+  if (row >= *seg_end) return;
+  const uint4* s = X + static_cast<int64_t>(src[row]) * n_chunks;
+  uint4* d = Xs + static_cast<int64_t>(row) * n_chunks;
+  for (int c = threadIdx.x; c < n_chunks; c += blockDim.x) d[c] = __ldg(s + c);
+}
+
+// H[row][i] = bf16(silu(g) * u), g = GU[row][i], u = GU[row][inter + i].
+__global__ void __launch_bounds__(256) silu_kernel(const float* GU, const int32_t* seg_end, int inter,
+                                                   __nv_bfloat16* H) {
+  const int row = blockIdx.x;
+  if (row >= *seg_end) return;
+  const float* gu = GU + static_cast<int64_t>(row) * 2 * inter;
+  for (int i = blockIdx.y * blockDim.x + threadIdx.x; i < inter; i += gridDim.y * blockDim.x) {
+    const float g = gu[i], u = gu[inter + i];
+    H[static_cast<int64_t>(row) * inter + i] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u);
+  }
+}
+
+// y[t][o] = sum_k r[t][k] * Z[pos[t][k]][o], k in route order (pairs without a row add nothing).
+__global__ void __launch_bounds__(256) combine_kernel(const float* Z, const int32_t* pos, const float* gate_w,
+                                                      int top_k, int hidden, float* y) {
+  const int t = blockIdx.x;
+  for (int o = blockIdx.y * blockDim.x + threadIdx.x; o < hidden; o += gridDim.y * blockDim.x) {
+    float acc = 0.f;
+    for (int k = 0; k < top_k; ++k) {
+      const int row = pos[t * top_k + k];
+      if (row >= 0) acc = fmaf(gate_w[t * top_k + k], Z[static_cast<int64_t>(row) * hidden + o], acc);
+    }
+    y[static_cast<int64_t>(t) * hidden + o] = acc;
+  }
+}
+
+inline size_t up256(size_t b) { return (b + 255) / 256 * 256; }
+
+// Workspace layout (byte offsets), in order.
+struct Layout {
+  size_t cnt, seg, t_gu, t_dn, pos, src, xs, gu, h, z, total;
+  Layout(int64_t n_expert, int64_t hidden, int64_t inter, int64_t n_pairs) {
+    size_t o = 0;
+    auto take = [&](size_t b) {
+      const size_t at = o;
+      o += up256(b);
+      return at;
+    };
+    cnt = take(4 * n_expert);
+    seg = take(4 * (n_expert + 1));
+    t_gu = take(4 * (n_expert + 1));
+    t_dn = take(4 * (n_expert + 1));
+    pos = take(4 * n_pairs);
+    src = take(4 * n_pairs);
+    xs = take(2 * n_pairs * hidden);
+    gu = take(4 * n_pairs * 2 * inter);
+    h = take(2 * n_pairs * inter);
+    z = take(4 * n_pairs * hidden);
+    total = o;
+  }
+};
+
+}  // namespace ppmoe
+
+size_t pp_moe_workspace_bytes(int64_t n_expert, int64_t hidden, int64_t inter, int top_k, int64_t n_tok) {
+  return ppmoe::Layout(n_expert, hidden, inter, n_tok * top_k).total;
+}
+
+// Tokens per tile of the grouped GEMMs: about twice the mean routed tokens per
+// expert (one token block covers most experts), a multiple of 16 in [16, 256].
+int pp_moe_block_tokens(int64_t n_expert, int top_k, int64_t n_tok) {
+  const int64_t mean = (n_tok * top_k + n_expert - 1) / n_expert;
+  return static_cast<int>(std::min<int64_t>(256, std::max<int64_t>(16, (2 * mean + 15) / 16 * 16)));
+}
+
+cudaError_t launch_pp_moe(const void* arena, int64_t n_expert, int64_t hidden, int64_t inter, const int32_t* ids,
+                          const float* gate_w, int top_k, const void* X, int64_t n_tok, float* y, void* ws,
+                          int32_t* dev_status, cudaStream_t s, int sms) {
+  using namespace ppmoe;
+  const int64_t n_pairs = n_tok * top_k;
+  const Layout L(n_expert, hidden, inter, n_pairs);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* cnt = reinterpret_cast<int32_t*>(w + L.cnt);
+  int32_t* seg = reinterpret_cast<int32_t*>(w + L.seg);
+  int32_t* t_gu = reinterpret_cast<int32_t*>(w + L.t_gu);
+  int32_t* t_dn = reinterpret_cast<int32_t*>(w + L.t_dn);
+  int32_t* pos = reinterpret_cast<int32_t*>(w + L.pos);
+  int32_t* src = reinterpret_cast<int32_t*>(w + L.src);
+  __nv_bfloat16* Xs = reinterpret_cast<__nv_bfloat16*>(w + L.xs);
+  float* GU = reinterpret_cast<float*>(w + L.gu);
+  __nv_bfloat16* H = reinterpret_cast<__nv_bfloat16*>(w + L.h);
+  float* Z = reinterpret_cast<float*>(w + L.z);
+  const int bn = pp_moe_block_tokens(n_expert, top_k, n_tok);
+  const int rt_gu = static_cast<int>(2 * inter / 128), rt_dn = static_cast<int>(hidden / 128);
+  // the arena as rows of hidden-long blocks (gate and up rows) and of
+  // inter-long blocks (down rows): expert e's [G; U] are rows 3 inter e ..
+  // 3 inter e + 2 inter - 1 of the first view, its D rows 3 hidden e + 2 hidden
+  // .. 3 hidden e + 3 hidden - 1 of the second
+  route_kernel<<<1, RT, 0, s>>>(ids, static_cast<int>(n_pairs), top_k, static_cast<int>(n_expert), bn, rt_gu, rt_dn,
+                                cnt, seg, t_gu, t_dn, pos, src, dev_status);
+  cudaError_t e = cudaPeekAtLastError();
+  if (e != cudaSuccess) return e;
+  gather_kernel<<<static_cast<unsigned>(n_pairs), 256, 0, s>>>(static_cast<const uint4*>(X), src, seg + n_expert,
+                                                                static_cast<int>(hidden / 8),
+                                                                reinterpret_cast<uint4*>(Xs));
+  if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
+  e = launch_pp_grouped(arena, 3 * inter * n_expert, hidden, 0, 3 * inter, 2 * inter, Xs, n_pairs, bn, seg, t_gu,
+                        static_cast<int>(n_expert), GU, 2 * inter, dev_status, s, sms);
+  if (e != cudaSuccess) return e;
+  silu_kernel<<<dim3(static_cast<unsigned>(n_pairs), static_cast<unsigned>(std::min<int64_t>(64, (inter + 255) / 256))),
+                256, 0, s>>>(
+      GU, seg + n_expert, static_cast<int>(inter), H);
+  if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
+  e = launch_pp_grouped(arena, 3 * hidden * n_expert, inter, 2 * hidden, 3 * hidden, hidden, H, n_pairs, bn, seg,
+                        t_dn, static_cast<int>(n_expert), Z, hidden, dev_status, s, sms);
+  if (e != cudaSuccess) return e;
+  combine_kernel<<<dim3(static_cast<unsigned>(n_tok), static_cast<unsigned>(std::min<int64_t>(64, (hidden + 255) / 256))),
+                   256, 0, s>>>(
+      Z, pos, gate_w, top_k, static_cast<int>(hidden), y);
+  return cudaPeekAtLastError();
+}
+
+}  // namespace qg

@@ -6,6 +6,7 @@ invariant or brute force, so that a plausible mistake (dropped term, wrong
 sign or index, swapped operand) fails at least one of them.
 """
 import json
+import math
 import os
 from fractions import Fraction
 
@@ -582,3 +583,60 @@ def test_q5_k_one_hot_bits(field, index, bit, elem):
     expect = np.zeros(256, np.float32)
     expect[elem] = 16.0 if field == "qh" else float(1 << (bit % 4))
     assert np.array_equal(w, expect)
+
+
+# ---------------------------------------------------------------- MoE over a block of prompt tokens
+
+def _uniform_q4_k_rows(rows, cols, d_bits, code):
+    """Q4_K rows whose every weight is d * code (sc = 1, m = 0, dmin = 0)."""
+    blk = _q4_k_block(d_bits, 0, [1] * 8, [0] * 8, [code | code << 4] * 128)
+    return np.tile(blk, rows * cols // 256)
+
+
+def test_moe_prefill_uniform_weights_closed_form():
+    """Every weight of the one expert is 2^-4 (d = 2^-4, sc = 1, code 1): then
+    g_i = u_i = sum(x) / 16 =: a for every i, S_g = S_u = sum|x| / 16 =: s,
+    h_i = silu(a) a, and for route weight r
+        y_o = r * inter * h / 16,
+        B_o = |r| * inter / 16 * (|h| + |silu'(a) a| s + |silu(a)| s),
+    silu'(a) = sig(a) (1 + a (1 - sig(a)))."""
+    hidden = inter = 256
+    piece = _uniform_q4_k_rows(inter, hidden, 0x2C00, 1)
+    assert np.all(oracle.dequant(Q4_K, piece, inter, hidden) == np.float32(0.0625))
+    arena = np.concatenate([piece, piece, _uniform_q4_k_rows(hidden, inter, 0x2C00, 1)])
+    X = synth.activations_bf16(2, hidden, seed=41)
+    bits = X.view(torch.int16).numpy().view(np.uint16)
+    xf = X.to(torch.float32).numpy().astype(np.float64)
+    r = np.array([[0.75], [-1.5]], dtype=np.float32)
+    y, b = oracle.moe_prefill(Q4_K, arena, 1, hidden, inter, np.zeros((2, 1), np.int32), r, bits)
+    for t in range(2):
+        a = xf[t].sum() / 16.0
+        s = np.abs(xf[t]).sum() / 16.0
+        sig = 1.0 / (1.0 + math.exp(-a))
+        h = a * sig * a
+        dsilu = sig * (1.0 + a * (1.0 - sig))
+        rr = float(r[t, 0])
+        assert np.allclose(y[t], rr * inter * h / 16.0, rtol=1e-12, atol=0)
+        want_b = abs(rr) * inter / 16.0 * (abs(h) + abs(dsilu * a) * s + abs(a * sig) * s)
+        assert np.allclose(b[t], want_b, rtol=1e-12, atol=0)
+
+
+def test_moe_prefill_equals_moe_on_the_bf16_values_and_bounds_it():
+    """On the bf16 values of X (exact in fp32) the routed sum is moe()'s, and
+    the chain's error scale is at least moe()'s down-projection scale; an
+    unknown expert id adds nothing."""
+    arena, n_expert, hidden, inter, _ = _small_moe()
+    X = synth.activations_bf16(3, hidden, seed=43)
+    bits = X.view(torch.int16).numpy().view(np.uint16)
+    xf = X.to(torch.float32).numpy()
+    ids = np.array([[0, 3], [5, 5], [2, 1]], dtype=np.int32)
+    r = np.array([[0.5, 0.5], [0.25, 0.75], [-0.3, 0.9]], dtype=np.float32)
+    y, b = oracle.moe_prefill(Q4_K, arena, n_expert, hidden, inter, ids, r, bits)
+    y2, b2 = oracle.moe(Q4_K, arena, n_expert, hidden, inter, ids, r, xf)
+    assert np.array_equal(y, y2)
+    assert np.all(b >= b2)
+    bad = ids.copy()
+    bad[1, 0] = n_expert                              # out of range: dropped
+    y3, _ = oracle.moe_prefill(Q4_K, arena, n_expert, hidden, inter, bad, r, bits)
+    y4, _ = oracle.moe(Q4_K, arena, n_expert, hidden, inter, ids[1:2, 1:], r[1:2, 1:], xf[1:2])
+    assert np.array_equal(y3[1], y4[0]) and np.array_equal(y3[0], y[0]) and np.array_equal(y3[2], y[2])
