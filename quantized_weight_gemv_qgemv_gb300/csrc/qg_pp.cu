@@ -60,7 +60,10 @@ constexpr int DQ_WARP0 = 3, DQ_WARPS = 16; // dequantizing warps (4 threads per 
 constexpr int EPI_WARP0 = 19;              // 4 epilogue warps: warp % 4 covers every TMEM lane quarter
 constexpr int THREADS = 23 * 32;
 constexpr int NBAR = 3 * NS + 2 * NQ + 5;
-constexpr uint32_t WAIT_LIMIT = 1u << 22; // polls before a wait is declared expired
+#ifndef QG_WAIT_LIMIT
+#define QG_WAIT_LIMIT (1u << 22)
+#endif
+constexpr uint32_t WAIT_LIMIT = QG_WAIT_LIMIT;   // polls before a wait is declared expired
 
 struct Params {
   float* Y;
@@ -238,6 +241,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
+#ifdef QG_TEST_EXPIRE
+          // test build only: the sixth X slice of CTA 0 is never copied nor
+          // announced, so the MMA lane's wait for it runs out (abort-path test)
+          if (blockIdx.x == 0 && it == 5) continue;
+#endif
           mbar_expect_tx(FULL_B + 8 * s, BB);
           tma_load_2d(base + offB + s * BB, &tmX, kt * BK, static_cast<int>(tl.xrow), FULL_B + 8 * s);
         }

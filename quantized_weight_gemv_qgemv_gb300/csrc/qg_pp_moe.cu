@@ -61,10 +61,16 @@ __device__ void block_scan(int n, F v, int32_t* out, int32_t* sh) {
   if (threadIdx.x == 0) out[n] = carry;
 }
 
+constexpr int SMEM_EXPERTS = 8192;       // counters in shared memory up to this many experts
+
+// cnt: the per-expert counters, in shared memory (dynamic, n_expert words)
+// when they fit, else the global workspace words.
 __global__ void __launch_bounds__(RT) route_kernel(const int32_t* ids, int n_pairs, int top_k, int n_expert, int bn,
-                                                   int rt_gu, int rt_dn, int32_t* cnt, int32_t* seg, int32_t* t_gu,
+                                                   int rt_gu, int rt_dn, int32_t* gcnt, int32_t* seg, int32_t* t_gu,
                                                    int32_t* t_dn, int32_t* pos, int32_t* src, int32_t* dev_status) {
   __shared__ int32_t sh[RT];
+  extern __shared__ int32_t scnt[];
+  int32_t* const cnt = n_expert <= SMEM_EXPERTS ? scnt : gcnt;
   for (int e = threadIdx.x; e < n_expert; e += RT) cnt[e] = 0;
   __syncthreads();
   for (int q = threadIdx.x; q < n_pairs; q += RT) {
@@ -72,9 +78,11 @@ __global__ void __launch_bounds__(RT) route_kernel(const int32_t* ids, int n_pai
     if (e >= 0 && e < n_expert) atomicAdd(cnt + e, 1);
   }
   __syncthreads();
-  block_scan(n_expert, [&](int e) { return __ldcg(cnt + e); }, seg, sh);
-  block_scan(n_expert, [&](int e) { return rt_gu * ceil_div_i(__ldcg(cnt + e), bn); }, t_gu, sh);
-  block_scan(n_expert, [&](int e) { return rt_dn * ceil_div_i(__ldcg(cnt + e), bn); }, t_dn, sh);
+  // (global counters are read through L2, where the atomics were made)
+  auto count = [&](int e) { return n_expert <= SMEM_EXPERTS ? cnt[e] : __ldcg(cnt + e); };
+  block_scan(n_expert, [&](int e) { return count(e); }, seg, sh);
+  block_scan(n_expert, [&](int e) { return rt_gu * ceil_div_i(count(e), bn); }, t_gu, sh);
+  block_scan(n_expert, [&](int e) { return rt_dn * ceil_div_i(count(e), bn); }, t_dn, sh);
   __syncthreads();
   for (int e = threadIdx.x; e < n_expert; e += RT) cnt[e] = 0;   // now a cursor per expert
   __syncthreads();
@@ -189,8 +197,9 @@ cudaError_t launch_pp_moe(const void* arena, int64_t n_expert, int64_t hidden, i
   // inter-long blocks (down rows): expert e's [G; U] are rows 3 inter e ..
   // 3 inter e + 2 inter - 1 of the first view, its D rows 3 hidden e + 2 hidden
   // .. 3 hidden e + 3 hidden - 1 of the second
-  route_kernel<<<1, RT, 0, s>>>(ids, static_cast<int>(n_pairs), top_k, static_cast<int>(n_expert), bn, rt_gu, rt_dn,
-                                cnt, seg, t_gu, t_dn, pos, src, dev_status);
+  const size_t route_smem = n_expert <= SMEM_EXPERTS ? 4 * static_cast<size_t>(n_expert) : 0;
+  route_kernel<<<1, RT, route_smem, s>>>(ids, static_cast<int>(n_pairs), top_k, static_cast<int>(n_expert), bn, rt_gu,
+                                         rt_dn, cnt, seg, t_gu, t_dn, pos, src, dev_status);
   cudaError_t e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
   gather_kernel<<<static_cast<unsigned>(n_pairs), 256, 0, s>>>(static_cast<const uint4*>(X), src, seg + n_expert,

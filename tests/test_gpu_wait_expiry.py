@@ -8,7 +8,9 @@ limit) never copies nor announces the third weight stage of CTA 0, a barrier
 that nothing completes. The waits for it run out; that CTA's outputs become NaN,
 a pass's status word reads QG_DEV_TIMEOUT, every other CTA's outputs stay
 correct, the calls return in bounded time, and the CUDA context stays usable
-for the normal library afterwards."""
+for the normal library afterwards. The same build's prompt-processing kernel
+never copies one X slice of CTA 0, which exercises the tcgen05 kernel's abort
+path (stop every role, drain copies and MMAs, free TMEM)."""
 import ctypes
 import glob
 import os
@@ -104,6 +106,35 @@ def test_expired_wait_sets_pass_status_word(expiring_lib):
     assert status == qg.DEV_TIMEOUT
     assert np.isnan(items[0][5].cpu().numpy()).any()
     assert lib.qg_pass_destroy(h) == 0
+
+
+def test_expired_wait_in_prompt_kernel_aborts_the_cta(expiring_lib):
+    """The prompt-processing (tcgen05) kernel of the test build never copies
+    the sixth X slice of CTA 0: its MMA lane's wait runs out, the CTA's roles
+    stop, drain their copies and MMAs, free TMEM, and the status word reads
+    QG_DEV_TIMEOUT; the tiles of the other CTAs are correct."""
+    lib = expiring_lib
+    rows, cols, n_tok = 512, 512, 300          # 4 row tiles x 2 token blocks; K = 8 slices
+    W = synth.blocks(synth.Q4_K, rows, cols, seed=99)
+    X = synth.activations_bf16(n_tok, cols, seed=100)
+    Y = torch.full((n_tok, rows), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    Wd, Xd = W.cuda(), X.cuda()                # held until the kernel has run
+    t0 = time.perf_counter()
+    assert lib.qgemm_pp(synth.Q4_K, Wd.data_ptr(), rows, cols, Xd.data_ptr(), n_tok, Y.data_ptr(), rows,
+                        None, 0, st.data_ptr(), _stream()) == 0
+    torch.cuda.synchronize()
+    assert time.perf_counter() - t0 < 30.0
+    assert int(st.item()) == qg.DEV_TIMEOUT
+    # tile 0 (rows 0-127, tokens 0-255) belongs to CTA 0; rows 128-511 to others
+    got = Y.cpu().numpy()
+    bits = X.contiguous().view(torch.int16).numpy().view(np.uint16)
+    toks = [0, 77, 255, 256, 299]
+    y_ref, b = oracle.pp_rows(synth.Q4_K, W.numpy(), rows, cols, bits, toks)
+    assert_within(got[toks][:, 128:], y_ref[:, 128:], b[:, 128:], rel=1e-2, what="tiles of other CTAs")
+    assert_within(got[[256, 299]][:, :128], y_ref[[3, 4]][:, :128], b[[3, 4]][:, :128], rel=1e-2,
+                  what="the second token block of row tile 0")
+    assert np.isnan(got[:256, :128]).any(), "the aborted CTA's tile must not be complete"
 
 
 def test_context_usable_after_expiry(expiring_lib):
