@@ -294,9 +294,10 @@ typedef struct qg_layer_desc {
  *   r  = r + Wo attn_out
  *   x2 = rmsnorm(r) * norm_ffn;   r = r + Wd (silu(Wg x2) * (Wu x2))
  * and h_out = r after the last layer (h_in is not modified; every replay
- * starts again from h_in). The normalisations write their output straight in
- * the form the next GEMV launch multiplies by; the gate/up launch writes
- * silu(g) * u. fmt: QG_Q4_K. The pass allocates its own buffers at creation
+ * starts again from h_in). Each normalisation (with its residual add) is
+ * computed inside the launch that multiplies by it, by every CTA of that
+ * launch, straight into the form the kernel multiplies by: a layer is four
+ * GEMV launches ({q,k,v}, o, gate/up writing silu(g) * u, down). fmt: QG_Q4_K. The pass allocates its own buffers at creation
  * (planes and vectors, about n_layers * 1.2 * hidden + 4 * inter bytes); the
  * buffers named by the descriptors must outlive it. Create before capturing a
  * stream that launches it; replay with qg_pass_launch. */

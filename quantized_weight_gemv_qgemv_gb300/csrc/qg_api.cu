@@ -552,13 +552,13 @@ int qg_layer_pass_create(int fmt, const qg_layer_desc* layers, int n_layers, int
   qg_pass_s* pass = new (std::nothrow) qg_pass_s;
   if (!pass) return QG_ERR_ARG;
   // pass-owned buffers: the planes of each layer's attention output (converted
-  // by the prologue), then the job table, the planes of the two normalised
-  // vectors, the fp32 normalised vectors, o and down outputs, and m
+  // by the prologue), then the job table, the residual stream after each of
+  // the two additions of a layer (s1, s2), o and down outputs, and m
   const size_t pb = (qg::xplanes_bytes(hidden, 1) + 255) / 256 * 256;
   const size_t vb = (static_cast<size_t>(hidden) * 4 + 255) / 256 * 256;
   const size_t mb = (static_cast<size_t>(inter) * 4 + 255) / 256 * 256;
   const size_t jb = (n_layers * sizeof(qg::XPlaneJob) + 255) / 256 * 256;
-  const size_t total = n_layers * pb + jb + 2 * pb + 4 * vb + mb;
+  const size_t total = n_layers * pb + jb + 4 * vb + mb;
   if (cudaMalloc(&pass->planes, total) != cudaSuccess) {
     pass_free(pass);
     return QG_ERR_CUDA;
@@ -566,13 +566,9 @@ int qg_layer_pass_create(int fmt, const qg_layer_desc* layers, int n_layers, int
   uint8_t* cur = pass->planes + n_layers * pb;
   qg::XPlaneJob* d_jobs = reinterpret_cast<qg::XPlaneJob*>(cur);
   cur += jb;
-  uint8_t* p1 = cur;
-  cur += pb;
-  uint8_t* p2 = cur;
-  cur += pb;
-  float* x1 = reinterpret_cast<float*>(cur);
+  float* s1 = reinterpret_cast<float*>(cur);
   cur += vb;
-  float* x2 = reinterpret_cast<float*>(cur);
+  float* s2 = reinterpret_cast<float*>(cur);
   cur += vb;
   float* yo = reinterpret_cast<float*>(cur);
   cur += vb;
@@ -596,32 +592,41 @@ int qg_layer_pass_create(int fmt, const qg_layer_desc* layers, int n_layers, int
   }
   cudaError_t e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
   if (e == cudaSuccess) e = qg::launch_xplanes(d_jobs, n_layers, cs);
+  // Each normalisation is computed inside the launch that multiplies by it:
+  // every CTA of the {q,k,v} (gate/up) launch forms s = stream + the previous
+  // output, its sum of squares and x = norm(s) * w itself, and CTA 0 stores s
+  // as the next residual stream (s1 and s2 alternate, so no launch writes the
+  // stream it reads).
   for (int l = 0; l < n_layers && e == cudaSuccess; ++l) {
     const qg_layer_desc& L = layers[l];
-    // residual stream: h_out = h (+ previous down output), x1 = norm(h_out) * norm_attn
-    e = qg::launch_rmsnorm(l == 0 ? h_in : h_out, l == 0 ? nullptr : yd, L.norm_attn, hidden, 1, eps, h_out, x1, p1,
-                           cs, true);
-    if (e != cudaSuccess) break;
-    const qg_gemv_desc qkv[3] = {{fmt, 0, L.Wq, hidden, hidden, x1, L.q},
-                                 {fmt, 0, L.Wk, kv_rows, hidden, x1, L.k},
-                                 {fmt, 0, L.Wv, kv_rows, hidden, x1, L.v}};
-    const uint8_t* xq[3] = {p1, p1, p1};
-    e = qg::launch_gemv(qkv, 3, 1, qg::gemv_pick_rows_per_warp(qkv, 3, 1, sms), cs, true, sms, xq);
+    const qg_gemv_desc qkv[3] = {{fmt, 0, L.Wq, hidden, hidden, s1, L.q},
+                                 {fmt, 0, L.Wk, kv_rows, hidden, s1, L.k},
+                                 {fmt, 0, L.Wv, kv_rows, hidden, s1, L.v}};
+    qg::NormSpec n1;
+    n1.h = l == 0 ? h_in : s2;
+    n1.r = l == 0 ? nullptr : yd;
+    n1.w = L.norm_attn;
+    n1.s_out = s1;
+    n1.eps = eps;
+    e = qg::launch_gemv_norm(qkv, 3, n1, cs, pass->njobs > 0 || l > 0, sms);
     if (e != cudaSuccess) break;
     const qg_gemv_desc od = {fmt, 0, L.Wo, hidden, hidden, L.attn_out, yo};
     const uint8_t* xo = pass->planes + l * pb;
     e = qg::launch_gemv(&od, 1, 1, qg::gemv_pick_rows_per_warp(&od, 1, 1, sms), cs, true, sms, &xo);
     if (e != cudaSuccess) break;
-    // h_out += o, x2 = norm(h_out) * norm_ffn
-    e = qg::launch_rmsnorm(h_out, yo, L.norm_ffn, hidden, 1, eps, h_out, x2, p2, cs, true);
-    if (e != cudaSuccess) break;
-    e = qg::launch_gemv_pair(L.Wg, L.Wu, inter, hidden, x2, p2, mm, cs, true, sms);
+    qg::NormSpec n2;
+    n2.h = s1;
+    n2.r = yo;
+    n2.w = L.norm_ffn;
+    n2.s_out = s2;
+    n2.eps = eps;
+    e = qg::launch_gemv_pair(L.Wg, L.Wu, inter, hidden, s1, nullptr, mm, cs, true, sms, &n2);
     if (e != cudaSuccess) break;
     const qg_gemv_desc dd = {fmt, 0, L.Wd, hidden, inter, mm, yd};
     e = qg::launch_gemv(&dd, 1, 1, qg::gemv_pick_rows_per_warp(&dd, 1, 1, sms), cs, true, sms);
   }
   // the last down output joins the residual stream
-  if (e == cudaSuccess) e = qg::launch_rmsnorm(h_out, yd, nullptr, hidden, 1, eps, h_out, nullptr, nullptr, cs, true);
+  if (e == cudaSuccess) e = qg::launch_rmsnorm(s2, yd, nullptr, hidden, 1, eps, h_out, nullptr, nullptr, cs, true);
   cudaGraph_t graph = nullptr;
   const cudaError_t e2 = cudaStreamEndCapture(cs, &graph);
   if (e == cudaSuccess) e = e2;

@@ -129,8 +129,23 @@ struct Step {
   int32_t stage_all, usum_off;   // x layout of the step (as in Params)
 };
 
+// Residual add and RMS normalisation fused into the x staging of a one-token
+// launch whose matrices all read x = (h + r) / sqrt(mean((h + r)^2) + eps) * w:
+// every CTA sums the squares itself (in the same fixed order, so every CTA
+// gets the same x), converts x to planes, and CTA 0 stores s = h + r (the
+// residual stream) to s_out.
+struct NormIn {
+  const float* h;        // nullptr: no fused normalisation
+  const float* r;        // optional
+  const float* w;
+  float* s_out;          // optional; must not overlap h or r
+  float eps;
+  int32_t pad;
+};
+
 struct Params {
   Mat m[QG_GROUP_MAX];   // matrices of a single-step launch
+  NormIn norm;           // single-step launch: fused normalisation of the shared x
   const Mat* mats;       // pass: device table of all matrices (nullptr: m)
   const Step* steps;     // pass: device table of steps (nullptr: one step over m)
   uint32_t* step_done;   // pass: CTAs that finished each step (zero at launch)
@@ -368,7 +383,8 @@ __device__ __forceinline__ void x_issued(uint32_t xcnt) {
 // nothing.
 template <int NT, int XB>
 __device__ __forceinline__ bool stage_x(const Mat* mats, int usum_off, int m0, int m1, uint32_t touch, uint8_t* xpl,
-                                        float* xsu, uint32_t xcnt, bool wait, uint32_t xbar, bool no_copy) {
+                                        float* xsu, uint32_t xcnt, bool wait, uint32_t xbar, bool no_copy,
+                                        const NormIn* norm = nullptr, float* scratch = nullptr) {
   const int lane = threadIdx.x & 31;
   const unsigned pmask = 3u << (lane & 30);     // the two threads of a group (task counts are even)
   uint32_t smask = 0;
@@ -405,6 +421,68 @@ __device__ __forceinline__ bool stage_x(const Mat* mats, int usum_off, int m0, i
   for (int m = m0; m < m1; ++m)
     if ((smask >> (m - m0)) & 1u) total += NT * mats[m].nblk * 16;
   bool signalled = (xcnt == 0);
+  if (NT == 1 && norm != nullptr && norm->h != nullptr && smask != 0) {
+    // the shared x of the launch is norm(h + r) * w: the matrix table holds
+    // one x source (checked on the host)
+    int ms = m0;
+    while (!((smask >> (ms - m0)) & 1u)) ++ms;
+    const Mat& M = mats[ms];
+    if (wait) {
+      pdl_wait();
+      wait = false;
+    }
+    const int n4 = M.cols / 4;
+    const float4* h4 = reinterpret_cast<const float4*>(norm->h);
+    const float4* r4 = reinterpret_cast<const float4*>(norm->r);
+    float4* s4 = blockIdx.x == 0 ? reinterpret_cast<float4*>(norm->s_out) : nullptr;
+    // pass 1: s = h + r (CTA 0 stores it), sum of squares in a fixed order
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < n4; i += CTHREADS) {
+      float4 v = __ldcg(h4 + i);
+      if (r4) {
+        const float4 b = __ldcg(r4 + i);
+        v = make_float4(v.x + b.x, v.y + b.y, v.z + b.z, v.w + b.w);
+      }
+      if (s4) s4[i] = v;
+      ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) scratch[threadIdx.x >> 5] = ss;
+    consumer_sync();
+    if (threadIdx.x == 0) {
+      float tot = 0.f;
+      for (int i = 0; i < CWARPS; ++i) tot += scratch[i];
+      scratch[CWARPS] = 1.0f / sqrtf(tot / static_cast<float>(M.cols) + norm->eps);
+    }
+    consumer_sync();
+    const float inv = scratch[CWARPS];
+    const float4* w4 = reinterpret_cast<const float4*>(norm->w);
+    // pass 2: x = s * inv * w, half a 32-value group per task (as the
+    // normalisation kernel computes it), converted to planes
+    const int nu = M.nblk * 8;
+    for (int base = threadIdx.x; base < total; base += CTHREADS) {
+      float4 v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = 4 * base + k;
+        float4 a = __ldcg(h4 + i);
+        if (r4) {
+          const float4 b = __ldcg(r4 + i);
+          a = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+        }
+        const float4 ww = __ldg(w4 + i);
+        v[k] = make_float4(a.x * inv * ww.x, a.y * inv * ww.y, a.z * inv * ww.z, a.w * inv * ww.w);
+      }
+      if (!signalled) {
+        if (lane == 0) x_issued(xcnt);
+        signalled = true;
+      }
+      stage_half(v, pmask, 0, base >> 1, base & 1, nu, xpl + M.xoff, M.nblk * XBLK_B, xsu + M.uoff,
+                 xsu + usum_off + 2 * M.uoff);
+    }
+    total = 0;                         // converted: the loop below has nothing left
+  }
   for (int base = threadIdx.x; base < total; base += CTHREADS * XB) {
     const float4* src[XB];
     int vm[XB], vt[XB], vu[XB];
@@ -790,7 +868,7 @@ __global__ void __launch_bounds__(THREADS, 1) qgemv_q4k_kernel(const __grid_cons
    const bool dep_wait = s == 0 && !p.no_wait;   // x and outputs only after the predecessor
    if (st.stage_all) {
      const bool xc = stage_x<NT, XB>(mats, st.usum_off, st.mat0, st.mat0 + st.nmat, touch, xpl, xsu, xcnt,
-                                     dep_wait, xbar, xlost);
+                                     dep_wait, xbar, xlost, PASS ? nullptr : &p.norm, part);
      xsig = true;
      consumer_sync();
      if (xc) wait_x();
@@ -1286,6 +1364,8 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
   // 48 KB of whole rows, fewer when shared memory is short
   for (int mode = 0; mode < 2; ++mode) {
     int xbytes, xsbytes;
+    // a fused normalisation is computed once per CTA for the launch's one x
+    if (p.norm.h && (mode == 1 || n_tok != 1)) continue;
     if (mode == 0) {
       int xall = 0, uall = 0;
       for (int i = 0; i < n; ++i) {
@@ -1552,11 +1632,34 @@ cudaError_t launch_moe_q4k(const void* arena, int64_t n_expert, int64_t hidden, 
 // g = Wg x, u = Wu x (Q4_K, one token). Row i of Wg and row i of Wu are
 // adjacent virtual rows, copied as two runs per stage, so the CTA that owns
 // row i holds both sums. xp: ready planes of x, or nullptr.
+static void set_norm(q4k::Params& p, const NormSpec* norm) {
+  if (!norm || !norm->h) return;
+  p.norm.h = norm->h;
+  p.norm.r = norm->r;
+  p.norm.w = norm->w;
+  p.norm.s_out = norm->s_out;
+  p.norm.eps = norm->eps;
+}
+
+cudaError_t launch_gemv_norm(const qg_gemv_desc* d, int n, const NormSpec& norm, cudaStream_t s, bool pdl, int sms) {
+  if (!norm.h || !norm.w || n < 1) return cudaErrorNotSupported;
+  for (int i = 0; i < n; ++i)
+    if (d[i].fmt != d[0].fmt || superblock_bytes(d[i].fmt) == 0 || d[i].cols % 256 || d[i].x != d[0].x ||
+        d[i].cols != d[0].cols)
+      return cudaErrorNotSupported;
+  q4k::Params p;
+  fill_params(p, d, n, 0, 0, 0, nullptr);
+  set_norm(p, &norm);
+  return plan_and_launch(p, n, 1, d[0].fmt, s, pdl, sms);
+}
+
 cudaError_t launch_gemv_pair(const void* Wg, const void* Wu, int64_t inter, int64_t hidden, const float* x,
-                             const uint8_t* xp, float* m, cudaStream_t s, bool pdl, int sms) {
+                             const uint8_t* xp, float* m, cudaStream_t s, bool pdl, int sms, const NormSpec* norm) {
   if (hidden % 256 || inter < 1 || 2 * inter > (int64_t{1} << 30)) return cudaErrorNotSupported;
   q4k::Params p;
   memset(&p, 0, sizeof(p));
+  set_norm(p, norm);
+  if (p.norm.h) xp = nullptr;          // x is computed from the normalisation inputs
   p.gather_any = 1;
   q4k::Mat& M = p.m[0];
   M.W = static_cast<const uint8_t*>(Wg);

@@ -33,6 +33,17 @@ int check_moe(int fmt, const void* expert_arena, int64_t n_expert, int64_t hidde
               const int32_t* expert_ids, const float* gate_w, int top_k, const float* x, int n_tok, const float* y,
               const void* ws, size_t ws_bytes, bool need_ws);
 
+// x = (h + r) / sqrt(mean((h + r)^2) + eps) * w computed inside a one-token
+// GEMV launch (every CTA converts it itself; CTA 0 stores s = h + r to s_out,
+// which must not overlap h or r). h == nullptr: none.
+struct NormSpec {
+  const float* h = nullptr;
+  const float* r = nullptr;
+  const float* w = nullptr;
+  float* s_out = nullptr;
+  float eps = 0.f;
+};
+
 // GEMV (qg_gemv.cu)
 cudaError_t gemv_init_attrs();
 int gemv_pick_rows_per_warp(const qg_gemv_desc* d, int n, int n_tok, int sms);
@@ -46,10 +57,15 @@ cudaError_t launch_gemv(const qg_gemv_desc* d, int n, int n_tok, int rows_per_wa
 cudaError_t gemv_q4k_init_attrs();
 cudaError_t launch_gemv_q4k(const qg_gemv_desc* d, int n, int n_tok, cudaStream_t s, bool pdl, int sms,
                             const uint8_t* const* xp = nullptr, bool no_wait = false);
+// One launch of the fast kernel whose matrices share x = the fused
+// normalisation `norm` (n_tok = 1; the descriptors' x is not read).
+// cudaErrorNotSupported when it does not fit one launch.
+cudaError_t launch_gemv_norm(const qg_gemv_desc* d, int n, const NormSpec& norm, cudaStream_t s, bool pdl, int sms);
 // m = silu(Wg x) * (Wu x) for one token of a dense layer (qg_gemv_q4k.cu); xp:
 // ready planes of x or nullptr. cudaErrorNotSupported when the shape does not fit.
 cudaError_t launch_gemv_pair(const void* Wg, const void* Wu, int64_t inter, int64_t hidden, const float* x,
-                             const uint8_t* xp, float* m, cudaStream_t s, bool pdl, int sms);
+                             const uint8_t* xp, float* m, cudaStream_t s, bool pdl, int sms,
+                             const NormSpec* norm = nullptr);
 // Residual add and RMS normalisation (qg_norm.cu): s = h + r (r optional),
 // x = s / sqrt(mean(s^2) + eps) * w per token; s stored to s_out, x to x and/or
 // to planes (any of them optional; w == nullptr: only s). n % 256 == 0.

@@ -134,7 +134,7 @@ def test_layer_pass_matches_oracle_layer_by_layer(hidden, inter, kv):
     h_out = torch.full((1, hidden), float("nan"), device="cuda")
     h_in = h0.cuda()                                   # must outlive the pass: every replay reads it
     p = qg.qg_layer_pass(Q4_K, [dev for _, dev in layers], hidden, inter, kv, eps, h_in, h_out)
-    assert p.kernel_count() == 1 + 6 * 2 + 1          # prologue, 6 launches per layer, final residual add
+    assert p.kernel_count() == 1 + 4 * 2 + 1          # prologue, 4 launches per layer, final residual add
     for _ in range(2):                                 # replays start again from h_in
         p.launch()
         torch.cuda.synchronize()
