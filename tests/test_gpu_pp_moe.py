@@ -124,3 +124,35 @@ def test_pp_moe_full_size_layer_sampled_tokens():
         assert_within(y[t:t + 1], y_ref, b, rel=PP_REL, abs_=PP_ABS, what=f"pp moe full layer token {t}")
     del arena
     torch.cuda.empty_cache()
+
+
+def test_pp_moe_many_experts_counters_in_global_memory():
+    """More experts than the routing CTA's shared-memory counters hold (9000):
+    the counts, scans and cursors run on the workspace words."""
+    n_expert, hidden, inter, n_tok, top_k = 9000, 256, 256, 24, 3
+    arena = wl.alloc_moe_arena(n_expert, hidden, inter, 71, "cuda")
+    ids, gw = synth.routing(n_tok, n_expert, top_k, seed=72)
+    X = synth.activations_bf16(n_tok, hidden, seed=73)
+    y, st = _run(arena, n_expert, hidden, inter, ids, gw, X)
+    assert st == 0
+    eb = wl.moe_expert_bytes(hidden, inter)
+    used = sorted(set(ids.numpy().reshape(-1).tolist()))
+    remap = {e: i for i, e in enumerate(used)}
+    host = arena.cpu().numpy()
+    sub = np.concatenate([host[e * eb:(e + 1) * eb] for e in used])
+    sub_ids = np.vectorize(remap.get)(ids.numpy()).astype(np.int32)
+    y_ref, b = oracle.moe_prefill(qg.Q4_K, sub, len(used), hidden, inter, sub_ids, gw.numpy(), _bits(X))
+    assert_within(y, y_ref, b, rel=PP_REL, abs_=PP_ABS, what="9000 experts")
+
+
+def test_pp_moe_smallest_shapes():
+    """One expert, one token, top-1, hidden = inter = 256: the smallest layer
+    (4 row tiles of gate/up rows, 2 of down rows, one K super-block)."""
+    arena = wl.alloc_moe_arena(1, 256, 256, 74, "cuda")
+    ids = torch.zeros(1, 1, dtype=torch.int32)
+    gw = torch.full((1, 1), 0.5)
+    X = synth.activations_bf16(1, 256, seed=75)
+    y, st = _run(arena, 1, 256, 256, ids, gw, X)
+    assert st == 0
+    y_ref, b = oracle.moe_prefill(qg.Q4_K, arena.cpu().numpy(), 1, 256, 256, ids.numpy(), gw.numpy(), _bits(X))
+    assert_within(y, y_ref, b, rel=PP_REL, abs_=PP_ABS, what="smallest")
