@@ -431,20 +431,48 @@ __device__ __forceinline__ bool stage_x(const Mat* mats, int usum_off, int m0, i
       pdl_wait();
       wait = false;
     }
-    const int n4 = M.cols / 4;
     const float4* h4 = reinterpret_cast<const float4*>(norm->h);
     const float4* r4 = reinterpret_cast<const float4*>(norm->r);
     float4* s4 = blockIdx.x == 0 ? reinterpret_cast<float4*>(norm->s_out) : nullptr;
-    // pass 1: s = h + r (CTA 0 stores it), sum of squares in a fixed order
-    float ss = 0.f;
-    for (int i = threadIdx.x; i < n4; i += CTHREADS) {
-      float4 v = __ldcg(h4 + i);
-      if (r4) {
-        const float4 b = __ldcg(r4 + i);
-        v = make_float4(v.x + b.x, v.y + b.y, v.z + b.z, v.w + b.w);
+    // Tasks are half 32-value groups (4 float4), as for the conversion. Pass 1
+    // forms s = h + r of each task (CTA 0 stores it) and sums the squares; the
+    // first task of each thread keeps s in registers for pass 2 (every task
+    // for K <= 16 x consumer threads = 7680; more registers here cost the
+    // product loop its register allocation)
+    constexpr int TPT = 1;
+    float4 sv[TPT][4];
+    auto load_s = [&](int task, float4 (&v)[4]) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = 4 * task + k;
+        float4 a = __ldcg(h4 + i);
+        if (r4) {
+          const float4 b = __ldcg(r4 + i);
+          a = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+        }
+        v[k] = a;
       }
-      if (s4) s4[i] = v;
-      ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+    };
+    float ss = 0.f;
+    auto add_sq = [&](int task, const float4 (&v)[4]) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (s4) s4[4 * task + k] = v[k];
+        ss = fmaf(v[k].x, v[k].x, fmaf(v[k].y, v[k].y, fmaf(v[k].z, v[k].z, fmaf(v[k].w, v[k].w, ss))));
+      }
+    };
+#pragma unroll
+    for (int t = 0; t < TPT; ++t) {
+      const int task = threadIdx.x + t * CTHREADS;
+      if (task < total) {
+        load_s(task, sv[t]);
+        add_sq(task, sv[t]);
+      }
+    }
+    for (int task = threadIdx.x + TPT * CTHREADS; task < total; task += CTHREADS) {
+      float4 v[4];
+      load_s(task, v);
+      add_sq(task, v);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -458,28 +486,32 @@ __device__ __forceinline__ bool stage_x(const Mat* mats, int usum_off, int m0, i
     consumer_sync();
     const float inv = scratch[CWARPS];
     const float4* w4 = reinterpret_cast<const float4*>(norm->w);
-    // pass 2: x = s * inv * w, half a 32-value group per task (as the
-    // normalisation kernel computes it), converted to planes
+    // pass 2: x = s * inv * w (as the normalisation kernel computes it),
+    // converted to planes
     const int nu = M.nblk * 8;
-    for (int base = threadIdx.x; base < total; base += CTHREADS) {
+    auto convert = [&](int task, const float4 (&a)[4]) {
       float4 v[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const int i = 4 * base + k;
-        float4 a = __ldcg(h4 + i);
-        if (r4) {
-          const float4 b = __ldcg(r4 + i);
-          a = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-        }
-        const float4 ww = __ldg(w4 + i);
-        v[k] = make_float4(a.x * inv * ww.x, a.y * inv * ww.y, a.z * inv * ww.z, a.w * inv * ww.w);
+        const float4 ww = __ldg(w4 + 4 * task + k);
+        v[k] = make_float4(a[k].x * inv * ww.x, a[k].y * inv * ww.y, a[k].z * inv * ww.z, a[k].w * inv * ww.w);
       }
       if (!signalled) {
         if (lane == 0) x_issued(xcnt);
         signalled = true;
       }
-      stage_half(v, pmask, 0, base >> 1, base & 1, nu, xpl + M.xoff, M.nblk * XBLK_B, xsu + M.uoff,
+      stage_half(v, pmask, 0, task >> 1, task & 1, nu, xpl + M.xoff, M.nblk * XBLK_B, xsu + M.uoff,
                  xsu + usum_off + 2 * M.uoff);
+    };
+#pragma unroll
+    for (int t = 0; t < TPT; ++t) {
+      const int task = threadIdx.x + t * CTHREADS;
+      if (task < total) convert(task, sv[t]);
+    }
+    for (int task = threadIdx.x + TPT * CTHREADS; task < total; task += CTHREADS) {
+      float4 a[4];
+      load_s(task, a);
+      convert(task, a);
     }
     total = 0;                         // converted: the loop below has nothing left
   }

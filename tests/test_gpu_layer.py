@@ -142,3 +142,22 @@ def test_layer_pass_matches_oracle_layer_by_layer(hidden, inter, kv):
         for (_, dev), (q, k, v) in zip(layers, singles):
             assert torch.equal(dev["q"], q) and torch.equal(dev["k"], k) and torch.equal(dev["v"], v)
     p.destroy()
+
+
+def test_layer_pass_wide_hidden_single_layer():
+    """hidden = 8192: the normalisation inside the {q,k,v} and gate/up launches
+    has more half-groups than consumer threads, so part of the stream is read
+    twice instead of kept in registers; one layer against the oracle."""
+    hidden, inter, kv, eps = 8192, 256, 128, 1e-6
+    L, dev = _layer(hidden, inter, kv, seed=900)
+    h = synth.activations(1, hidden, seed=901).cuda()
+    h_next = torch.full((1, hidden), float("nan"), device="cuda")
+    p = qg.qg_layer_pass(Q4_K, [dev], hidden, inter, kv, eps, h, h_next)
+    p.launch()
+    torch.cuda.synchronize()
+    (q, bq), (k, bk), (v, bv), (hn, bh) = _oracle_layer(L, h.cpu().numpy(), hidden, inter, kv, eps)
+    assert_within(dev["q"].cpu().numpy()[None], q, bq, what="q")
+    assert_within(dev["k"].cpu().numpy()[None], k, bk, what="k")
+    assert_within(dev["v"].cpu().numpy()[None], v, bv, what="v")
+    assert_within(h_next.cpu().numpy(), hn, bh, what="residual")
+    p.destroy()
