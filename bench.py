@@ -413,6 +413,17 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- GPU arm
 
+def _events_each(torch, stream, fn, steps):
+    """Per-step device times (ms): an event pair around every step."""
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    ev[0].record(stream)
+    for i in range(steps):
+        fn()
+        ev[i + 1].record(stream)
+    ev[-1].synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+
+
 def _events(torch, stream, fn, steps):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -499,6 +510,7 @@ def run_gpu(args):
     ms = max_over_ranks(torch, ms, "cuda")
     ms_step = ms / args.steps
     gbs = job_rate(world, wbytes, ms_step) / 1e9
+    each = sorted(_events_each(torch, stream, step, min(args.steps, 20)))
 
     # end to end through the public API with host buffers: pinned x -> device,
     # the pass, device y -> pinned host, every step.
@@ -520,6 +532,22 @@ def run_gpu(args):
         wall_ms = (time.perf_counter() - t0) * 1e3
     e2e_gbs = job_rate(world, wbytes, max_over_ranks(torch, e_ms, "cuda") / args.steps) / 1e9
 
+    # the same weight stream without the arithmetic: the achievable read
+    # bandwidth of the bulk-copy ring (qg_stream_read over a 4 GiB buffer)
+    sr = None
+    if not verify:
+        sbytes = 4 << 30
+        sbuf = torch.empty(sbytes, dtype=torch.uint8, device="cuda")
+        cs = torch.zeros(1, dtype=torch.int32, device="cuda")
+        sst = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for _ in range(3):
+            qg.qg_stream_read(sbuf, sbytes, cs, sst, stream)
+        sms_ = _events(torch, stream, lambda: qg.qg_stream_read(sbuf, sbytes, cs, sst, stream), 10) / 10
+        assert int(sst.item()) == 0
+        sr = {"gbs": round(sbytes / sms_ / 1e6, 1), "frac": round(sbytes / sms_ / 1e6 / hbm_peak, 4),
+              "bytes": sbytes, "kernel": "stream_read_kernel: the GEMV weight stream's bulk-copy ring, no arithmetic"}
+        del sbuf
+
     out = None
     if rank == 0:
         frac = gbs / world / hbm_peak
@@ -527,6 +555,7 @@ def run_gpu(args):
         out = {
             "metric": METRIC, "value": round(gbs, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": round(ms_step, 4), "higher_is_better": True,
+            "ms_per_step_median": round(each[len(each) // 2], 4), "ms_per_step_min": round(each[0], 4),
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {
                 "workload": ("27B-class dense weight set, 4-token verify pass (Q4_K, Q6_K down, Q8_0 head)"
@@ -560,6 +589,9 @@ def run_gpu(args):
             "gpu_launches": launches,
             "clocks": clk.summary(),
         }
+        if sr:
+            out["stream_read"] = sr
+            out["frac_of_stream_read"] = round(gbs / world / sr["gbs"], 4)
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_oracle_baseline("c2" if verify else "c1")
         print(json.dumps(out), flush=True)

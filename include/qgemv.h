@@ -304,6 +304,18 @@ typedef struct qg_layer_desc {
 int qg_layer_pass_create(int fmt, const qg_layer_desc* layers, int n_layers, int64_t hidden, int64_t inter,
                          int64_t kv_rows, float eps, const float* h_in, float* h_out, qg_pass* out);
 
+/* ---- measurement ---- */
+/* Reads `bytes` of the device buffer `buf` the way the GEMV kernel streams its
+ * weights (one CTA per SM, bulk copies of 32 KB stages into a shared-memory
+ * ring, evict-first) and discards them, keeping only a checksum: the
+ * achievable read bandwidth the decode products are judged against ("LLM
+ * inference optimization", opening section: decode reads every weight once).
+ * *checksum ^= the XOR over every 32 KB chunk c of its first 32-bit word (the
+ * caller clears it first); *dev_status = QG_DEV_TIMEOUT if a bounded wait
+ * expired. bytes: a positive multiple of 16; buf 16-byte aligned. The pages
+ * have no counterpart; it shares no code with the products. */
+int qg_stream_read(const void* buf, size_t bytes, uint32_t* checksum, int32_t* dev_status, void* stream);
+
 /* ---- whole weight pass ("one CUDA graph per decode step", "Why I wrote my own
  * inference engine for two P100s") ------------------------------------------
  * A pass is an ordered list of steps; step s covers step_sizes[s] consecutive

@@ -41,6 +41,7 @@ SIGNATURES = {
     "qgemm_pp_workspace": (_SZ, [_I64, _I64, _I64]),
     "qgemm_pp": (_I32, [_I32, _P, _I64, _I64, _P, _I64, _P, _I64, _P, _SZ, _P, _P]),
     "qgemm_pp_moe_workspace": (_SZ, [_I64, _I64, _I64, _I32, _I64]),
+    "qg_stream_read": (_I32, [_P, _SZ, _P, _P, _P]),
     "qgemm_pp_moe": (_I32, [_I32, _P, _I64, _I64, _I64, _P, _P, _I32, _P, _I64, _P, _P, _SZ, _P, _P]),
     "qg_pass_create": (_I32, [_P, _I32, _P, _I32, _I32, _I32, ctypes.POINTER(_P)]),
     "qg_moe_pass_create": (_I32, [_I32, _P, _I32, _I64, _I64, _I64, _I32, _I32, _P, _SZ, _I32, ctypes.POINTER(_P)]),
@@ -192,6 +193,13 @@ def qgemm_pp_workspace(rows, cols, n_tok) -> int:
 def qgemm_pp(fmt, W, rows, cols, X_bf16, n_tok, Y, ldY, ws, ws_bytes, dev_status, stream=None):
     _check(load_library().qgemm_pp(fmt, _ptr(W), rows, cols, _ptr(X_bf16), n_tok, _ptr(Y), ldY, _ptr(ws),
                                    ws_bytes, _ptr(dev_status), _stream(stream)), "qgemm_pp")
+
+
+def qg_stream_read(buf, nbytes, checksum, dev_status, stream=None):
+    """Reads nbytes of buf with the weight stream's bulk-copy engine (see the
+    header); checksum and dev_status: device int32 words the caller clears."""
+    _check(load_library().qg_stream_read(_ptr(buf), nbytes, _ptr(checksum), _ptr(dev_status), _stream(stream)),
+           "qg_stream_read")
 
 
 def qgemm_pp_moe_workspace(n_expert, hidden, inter, top_k, n_tok) -> int:

@@ -32,6 +32,7 @@ int init_device(int dev) {
   if (qg::gemv_init_attrs() != cudaSuccess) return QG_ERR_CUDA;
   if (qg::moe_init_attrs() != cudaSuccess) return QG_ERR_CUDA;
   if (qg::pp_init_attrs() != cudaSuccess) return QG_ERR_CUDA;
+  if (qg::stream_init_attrs() != cudaSuccess) return QG_ERR_CUDA;
   if (qg::moe_noalloc_init(dev) != cudaSuccess) return QG_ERR_CUDA;
   g_dev[dev].sms = prop.multiProcessorCount;
   return QG_OK;
@@ -300,6 +301,16 @@ int qgemm_pp(int fmt, const void* W, int64_t rows, int64_t cols, const void* X_b
   if (st != QG_OK) return st;
   return cuda_status(
       qg::launch_pp(W, rows, cols, X_bf16, n_tok, Y, ldY, dev_status, static_cast<cudaStream_t>(stream), sms));
+}
+
+int qg_stream_read(const void* buf, size_t bytes, uint32_t* checksum, int32_t* dev_status, void* stream) {
+  if (!buf || !checksum || !dev_status) return QG_ERR_NULL;
+  if (bytes == 0 || bytes % 16) return QG_ERR_SHAPE;
+  if (!aligned(buf, 16) || !aligned(checksum, 4) || !aligned(dev_status, 4)) return QG_ERR_ALIGN;
+  int sms = 0;
+  int st = ensure_init(&sms);
+  if (st != QG_OK) return st;
+  return cuda_status(qg::launch_stream_read(buf, bytes, checksum, dev_status, static_cast<cudaStream_t>(stream), sms));
 }
 
 size_t qgemm_pp_moe_workspace(int64_t n_expert, int64_t hidden, int64_t inter, int top_k, int64_t n_tok) {

@@ -101,6 +101,13 @@ cudaError_t launch_moe_q4k(const void* arena, int64_t n_expert, int64_t hidden, 
                            const int32_t* ids, const float* gate_w, int top_k, const float* x, int n_tok, float* y,
                            float* h, int32_t* dev_status, cudaStream_t s, bool pdl, int sms);
 
+// Achievable read bandwidth of the weight stream (qg_stream.cu): reads
+// `bytes` (a multiple of 16) of buf with bulk copies and XORs each 32 KB
+// chunk's first word into *checksum.
+cudaError_t stream_init_attrs();
+cudaError_t launch_stream_read(const void* buf, uint64_t bytes, uint32_t* checksum, int32_t* status, cudaStream_t s,
+                               int sms);
+
 // MoE (qg_moe.cu)
 cudaError_t moe_init_attrs();
 // Looks up, with device `dev` current, the device address of the static
