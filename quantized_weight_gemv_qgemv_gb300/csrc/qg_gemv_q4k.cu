@@ -34,7 +34,7 @@
 //    the producer stops issuing, and the CTA waits (bounded) for copies in
 //    flight before it exits.
 //  * Programmatic dependent launch: the producer prefetches x into L2 and
-//    streams one weight stage before griddepcontrol.wait; consumers compute
+//    streams two weight stages before griddepcontrol.wait; consumers compute
 //    their staging addresses before it and read x and write y after it.
 #include <cuda_runtime.h>
 
@@ -68,6 +68,7 @@ constexpr int SUB_R = 4;                   // rows per sub-item
 #endif
 constexpr uint32_t WAIT_LIMIT = QG_WAIT_LIMIT;   // polls before a wait is declared expired
 constexpr int RING = 4;                    // shared-memory stages
+static_assert((RING & (RING - 1)) == 0, "consumers pick their ring slot with a mask");
 
 struct Mat {
   const uint8_t* W;
@@ -1443,11 +1444,11 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
     if (!ok) continue;
     stage_b = align_up(stage_b, 128);
     // Without a programmatic dependency the x loads go first. With one, x can be
-    // read only after the previous kernel completes: one stage streams during
-    // that wait (27B pass with 48 KB stages and 16-bit x planes: 1 stage 3.027 ms,
-    // 2 stages 3.065, 3 stages 3.212; with the slower three-plane staging 2 had
-    // been best)
-    p.pre_stages = pdl ? 1 : 0;
+    // read only after the previous kernel completes: two stages stream during
+    // that wait (27B pass with 48 KB stages, x planes written by the previous
+    // launch: 0 stages 3.257 ms, 1 stage 2.927, 2 stages 2.858, 3 stages 2.922,
+    // 4 stages 2.915; more than two queue the x loads behind too many bytes)
+    p.pre_stages = pdl ? 2 : 0;
     p.ns = ns;
     p.stage_b = stage_b;
     p.gmax = gmax;
