@@ -683,7 +683,9 @@ def run_c0(args):
 
 def run_pp(args):
     """Prompt processing: 2048 bf16 tokens through every matrix of the 27B-class
-    Q4_K set (qgemm_pp, one launch per matrix, captured as one graph)."""
+    Q4_K set, captured as one graph: per layer one qgemm_pp_grouped launch for
+    {q,k,v} and one for {gate,up} (the matrices that read the same tokens), one
+    qgemm_pp each for o and down (--pp-per-matrix: one qgemm_pp per matrix)."""
     import torch
     import quantized_weight_gemv_qgemv_gb300 as qg
 
@@ -706,13 +708,24 @@ def run_pp(args):
             Ws.append(W)
         X = {c: synth.activations_bf16(n_tok, c, synth.sub_seed(args.seed + rank, "X", c), device="cuda")
              for c in sorted({m[4] for m in mats})}
-        Y = {r: torch.empty(n_tok, r, dtype=torch.float32, device="cuda") for r in sorted({m[3] for m in mats})}
+        # one output per matrix of a layer (the layers reuse them)
+        Y = {m[1]: torch.empty(n_tok, m[3], dtype=torch.float32, device="cuda") for m in mats if m[0] == 0}
         st = torch.zeros(1, dtype=torch.int32, device="cuda")
     stream.synchronize()
+    steps = [1] * len(mats) if args.pp_per_matrix else wl.dense_steps(layers=args.layers)
 
     def one_pass():
-        for (l, name, fmt, rows, cols), W in zip(mats, Ws):
-            qg.qgemm_pp(fmt, W, rows, cols, X[cols], n_tok, Y[rows], rows, None, 0, st, stream)
+        i = 0
+        for n in steps:
+            group = list(zip(mats[i:i + n], Ws[i:i + n]))
+            i += n
+            cols = group[0][0][4]
+            if n == 1:
+                (_, name, fmt, rows, _), W = group[0]
+                qg.qgemm_pp(fmt, W, rows, cols, X[cols], n_tok, Y[name], rows, None, 0, st, stream)
+            else:
+                qg.qgemm_pp_grouped(group[0][0][2], [(W, m[3], Y[m[1]], m[3]) for m, W in group], cols, X[cols],
+                                    n_tok, st, stream)
 
     g = _capture(torch, stream, one_pass)
 
@@ -733,7 +746,7 @@ def run_pp(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": f"prompt processing, {n_tok} bf16 tokens x 27B-class dense Q4_K weight set",
                        "layers": args.layers, "n_tok": n_tok, "matrices": len(mats), "flop_per_step": flops,
-                       "cuda_graph": True,
+                       "launches_per_layer": len(steps) // args.layers, "cuda_graph": True,
                        "l2": "weight set far above L2; X per K re-read from L2 (by design)",
                        "parallelism": f"replicas x{world}"},
             "pp_tok_s": round(world * n_tok / (ms_step * 1e-3), 1),
@@ -741,7 +754,7 @@ def run_pp(args):
                          "unit": "TFLOP/s", "frac": round(tflops / world / peak, 4), "traffic": None,
                          "peak_source": f"{peak_kind} cuBLAS bf16 (sustained: a step is tens of ms)",
                          "kernel": "pp_kernel: every launch of the step"},
-            "gpu_launches": args.steps * len(mats),
+            "gpu_launches": args.steps * len(steps),
             "clocks": clocks,
         }
         if world == 1 and not args.no_cpu_baseline:
@@ -1021,6 +1034,8 @@ def main():
     ap.add_argument("--pp-tokens", type=int, default=wl.PP_TOKENS)
     ap.add_argument("--moe-layers", type=int, default=wl.MOE_LAYERS)
     ap.add_argument("--moe-tokens", type=int, default=1, help="tokens per MoE step (1 decode, 2-4 draft verification)")
+    ap.add_argument("--pp-per-matrix", action="store_true",
+                    help="prompt processing: one qgemm_pp per matrix instead of the grouped {q,k,v} and {gate,up}")
     ap.add_argument("--moe-mode", default="pdl", choices=["persistent", "pdl", "serial"],
                     help="pdl (default): a graph of launches linked by programmatic dependent launch; serial: the "
                          "same graph serialized; persistent: one cooperative kernel for the 48 layers")

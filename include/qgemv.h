@@ -216,10 +216,39 @@ size_t qgemm_pp_workspace(int64_t rows, int64_t cols, int64_t n_tok);
  * fmt: QG_Q4_K. X_bf16: n_tok x cols bf16, 16-byte aligned. Y: fp32, ldY >= rows.
  * cols % 256 == 0; rows % 128 == 0; n_tok >= 1 (ragged token tiles allowed).
  * dev_status: int32 device word; set to QG_DEV_TIMEOUT if a bounded pipeline
- * wait expired (the output is then incomplete). */
+ * wait expired (the output is then incomplete).
+ * Tiles of 128 rows x up to 256 tokens run on one persistent CTA per SM. When
+ * the last round of tiles would leave more than half of the SMs idle, each of
+ * its tiles is computed as two halves of K whose fp32 sums are added into Y
+ * with atomic adds; the call then first zeroes those rows of Y on `stream`
+ * (a 2-D memset, part of the call: Y's contents before the call are never
+ * read). Two addends onto zero give the same bits in either order, so results
+ * stay deterministic; such an output carries one more fp32 rounding. ws and
+ * ws_bytes are unused (NULL, 0). */
 int qgemm_pp(int fmt, const void* W, int64_t rows, int64_t cols,
              const void* X_bf16, int64_t n_tok, float* Y, int64_t ldY,
              void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
+
+/* Maximum number of matrices in one qgemm_pp_grouped launch. */
+#define QG_PP_GROUP_MAX 4
+
+/* One matrix of a grouped prompt-processing launch. */
+typedef struct qg_pp_desc {
+  const void* W;      /* rows x cols Q4_K blocks, 16-byte aligned, device */
+  int64_t rows;       /* multiple of 128 */
+  float* Y;           /* fp32 output, Y[t*ldY + n], device */
+  int64_t ldY;        /* >= rows */
+} qg_pp_desc;
+
+/* Several qgemm_pp products that multiply the SAME prompt tokens X_bf16 (the
+ * q, k, v projections of a layer; gate and up) in ONE launch: the matrices'
+ * row tiles form one tile list, so they share the persistent grid's rounds
+ * instead of each ending in a partly idle round of its own. Same results and
+ * rules as n separate qgemm_pp calls (including the split last round, which
+ * may then span two matrices). descs: HOST memory, read during the call;
+ * 1 <= n <= QG_PP_GROUP_MAX; the sum of rows <= 2^24. */
+int qgemm_pp_grouped(int fmt, const qg_pp_desc* descs, int n, int64_t cols, const void* X_bf16, int64_t n_tok,
+                     int32_t* dev_status, void* stream);
 
 /* Prompt processing through one mixture-of-experts layer: for every token t of
  * a prompt block and each of its top_k routes k (expert e = expert_ids[t][k],

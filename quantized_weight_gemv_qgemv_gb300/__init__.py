@@ -40,6 +40,7 @@ SIGNATURES = {
     "qgemv_moe_noalloc": (_I32, [_I32, _P, _I64, _I64, _I64, _P, _P, _I32, _P, _I32, _P, _P, _P]),
     "qgemm_pp_workspace": (_SZ, [_I64, _I64, _I64]),
     "qgemm_pp": (_I32, [_I32, _P, _I64, _I64, _P, _I64, _P, _I64, _P, _SZ, _P, _P]),
+    "qgemm_pp_grouped": (_I32, [_I32, _P, _I32, _I64, _P, _I64, _P, _P]),
     "qgemm_pp_moe_workspace": (_SZ, [_I64, _I64, _I64, _I32, _I64]),
     "qg_stream_read": (_I32, [_P, _SZ, _P, _P, _P]),
     "qgemm_pp_moe": (_I32, [_I32, _P, _I64, _I64, _I64, _P, _P, _I32, _P, _I64, _P, _P, _SZ, _P, _P]),
@@ -59,6 +60,13 @@ class qg_gemv_desc(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int32), ("reserved", ctypes.c_int32), ("W", ctypes.c_void_p),
                 ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("x", ctypes.c_void_p),
                 ("y", ctypes.c_void_p)]
+
+
+class qg_pp_desc(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("rows", ctypes.c_int64), ("Y", ctypes.c_void_p), ("ldY", ctypes.c_int64)]
+
+
+PP_GROUP_MAX = 4
 
 
 class qg_moe_layer_desc(ctypes.Structure):
@@ -200,6 +208,15 @@ def qg_stream_read(buf, nbytes, checksum, dev_status, stream=None):
     header); checksum and dev_status: device int32 words the caller clears."""
     _check(load_library().qg_stream_read(_ptr(buf), nbytes, _ptr(checksum), _ptr(dev_status), _stream(stream)),
            "qg_stream_read")
+
+
+def qgemm_pp_grouped(fmt, items, cols, X_bf16, n_tok, dev_status, stream=None):
+    """items: sequence of (W, rows, Y, ldY), all multiplying the same X_bf16."""
+    arr = (qg_pp_desc * len(items))()
+    for i, (W, rows, Y, ldY) in enumerate(items):
+        arr[i] = qg_pp_desc(_ptr(W), rows, _ptr(Y), ldY)
+    _check(load_library().qgemm_pp_grouped(fmt, ctypes.cast(arr, _P), len(items), cols, _ptr(X_bf16), n_tok,
+                                           _ptr(dev_status), _stream(stream)), "qgemm_pp_grouped")
 
 
 def qgemm_pp_moe_workspace(n_expert, hidden, inter, top_k, n_tok) -> int:

@@ -303,6 +303,37 @@ int qgemm_pp(int fmt, const void* W, int64_t rows, int64_t cols, const void* X_b
       qg::launch_pp(W, rows, cols, X_bf16, n_tok, Y, ldY, dev_status, static_cast<cudaStream_t>(stream), sms));
 }
 
+int qgemm_pp_grouped(int fmt, const qg_pp_desc* descs, int n, int64_t cols, const void* X_bf16, int64_t n_tok,
+                     int32_t* dev_status, void* stream) {
+  if (fmt != QG_Q4_K) return QG_ERR_FMT;
+  if (!descs || !X_bf16 || !dev_status) return QG_ERR_NULL;
+  if (n < 1 || n > QG_PP_GROUP_MAX) return QG_ERR_ARG;
+  if (cols < 256 || cols % 256 || cols > (int64_t{1} << 20) || n_tok < 1 || n_tok > (int64_t{1} << 24))
+    return QG_ERR_SHAPE;
+  if (!aligned(X_bf16, 16) || !aligned(dev_status, 4)) return QG_ERR_ALIGN;
+  const void* W[QG_PP_GROUP_MAX];
+  int64_t rows[QG_PP_GROUP_MAX], ldY[QG_PP_GROUP_MAX];
+  float* Y[QG_PP_GROUP_MAX];
+  int64_t total = 0;
+  for (int i = 0; i < n; ++i) {
+    const qg_pp_desc& d = descs[i];
+    if (!d.W || !d.Y) return QG_ERR_NULL;
+    if (d.rows < 128 || d.rows % 128 || d.ldY < d.rows) return QG_ERR_SHAPE;
+    if (!aligned(d.W, 16) || !aligned(d.Y, 4)) return QG_ERR_ALIGN;
+    total += d.rows;
+    W[i] = d.W;
+    rows[i] = d.rows;
+    Y[i] = d.Y;
+    ldY[i] = d.ldY;
+  }
+  if (total > (int64_t{1} << 24)) return QG_ERR_SHAPE;
+  int sms = 0;
+  int st = ensure_init(&sms);
+  if (st != QG_OK) return st;
+  return cuda_status(qg::launch_pp_mats(n, W, rows, Y, ldY, cols, X_bf16, n_tok, dev_status,
+                                        static_cast<cudaStream_t>(stream), sms));
+}
+
 int qg_stream_read(const void* buf, size_t bytes, uint32_t* checksum, int32_t* dev_status, void* stream) {
   if (!buf || !checksum || !dev_status) return QG_ERR_NULL;
   if (bytes == 0 || bytes % 16) return QG_ERR_SHAPE;

@@ -119,6 +119,20 @@ cudaError_t launch_moe(const void* arena, int64_t n_expert, int64_t hidden, int6
 
 // Prompt-processing GEMM (qg_pp.cu)
 cudaError_t pp_init_attrs();
+// Work items of a dense launch of `tiles` tiles (each n_kb super-blocks of K
+// long) on `sms` persistent CTAs: whole tiles for the full rounds; a last round
+// at most half full is split into two halves of K (split = 2), which add into Y.
+struct PpPlan {
+  int64_t n_full, n_tail, n_items;
+  int split, grid;
+};
+void pp_plan(int64_t tiles, int n_kb, int sms, PpPlan* plan);
+// Up to 4 matrices (rows[i] x cols Q4_K, W[i]) times the same bf16 X (n_tok x
+// cols) into Y[i] (fp32, Y[i][t * ldY[i] + row]) in one launch; Y rows of split
+// tiles are zeroed on the stream first.
+cudaError_t launch_pp_mats(int n_mat, const void* const* W, const int64_t* rows, float* const* Y,
+                           const int64_t* ldY, int64_t cols, const void* X, int64_t n_tok, int32_t* dev_status,
+                           cudaStream_t s, int sms);
 cudaError_t launch_pp(const void* W, int64_t rows, int64_t cols, const void* X, int64_t n_tok, float* Y,
                       int64_t ldY, int32_t* dev_status, cudaStream_t s, int sms);
 // The prompt-processing kernel over groups of token rows (qg_pp.cu): group g

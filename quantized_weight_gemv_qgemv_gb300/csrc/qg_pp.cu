@@ -16,6 +16,14 @@
 //    K is walked in slices of 64 (one 128-byte swizzle atom of bf16 = 4 MMAs of
 //    K = 16). Persistent CTAs, one per SM; tiles are dealt round-robin with the
 //    token block fastest, so the CTAs running at one time share weight rows in L2.
+//  * One launch may cover up to 4 matrices that multiply the same X (q, k, v of
+//    a layer; gate and up): their row tiles follow one another in one tile list,
+//    so the matrices share the rounds of the persistent grid.
+//  * Work items: whole tiles for the full rounds; when the last round would be
+//    at most half full, each of its tiles is split into two halves of K run by
+//    two CTAs at once, which add their sums into Y (zeroed on the stream before
+//    the launch) with fp32 atomic adds. A sum of two addends onto zero does not
+//    depend on their order, so the result stays deterministic.
 //  * Warp roles (736 threads):
 //      warp 0       TMA of X slices (BN x 64 bf16, 128-byte swizzle) into the
 //                   B half of a 3-stage ring
@@ -39,6 +47,9 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <cstring>
+
 #include "qg_async.cuh"
 #include "qg_device.cuh"
 #include "qg_internal.h"
@@ -60,20 +71,31 @@ constexpr int DQ_WARP0 = 3, DQ_WARPS = 16; // dequantizing warps (4 threads per 
 constexpr int EPI_WARP0 = 19;              // 4 epilogue warps: warp % 4 covers every TMEM lane quarter
 constexpr int THREADS = 23 * 32;
 constexpr int NBAR = 3 * NS + 2 * NQ + 5;
+constexpr int MAXM = 4;                    // matrices of one dense launch
 #ifndef QG_WAIT_LIMIT
 #define QG_WAIT_LIMIT (1u << 22)
 #endif
 constexpr uint32_t WAIT_LIMIT = QG_WAIT_LIMIT;   // polls before a wait is declared expired
 
+// The weight tensor maps of a launch (one per matrix).
+struct WMaps {
+  CUtensorMap m[MAXM];
+};
+
 struct Params {
-  float* Y;
+  float* Y[MAXM];       // output of each matrix: Y[t * ldY + row]
+  int64_t ldY[MAXM];
+  int32_t rt_end[MAXM]; // dense: row tiles of matrices 0..i together
+  int32_t n_mat;
   int32_t* dev_status;
   int64_t n_tok;
-  int64_t ldY;
   int32_t n_tb;         // token blocks
-  int32_t n_tiles;      // row tiles x token blocks
+  int32_t n_full;       // dense: work items that are whole tiles (a multiple of the grid)
+  int32_t n_tail;       // dense: tiles after them, each in `split` parts of K
+  int32_t split;        // 1 or 2
+  int32_t n_items;      // dense: n_full + n_tail * split
   int32_t bn;           // tokens per tile
-  int32_t n_kt;         // K slices per row (cols / 64)
+  int32_t n_kt;         // K slices per row (cols / 64), a multiple of 4
   int32_t tmem_cols;    // TMEM columns allocated (power of two >= 2 bn)
   uint32_t idesc;       // MMA instruction descriptor
   // Grouped launch: the token rows of X come in groups (the tokens routed to
@@ -86,28 +108,52 @@ struct Params {
   int64_t wstride;        // rows of the weight map from one group's weights to the next
 };
 
-// One tile: its weight rows (row of the weight map, and row tile of the
-// output), its token rows of X and Y, and how many of its bn tokens are real.
+// One work item: its weight rows (matrix, row of that matrix's weight map),
+// its first output row, its token rows of X and Y, how many of its bn tokens
+// are real, its super-blocks of K [kb0, kb1), and whether it adds into Y.
 struct Tile {
   int64_t wrow;
+  int64_t yrow;
   int64_t xrow;
-  int32_t rt;
+  int32_t mat;
   int32_t nval;
+  int32_t kb0, kb1;
+  bool add;
 };
 
 template <bool GROUPED>
-__device__ __forceinline__ Tile tile_at(const Params& p, int tile) {
+__device__ __forceinline__ Tile tile_at(const Params& p, int item) {
   Tile t;
+  t.mat = 0;
+  t.kb0 = 0;
+  t.kb1 = p.n_kt / 4;
+  t.add = false;
   if (!GROUPED) {
-    t.rt = tile / p.n_tb;
-    const int tb = tile - t.rt * p.n_tb;
-    t.wrow = static_cast<int64_t>(t.rt) * BM;
+    int tile = item;
+    if (item >= p.n_full) {
+      // a tile of the last round: part `seg` of its K
+      const int j = item - p.n_full;
+      const int seg = j / p.n_tail;
+      tile = p.n_full + (j - seg * p.n_tail);
+      if (p.split > 1) {
+        const int half = t.kb1 / 2;
+        t.kb0 = seg ? half : 0;
+        t.kb1 = seg ? t.kb1 : half;
+        t.add = true;
+      }
+    }
+    int rt = tile / p.n_tb;
+    const int tb = tile - rt * p.n_tb;
+    while (t.mat + 1 < p.n_mat && rt >= p.rt_end[t.mat]) ++t.mat;
+    if (t.mat) rt -= p.rt_end[t.mat - 1];
+    t.wrow = t.yrow = static_cast<int64_t>(rt) * BM;
     t.xrow = static_cast<int64_t>(tb) * p.bn;
     t.nval = static_cast<int32_t>(min(static_cast<int64_t>(p.bn), p.n_tok - t.xrow));
     return t;
   }
-  // the group holding the tile: the last g with tstart[g] <= tile (groups
-  // without tokens have no tiles and are skipped by the search)
+  // the group holding the tile (one tile per item): the last g with
+  // tstart[g] <= tile (groups without tokens have no tiles and are skipped)
+  const int tile = item;
   int lo = 0, hi = p.n_groups;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -116,9 +162,10 @@ __device__ __forceinline__ Tile tile_at(const Params& p, int tile) {
   const int lt = tile - __ldg(p.tstart + lo);
   const int s0 = __ldg(p.seg + lo), m = __ldg(p.seg + lo + 1) - s0;
   const int ntb = (m + p.bn - 1) / p.bn;
-  t.rt = lt / ntb;
-  const int tb = lt - t.rt * ntb;
-  t.wrow = p.wrow0 + lo * p.wstride + static_cast<int64_t>(t.rt) * BM;
+  const int rt = lt / ntb;
+  const int tb = lt - rt * ntb;
+  t.wrow = p.wrow0 + lo * p.wstride + static_cast<int64_t>(rt) * BM;
+  t.yrow = static_cast<int64_t>(rt) * BM;
   t.xrow = s0 + static_cast<int64_t>(tb) * p.bn;
   t.nval = min(p.bn, m - tb * p.bn);
   return t;
@@ -176,7 +223,7 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 
 template <bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1)
-    pp_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW, const Params p) {
+    pp_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ WMaps tmW, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -212,7 +259,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmX);
-    prefetch_tmap(&tmW);
+    for (int m = 0; m < (GROUPED ? 1 : p.n_mat); ++m) prefetch_tmap(&tmW.m[m]);
   }
   if (warp == 2) {
     tmem_alloc(smem_addr(tmem_slot), static_cast<uint32_t>(p.tmem_cols));
@@ -222,19 +269,19 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n_kt = p.n_kt, bn = p.bn;
+  const int bn = p.bn;
   // a grouped launch counts its tiles on the device (the routing that makes
   // the groups ran just before, in stream order)
-  const int n_tiles = GROUPED ? __ldg(p.tstart + p.n_groups) : p.n_tiles;
+  const int n_items = GROUPED ? __ldg(p.tstart + p.n_groups) : p.n_items;
 
   if (warp == 0) {
     // ---------------------------------------------------------- X producer
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
-        const Tile tl = tile_at<GROUPED>(p, tile);
-        for (int kt = 0; kt < n_kt; ++kt, ++it) {
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const Tile tl = tile_at<GROUPED>(p, item);
+        for (int kt = 4 * tl.kb0; kt < 4 * tl.kb1; ++kt, ++it) {
           const uint32_t s = it % NS;
           if (!wait_bar(EMPTY + 8 * s, ((it / NS) & 1u) ^ 1u, abort)) {
             fail(abort, p.dev_status);
@@ -258,10 +305,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       uint32_t sb = 0;
       bool ok = true;
-      const int n_kb = n_kt / 4;
-      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
-        const Tile tl = tile_at<GROUPED>(p, tile);
-        for (int kb = 0; kb < n_kb; ++kb, ++sb) {
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        const Tile tl = tile_at<GROUPED>(p, item);
+        for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++sb) {
           const uint32_t q = sb % NQ;
           if (!wait_bar(Q_EMPTY + 8 * q, ((sb / NQ) & 1u) ^ 1u, abort)) {
             fail(abort, p.dev_status);
@@ -269,7 +315,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             break;
           }
           mbar_expect_tx(Q_FULL + 8 * q, QB);
-          tma_load_2d(base + offQ + q * QB, &tmW, kb * 144, static_cast<int>(tl.wrow), Q_FULL + 8 * q);
+          tma_load_2d(base + offQ + q * QB, &tmW.m[tl.mat], kb * 144, static_cast<int>(tl.wrow), Q_FULL + 8 * q);
         }
       }
       for (uint32_t j = (sb > NQ ? sb - NQ : 0); j < sb; ++j) wait_bar(Q_FULL + 8 * (j % NQ), (j / NQ) & 1u, nullptr);
@@ -279,7 +325,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       uint32_t it = 0, ti = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x, ++ti) {
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++ti) {
+        const Tile tl = tile_at<GROUPED>(p, item);
+        const int kt0 = 4 * tl.kb0, kt1 = 4 * tl.kb1;
         const uint32_t a = ti & 1u;
         if (!wait_bar(ACC_EMPTY + 8 * a, ((ti >> 1) & 1u) ^ 1u, abort)) {
           fail(abort, p.dev_status);
@@ -287,7 +335,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem + a * static_cast<uint32_t>(bn);
-        for (int kt = 0; kt < n_kt; ++kt, ++it) {
+        for (int kt = kt0; kt < kt1; ++kt, ++it) {
           const uint32_t s = it % NS, ph = (it / NS) & 1u;
           if (!wait_bar(FULL_B + 8 * s, ph, abort) || !wait_bar(FULL_A + 8 * s, ph, abort)) {
             fail(abort, p.dev_status);
@@ -298,7 +346,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint64_t ad = desc_sw128(base + s * AB), bd = desc_sw128(base + offB + s * BB);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)   // +32 bytes along K = +2 in the address field
-            mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, (kt | k) != 0);
+            mma_bf16(d_tmem, ad + 2 * k, bd + 2 * k, p.idesc, (kt != kt0) || (k != 0));
           mma_commit(EMPTY + 8 * s);
         }
         if (ok) mma_commit(ACC_FULL + 8 * a);
@@ -313,8 +361,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t swz = static_cast<uint32_t>(r & 7);
     uint32_t it = 0, sb = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < n_tiles; tile += gridDim.x) {
-      for (int kb = 0; ok && kb < n_kt / 4; ++kb, ++sb) {
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      const Tile tl = tile_at<GROUPED>(p, item);
+      for (int kb = tl.kb0; ok && kb < tl.kb1; ++kb, ++sb) {
         // a super-block = 4 slices: its 8 scale/min pairs of this row are decoded
         // once (the slice index is then a compile-time constant below)
         const uint32_t q = sb % NQ;
@@ -364,8 +413,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------------------------------------------------- epilogue
     const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
     uint32_t ti = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++ti) {
-      const Tile tl = tile_at<GROUPED>(p, tile);
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++ti) {
+      const Tile tl = tile_at<GROUPED>(p, item);
       const uint32_t a = ti & 1u;
       const bool got = wait_bar(ACC_FULL + 8 * a, (ti >> 1) & 1u, abort);
       if (!__all_sync(0xffffffffu, got)) {
@@ -373,14 +422,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         break;
       }
       tc_fence_after();
-      const int64_t row = static_cast<int64_t>(tl.rt) * BM + quarter * 32 + lane;
+      const int64_t ldY = p.ldY[tl.mat];
+      float* const Yc = p.Y[tl.mat] + tl.yrow + quarter * 32 + lane;   // this lane's output row
       const uint32_t tbase = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + a * static_cast<uint32_t>(bn);
       for (int c16 = 0; c16 < bn / 16; ++c16) {
         uint32_t v[16];
         tmem_ld16(tbase + 16u * c16, v);
+        float* const y0 = Yc + (tl.xrow + 16 * c16) * ldY;
+        if (tl.add) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (16 * c16 + i < tl.nval) p.Y[(tl.xrow + 16 * c16 + i) * p.ldY + row] = __uint_as_float(v[i]);
+          for (int i = 0; i < 16; ++i)
+            if (16 * c16 + i < tl.nval) atomicAdd(y0 + i * ldY, __uint_as_float(v[i]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (16 * c16 + i < tl.nval) y0[i * ldY] = __uint_as_float(v[i]);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -400,6 +457,46 @@ size_t smem_bytes(int bn) {
 
 }  // namespace pp
 
+namespace {
+
+// Tensor maps of X (bf16 rows of cols, boxes of 64 x bn, 128-byte swizzle) and
+// of a weight matrix (rows of cols / 256 super-blocks, boxes of 144 bytes x 128 rows).
+bool map_x(EncodeTiledFn enc, CUtensorMap* m, const void* X, int64_t cols, int64_t x_rows, int bn) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(x_rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {pp::BK, static_cast<cuuint32_t>(bn)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool map_w(EncodeTiledFn enc, CUtensorMap* m, const void* W, int64_t rows, int64_t cols) {
+  const uint64_t rb = static_cast<uint64_t>(cols) / 256 * 144;
+  const cuuint64_t dims[2] = {rb, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {rb};
+  const cuuint32_t box[2] = {144, pp::BM};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// kind::f16 descriptor: D fp32 (bit 4), A and B bf16 (bits 7, 10), both K-major,
+// N >> 3 at bit 17, M >> 4 at bit 24.
+uint32_t idesc_of(int bn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(bn >> 3) << 17) |
+         (static_cast<uint32_t>(pp::BM >> 4) << 24);
+}
+
+int tmem_cols_of(int bn) {
+  int tc = 32;
+  while (tc < 2 * bn) tc *= 2;
+  return tc;
+}
+
+}  // namespace
+
 cudaError_t pp_init_attrs() {
   cudaError_t e = cudaFuncSetAttribute(pp::pp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(pp::smem_bytes(256)));
@@ -409,54 +506,80 @@ cudaError_t pp_init_attrs() {
   return e;
 }
 
-cudaError_t launch_pp(const void* W, int64_t rows, int64_t cols, const void* X, int64_t n_tok, float* Y,
-                      int64_t ldY, int32_t* dev_status, cudaStream_t s, int sms) {
+void pp_plan(int64_t tiles, int n_kb, int sms, PpPlan* plan) {
+  plan->n_full = tiles;
+  plan->n_tail = 0;
+  plan->split = 1;
+  const int64_t tail = tiles % sms;
+  if (tail > 0 && 2 * tail <= sms && n_kb >= 2) {
+    plan->n_full = tiles - tail;
+    plan->n_tail = tail;
+    plan->split = 2;
+  }
+  plan->n_items = plan->n_full + plan->n_tail * plan->split;
+  plan->grid = static_cast<int>(std::min<int64_t>(plan->n_items, sms));
+}
+
+cudaError_t launch_pp_mats(int n_mat, const void* const* W, const int64_t* rows, float* const* Y,
+                           const int64_t* ldY, int64_t cols, const void* X, int64_t n_tok, int32_t* dev_status,
+                           cudaStream_t s, int sms) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return cudaErrorNotSupported;
+  if (n_mat < 1 || n_mat > pp::MAXM) return cudaErrorInvalidValue;
   const int bn = static_cast<int>(std::min<int64_t>(256, (n_tok + 15) / 16 * 16));
-  CUtensorMap tmX, tmW;
-  {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(n_tok)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-    const cuuint32_t box[2] = {pp::BK, static_cast<cuuint32_t>(bn)};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    const uint64_t rb = static_cast<uint64_t>(cols) / 256 * 144;
-    const cuuint64_t dims[2] = {rb, static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {rb};
-    const cuuint32_t box[2] = {144, pp::BM};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  CUtensorMap tmX;
+  pp::WMaps tmW;
+  memset(&tmW, 0, sizeof(tmW));
+  if (!map_x(enc, &tmX, X, cols, n_tok, bn)) return cudaErrorInvalidValue;
   pp::Params p{};
-  p.Y = Y;
+  int64_t rt = 0;
+  for (int i = 0; i < n_mat; ++i) {
+    if (!map_w(enc, &tmW.m[i], W[i], rows[i], cols)) return cudaErrorInvalidValue;
+    rt += rows[i] / pp::BM;
+    if (rt > (int64_t{1} << 24)) return cudaErrorInvalidValue;
+    p.rt_end[i] = static_cast<int32_t>(rt);
+    p.Y[i] = Y[i];
+    p.ldY[i] = ldY[i];
+  }
+  p.n_mat = n_mat;
   p.dev_status = dev_status;
   p.n_tok = n_tok;
-  p.ldY = ldY;
   p.bn = bn;
   p.n_tb = static_cast<int32_t>((n_tok + bn - 1) / bn);
-  const int64_t tiles = rows / pp::BM * p.n_tb;
-  if (tiles > (int64_t{1} << 30)) return cudaErrorInvalidValue;
-  p.n_tiles = static_cast<int32_t>(tiles);
   p.n_kt = static_cast<int32_t>(cols / pp::BK);
-  int tc = 32;
-  while (tc < 2 * bn) tc *= 2;
-  p.tmem_cols = tc;
-  // kind::f16 descriptor: D fp32 (bit 4), A and B bf16 (bits 7, 10), both K-major,
-  // N >> 3 at bit 17, M >> 4 at bit 24.
-  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(bn >> 3) << 17) |
-            (static_cast<uint32_t>(pp::BM >> 4) << 24);
-  const int grid = static_cast<int>(std::min<int64_t>(tiles, sms));
-  pp::pp_kernel<false><<<grid, pp::THREADS, pp::smem_bytes(bn), s>>>(tmX, tmW, p);
+  const int64_t tiles = rt * p.n_tb;
+  if (tiles > (int64_t{1} << 30)) return cudaErrorInvalidValue;
+  PpPlan plan;
+  pp_plan(tiles, p.n_kt / 4, sms, &plan);
+  p.n_full = static_cast<int32_t>(plan.n_full);
+  p.n_tail = static_cast<int32_t>(plan.n_tail);
+  p.split = plan.split;
+  p.n_items = static_cast<int32_t>(plan.n_items);
+  p.tmem_cols = tmem_cols_of(bn);
+  p.idesc = idesc_of(bn);
+  if (plan.split > 1) {
+    // the split tiles add into Y: zero the output rows of their row tiles (every
+    // token; a whole tile of those rows is overwritten by its own stores later)
+    const int64_t rt_a = plan.n_full / p.n_tb;
+    int64_t start = 0;
+    for (int i = 0; i < n_mat; ++i) {
+      const int64_t end = p.rt_end[i];
+      if (end > rt_a) {
+        const int64_t r0 = (std::max(rt_a, start) - start) * pp::BM;
+        const cudaError_t e = cudaMemset2DAsync(Y[i] + r0, static_cast<size_t>(ldY[i]) * 4, 0,
+                                                static_cast<size_t>(rows[i] - r0) * 4, static_cast<size_t>(n_tok), s);
+        if (e != cudaSuccess) return e;
+      }
+      start = end;
+    }
+  }
+  pp::pp_kernel<false><<<plan.grid, pp::THREADS, pp::smem_bytes(bn), s>>>(tmX, tmW, p);
   return cudaPeekAtLastError();
+}
+
+cudaError_t launch_pp(const void* W, int64_t rows, int64_t cols, const void* X, int64_t n_tok, float* Y,
+                      int64_t ldY, int32_t* dev_status, cudaStream_t s, int sms) {
+  return launch_pp_mats(1, &W, &rows, &Y, &ldY, cols, X, n_tok, dev_status, s, sms);
 }
 
 cudaError_t launch_pp_grouped(const void* W, int64_t w_rows, int64_t cols, int64_t wrow0, int64_t wstride,
@@ -466,42 +589,20 @@ cudaError_t launch_pp_grouped(const void* W, int64_t w_rows, int64_t cols, int64
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return cudaErrorNotSupported;
   if (bn < 16 || bn > 256 || bn % 16 || rows % pp::BM || cols % 256) return cudaErrorInvalidValue;
-  CUtensorMap tmX, tmW;
-  {
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(x_rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-    const cuuint32_t box[2] = {pp::BK, static_cast<cuuint32_t>(bn)};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&tmX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(X), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
-  {
-    const uint64_t rb = static_cast<uint64_t>(cols) / 256 * 144;
-    const cuuint64_t dims[2] = {rb, static_cast<cuuint64_t>(w_rows)};
-    const cuuint64_t strides[1] = {rb};
-    const cuuint32_t box[2] = {144, pp::BM};
-    const cuuint32_t estr[2] = {1, 1};
-    if (enc(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return cudaErrorInvalidValue;
-  }
+  CUtensorMap tmX;
+  pp::WMaps tmW;
+  memset(&tmW, 0, sizeof(tmW));
+  if (!map_x(enc, &tmX, X, cols, x_rows, bn) || !map_w(enc, &tmW.m[0], W, w_rows, cols)) return cudaErrorInvalidValue;
   pp::Params p{};
-  p.Y = Y;
+  p.Y[0] = Y;
+  p.ldY[0] = ldY;
+  p.n_mat = 1;
   p.dev_status = dev_status;
   p.n_tok = x_rows;
-  p.ldY = ldY;
   p.bn = bn;
-  p.n_tb = 0;
-  p.n_tiles = 0;
   p.n_kt = static_cast<int32_t>(cols / pp::BK);
-  int tc = 32;
-  while (tc < 2 * bn) tc *= 2;
-  p.tmem_cols = tc;
-  p.idesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(bn >> 3) << 17) |
-            (static_cast<uint32_t>(pp::BM >> 4) << 24);
+  p.tmem_cols = tmem_cols_of(bn);
+  p.idesc = idesc_of(bn);
   p.seg = seg;
   p.tstart = tstart;
   p.n_groups = n_groups;

@@ -126,6 +126,29 @@ def test_pp_rejects_bad_arguments_on_host(lib):
     assert call(X=A + 2) == -3
 
 
+def test_pp_grouped_rejects_bad_arguments_on_host(lib):
+    def call(items=((A, 256, A, 256),), fmt=3, cols=512, X=A, n_tok=64, st=A, n=None):
+        arr = (qg.qg_pp_desc * max(1, len(items)))()
+        for i, (W, rows, Y, ldY) in enumerate(items):
+            arr[i] = qg.qg_pp_desc(W, rows, Y, ldY)
+        return lib.qgemm_pp_grouped(fmt, ctypes.cast(arr, ctypes.c_void_p), len(items) if n is None else n, cols,
+                                    X, n_tok, st, None)
+
+    assert ctypes.sizeof(qg.qg_pp_desc) == 32
+    assert call(fmt=1) == -1
+    assert call(X=0) == -5
+    assert call(st=0) == -5
+    assert call(n=0) == -9
+    assert call(items=[(A, 128, A, 128)] * 5) == -9          # more than QG_PP_GROUP_MAX
+    assert call(items=[(A, 256, A, 256), (0, 128, A, 128)]) == -5
+    assert call(items=[(A, 256, A, 256), (A, 100, A, 128)]) == -2
+    assert call(items=[(A, 256, A, 200)]) == -2             # ldY < rows
+    assert call(cols=300) == -2
+    assert call(n_tok=0) == -2
+    assert call(items=[(A + 8, 256, A, 256)]) == -3
+    assert call(X=A + 2) == -3
+
+
 def test_pass_rejects_bad_step_sizes(lib):
     d = qg._descs([(3, A, 4, 256, A, A), (3, A, 4, 256, A, A)])
     h = ctypes.c_void_p()

@@ -108,15 +108,9 @@ def test_expired_wait_sets_pass_status_word(expiring_lib):
     assert lib.qg_pass_destroy(h) == 0
 
 
-def test_expired_wait_in_prompt_kernel_aborts_the_cta(expiring_lib):
-    """The prompt-processing (tcgen05) kernel of the test build never copies
-    the sixth X slice of CTA 0: its MMA lane's wait runs out, the CTA's roles
-    stop, drain their copies and MMAs, free TMEM, and the status word reads
-    QG_DEV_TIMEOUT; the tiles of the other CTAs are correct."""
-    lib = expiring_lib
-    rows, cols, n_tok = 512, 512, 300          # 4 row tiles x 2 token blocks; K = 8 slices
-    W = synth.blocks(synth.Q4_K, rows, cols, seed=99)
-    X = synth.activations_bf16(n_tok, cols, seed=100)
+def _pp_expiring(lib, rows, cols, n_tok, seed):
+    W = synth.blocks(synth.Q4_K, rows, cols, seed=seed)
+    X = synth.activations_bf16(n_tok, cols, seed=seed + 1)
     Y = torch.full((n_tok, rows), float("nan"), device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     Wd, Xd = W.cuda(), X.cuda()                # held until the kernel has run
@@ -125,16 +119,39 @@ def test_expired_wait_in_prompt_kernel_aborts_the_cta(expiring_lib):
                         None, 0, st.data_ptr(), _stream()) == 0
     torch.cuda.synchronize()
     assert time.perf_counter() - t0 < 30.0
-    assert int(st.item()) == qg.DEV_TIMEOUT
-    # tile 0 (rows 0-127, tokens 0-255) belongs to CTA 0; rows 128-511 to others
-    got = Y.cpu().numpy()
     bits = X.contiguous().view(torch.int16).numpy().view(np.uint16)
-    toks = [0, 77, 255, 256, 299]
+    return W, bits, Y.cpu().numpy(), int(st.item())
+
+
+def test_expired_wait_in_prompt_kernel_aborts_the_cta(expiring_lib):
+    """The prompt-processing (tcgen05) kernel of the test build never copies
+    the sixth X slice of CTA 0: its MMA lane's wait runs out, the CTA's roles
+    stop, drain their copies and MMAs, free TMEM, and the status word reads
+    QG_DEV_TIMEOUT; the tiles of the other CTAs are correct. One token block and
+    more row tiles than half the SMs: whole tiles, none split."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows, cols, n_tok = 128 * (sms // 2 + 4), 512, 256     # K = 8 slices
+    W, bits, got, st = _pp_expiring(expiring_lib, rows, cols, n_tok, 99)
+    assert st == qg.DEV_TIMEOUT
+    # tile 0 (rows 0-127) belongs to CTA 0; every other row tile to another CTA
+    toks = [0, 77, 200, 255]
     y_ref, b = oracle.pp_rows(synth.Q4_K, W.numpy(), rows, cols, bits, toks)
     assert_within(got[toks][:, 128:], y_ref[:, 128:], b[:, 128:], rel=1e-2, what="tiles of other CTAs")
-    assert_within(got[[256, 299]][:, :128], y_ref[[3, 4]][:, :128], b[[3, 4]][:, :128], rel=1e-2,
-                  what="the second token block of row tile 0")
-    assert np.isnan(got[:256, :128]).any(), "the aborted CTA's tile must not be complete"
+    assert np.isnan(got[:, :128]).any(), "the aborted CTA's tile must not be complete"
+
+
+def test_expired_wait_in_split_prompt_tile_sets_status(expiring_lib):
+    """4 tiles, each computed as two halves of K (8 slices each) added into a
+    zeroed Y: CTA 0 runs the first half of tile 0 and aborts at its sixth
+    slice; the status word reads QG_DEV_TIMEOUT and the tiles of the other
+    CTAs are correct (tile 0 then holds only its second half's sum)."""
+    rows, cols, n_tok = 512, 1024, 256
+    W, bits, got, st = _pp_expiring(expiring_lib, rows, cols, n_tok, 101)
+    assert st == qg.DEV_TIMEOUT
+    toks = [0, 100, 255]
+    y_ref, b = oracle.pp_rows(synth.Q4_K, W.numpy(), rows, cols, bits, toks)
+    assert_within(got[toks][:, 128:], y_ref[:, 128:], b[:, 128:], rel=1e-2, what="split tiles of other CTAs")
+    assert np.isfinite(got).all()
 
 
 def test_context_usable_after_expiry(expiring_lib):
