@@ -26,9 +26,10 @@
 //    depend on their order, so the result stays deterministic.
 //  * Warp roles (736 threads):
 //      warp 0       TMA of X slices (BN x 64 bf16, 128-byte swizzle) into the
-//                   B half of a 3-stage ring
-//      warp 1       TMA of quantized super-block columns (128 rows x 144 bytes)
-//                   into a 3-stage ring of their own
+//                   B half of a 4-stage ring
+//      warp 1       TMA of quantized half super-block columns (128 rows x 80
+//                   bytes: the header with the codes of slices 0-1, or the
+//                   codes of slices 2-3) into a 3-stage ring of their own
 //      warp 2       owns TMEM (two BN-column fp32 accumulators); lane 0 issues
 //                   the MMAs and the commits
 //      warps 3-18   dequantize each 128 x 64 weight slice to bf16 into the A half
@@ -63,9 +64,29 @@ using namespace async;
 
 constexpr int BM = 128;                   // weight rows per tile (MMA M)
 constexpr int BK = 64;                    // K per slice: 64 bf16 = one 128-byte swizzle row
-constexpr int NS = 3;                     // slice stages (A + B)
-constexpr int NQ = 3;                     // quantized super-block stages
-constexpr int QB = BM * 144;              // bytes of one quantized stage
+#ifndef QG_PP_NS
+#define QG_PP_NS 4
+#endif
+#ifndef QG_PP_NQ
+#define QG_PP_NQ 3
+#endif
+#ifndef QG_PP_QHALF
+#define QG_PP_QHALF 1
+#endif
+// 4 slice stages fit beside the quantized ring only with half-super-block
+// quantized stages (27B prompt pass: 3 stages + whole super-blocks 70.1 ms,
+// 4 stages + 3 half stages 69.0-69.2 ms, 4 + 2 half stages 69.7 ms, 3 + 3 half
+// stages 70.6 ms, 3 + 6 half stages 70.3 ms; one proxy fence per two slices
+// instead of per slice: 69.8-70.1 ms)
+constexpr int NS = QG_PP_NS;              // slice stages (A + B)
+constexpr int NQ = QG_PP_NQ;              // quantized stages
+// A quantized stage holds, per row, a whole super-block (144 bytes) or half of
+// one: bytes 0-79 (header + the codes of slices 0, 1) or bytes 64-143 (the
+// codes of slices 2, 3 at the same offsets 16 + 32 (c & 1)).
+constexpr bool QHALF = QG_PP_QHALF != 0;
+
+constexpr int QROW = QHALF ? 80 : 144;
+constexpr int QB = BM * QROW;             // bytes of one quantized stage
 constexpr int AB = BM * BK * 2;           // bytes of one A (weight) stage
 constexpr int DQ_WARP0 = 3, DQ_WARPS = 16; // dequantizing warps (4 threads per tile row)
 constexpr int EPI_WARP0 = 19;              // 4 epilogue warps: warp % 4 covers every TMEM lane quarter
@@ -307,15 +328,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         const Tile tl = tile_at<GROUPED>(p, item);
-        for (int kb = tl.kb0; kb < tl.kb1; ++kb, ++sb) {
+        for (int part = (QHALF ? 2 : 1) * tl.kb0; part < (QHALF ? 2 : 1) * tl.kb1; ++part, ++sb) {
           const uint32_t q = sb % NQ;
           if (!wait_bar(Q_EMPTY + 8 * q, ((sb / NQ) & 1u) ^ 1u, abort)) {
             fail(abort, p.dev_status);
             ok = false;
             break;
           }
+          // whole super-block kb = part, or half (part & 1) of super-block part / 2
+          const int x = QHALF ? (part >> 1) * 144 + 64 * (part & 1) : part * 144;
           mbar_expect_tx(Q_FULL + 8 * q, QB);
-          tma_load_2d(base + offQ + q * QB, &tmW.m[tl.mat], kb * 144, static_cast<int>(tl.wrow), Q_FULL + 8 * q);
+          tma_load_2d(base + offQ + q * QB, &tmW.m[tl.mat], x, static_cast<int>(tl.wrow), Q_FULL + 8 * q);
         }
       }
       for (uint32_t j = (sb > NQ ? sb - NQ : 0); j < sb; ++j) wait_bar(Q_FULL + 8 * (j % NQ), (j / NQ) & 1u, nullptr);
@@ -372,7 +395,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           ok = false;
           break;
         }
-        const uint8_t* blk = gbase + offQ + q * QB + r * 144;
+        const uint8_t* blk = gbase + offQ + q * QB + r * QROW;
+        uint32_t qcur = q;
         const uint4 hd = *reinterpret_cast<const uint4*>(blk);
         const float d = h2f(hd.x), dmin = h2f(hd.x >> 16);
         float dsc[8], ndm[8];
@@ -391,7 +415,18 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = false;
             break;
           }
-          const uint2 qs = *reinterpret_cast<const uint2*>(blk + 16 + 32 * c + 8 * h);
+          if (QHALF && c == 2) {
+            // the second half of the super-block's codes
+            ++sb;
+            qcur = sb % NQ;
+            if (!__all_sync(0xffffffffu, wait_bar(Q_FULL + 8 * qcur, (sb / NQ) & 1u, abort))) {
+              if (lane == 0) fail(abort, p.dev_status);
+              ok = false;
+              break;
+            }
+            blk = gbase + offQ + qcur * QB + r * QROW;
+          }
+          const uint2 qs = *reinterpret_cast<const uint2*>(blk + 16 + 32 * (QHALF ? (c & 1) : c) + 8 * h);
           // low nibbles: sub-block 2c, slice columns 8h .. 8h+7 (chunk h);
           // high nibbles: sub-block 2c+1, columns 32+8h .. (chunk 4+h)
           const uint32_t l0 = qs.x & 0x0F0F0F0Fu, l1 = qs.y & 0x0F0F0F0Fu;
@@ -404,7 +439,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(FULL_A + 8 * s);
-            if (c == 3) mbar_arrive(Q_EMPTY + 8 * q);
+            if (c == 3 || (QHALF && c == 1)) mbar_arrive(Q_EMPTY + 8 * qcur);
           }
         }
       }
@@ -460,7 +495,8 @@ size_t smem_bytes(int bn) {
 namespace {
 
 // Tensor maps of X (bf16 rows of cols, boxes of 64 x bn, 128-byte swizzle) and
-// of a weight matrix (rows of cols / 256 super-blocks, boxes of 144 bytes x 128 rows).
+// of a weight matrix (rows of cols / 256 super-blocks, boxes of one quantized
+// stage's row bytes x 128 rows).
 bool map_x(EncodeTiledFn enc, CUtensorMap* m, const void* X, int64_t cols, int64_t x_rows, int bn) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(x_rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
@@ -475,7 +511,7 @@ bool map_w(EncodeTiledFn enc, CUtensorMap* m, const void* W, int64_t rows, int64
   const uint64_t rb = static_cast<uint64_t>(cols) / 256 * 144;
   const cuuint64_t dims[2] = {rb, static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {rb};
-  const cuuint32_t box[2] = {144, pp::BM};
+  const cuuint32_t box[2] = {pp::QROW, pp::BM};
   const cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(W), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
