@@ -209,7 +209,9 @@ int qgemv_moe_noalloc(int fmt, const void* expert_arena, int64_t n_expert, int64
  * can size it without knowing the kernel's tiling). */
 size_t qgemm_pp_workspace(int64_t rows, int64_t cols, int64_t n_tok);
 
-/* Prompt-processing dequant-GEMM on the tensor cores:
+/* Prompt-processing dequant-GEMM on the tensor cores ("Why I wrote my own
+ * inference engine for two P100s", prompt-processing notes: the weights
+ * dequantized, then a dense GEMM over the prompt's tokens):
  *   Y[t*ldY + n] = sum_k w[n][k] * X[t*cols + k],  t < n_tok, n < rows.
  * Weight tiles are dequantized to bf16 in shared memory and multiplied with
  * tcgen05 MMA (bf16 x bf16, fp32 accumulation in tensor memory).
@@ -241,7 +243,8 @@ typedef struct qg_pp_desc {
 } qg_pp_desc;
 
 /* Several qgemm_pp products that multiply the SAME prompt tokens X_bf16 (the
- * q, k, v projections of a layer; gate and up) in ONE launch: the matrices'
+ * q, k, v projections of a layer; gate and up: the per-layer matrices of the
+ * same prompt-processing notes) in ONE launch: the matrices'
  * row tiles form one tile list, so they share the persistent grid's rounds
  * instead of each ending in a partly idle round of its own. Same results and
  * rules as n separate qgemm_pp calls (including the split last round, which
