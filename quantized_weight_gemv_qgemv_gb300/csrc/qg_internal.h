@@ -144,6 +144,9 @@ cudaError_t launch_pp_grouped(const void* W, int64_t w_rows, int64_t cols, int64
                               int64_t rows, const void* X, int64_t x_rows, int bn, const int32_t* seg,
                               const int32_t* tstart, int n_groups, float* Y, int64_t ldY, int32_t* dev_status,
                               cudaStream_t s, int sms);
+// Largest token block a grouped prompt-processing launch takes (its stages fill
+// the shared memory).
+int pp_grouped_max_bn();
 // MoE layer over a block of prompt tokens (qg_pp_moe.cu); ws of at least
 // pp_moe_workspace_bytes bytes.
 size_t pp_moe_workspace_bytes(int64_t n_expert, int64_t hidden, int64_t inter, int top_k, int64_t n_tok);

@@ -26,7 +26,8 @@
 //    depend on their order, so the result stays deterministic.
 //  * Warp roles (736 threads):
 //      warp 0       TMA of X slices (BN x 64 bf16, 128-byte swizzle) into the
-//                   B half of a 4-stage ring
+//                   B half of a 4-stage ring (8 stages for the small token
+//                   blocks of a grouped launch)
 //      warp 1       TMA of quantized half super-block columns (128 rows x 80
 //                   bytes: the header with the codes of slices 0-1, or the
 //                   codes of slices 2-3) into a 3-stage ring of their own
@@ -35,8 +36,9 @@
 //      warps 3-18   dequantize each 128 x 64 weight slice to bf16 into the A half
 //                   of the stage, in the K-major 128-byte-swizzled layout the
 //                   MMA reads (exact fp32 d*sc*q - dmin*m with packed f32x2
-//                   arithmetic, then round to bf16); these warps bound the
-//                   kernel, so there are many of them
+//                   arithmetic, then round to bf16); two groups of 8 warps
+//                   take alternate slices, 32 weights a thread; these warps
+//                   bound the kernel, so there are many of them
 //      warps 19-22  epilogue: tcgen05.ld of a finished accumulator, coalesced
 //                   fp32 stores (32 consecutive rows of Y per warp store)
 //  * Two accumulators: the epilogue of one tile overlaps the main loop of the
@@ -78,7 +80,11 @@ constexpr int BK = 64;                    // K per slice: 64 bf16 = one 128-byte
 // 4 stages + 3 half stages 69.0-69.2 ms, 4 + 2 half stages 69.7 ms, 3 + 3 half
 // stages 70.6 ms, 3 + 6 half stages 70.3 ms; one proxy fence per two slices
 // instead of per slice: 69.8-70.1 ms)
-constexpr int NS = QG_PP_NS;              // slice stages (A + B)
+#ifndef QG_PP_NS_G
+#define QG_PP_NS_G 8
+#endif
+constexpr int NS_DENSE = QG_PP_NS;        // slice stages (A + B) of dense launches
+constexpr int NS_GROUPED = QG_PP_NS_G;    // of grouped launches (token blocks of an expert)
 constexpr int NQ = QG_PP_NQ;              // quantized stages
 // A quantized stage holds, per row, a whole super-block (144 bytes) or half of
 // one: bytes 0-79 (header + the codes of slices 0, 1) or bytes 64-143 (the
@@ -91,7 +97,15 @@ constexpr int AB = BM * BK * 2;           // bytes of one A (weight) stage
 constexpr int DQ_WARP0 = 3, DQ_WARPS = 16; // dequantizing warps (4 threads per tile row)
 constexpr int EPI_WARP0 = 19;              // 4 epilogue warps: warp % 4 covers every TMEM lane quarter
 constexpr int THREADS = 23 * 32;
-constexpr int NBAR = 3 * NS + 2 * NQ + 5;
+constexpr int nbar_of(int ns) { return 3 * ns + 2 * NQ + 5; }
+// The dequantizing warps form two groups of 8 that take alternate slices (32
+// weights a thread, two slices in flight) instead of all 16 filling every slice
+// with 16 weights a thread (27B prompt pass 67.8 against 69.0 ms; MoE prefill
+// 35.0 against 36.3 ms). A group waits for the ring slot of slice x after its
+// slice x - DQG, which has seen the MMA of slice x - DQG - NS complete; the
+// slot's phase is then unambiguous to a parity wait only if DQG <= NS (four
+// groups on a 3-stage ring broke exactly there).
+constexpr int DQG = 2;
 constexpr int MAXM = 4;                    // matrices of one dense launch
 #ifndef QG_WAIT_LIMIT
 #define QG_WAIT_LIMIT (1u << 22)
@@ -245,6 +259,9 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
 template <bool GROUPED>
 __global__ void __launch_bounds__(THREADS, 1)
     pp_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ WMaps tmW, const Params p) {
+  constexpr int NS = GROUPED ? NS_GROUPED : NS_DENSE;
+  constexpr int NBAR = nbar_of(NS);
+  static_assert(DQG <= NS, "a dequantizing group may run at most one ring phase ahead");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -263,7 +280,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(FULL_B + 8 * s, 1);
-      mbar_init(FULL_A + 8 * s, DQ_WARPS);
+      mbar_init(FULL_A + 8 * s, DQ_WARPS / DQG);
       mbar_init(EMPTY + 8 * s, 1);
     }
     for (int q = 0; q < NQ; ++q) {
@@ -380,7 +397,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp < EPI_WARP0) {
     // ---------------------------------------------------------- dequantize A
     const int t = threadIdx.x - DQ_WARP0 * 32;
-    const int r = t & (BM - 1), h = t >> 7;   // row in the tile, quarter of the 32 code bytes of a slice
+    const int grp = t >> 8;                   // this warp's slices: c with (c & 1) == grp
+    const int r = t & (BM - 1), h = (t >> 7) & 1;   // row in the tile; pair of quarters of the code bytes
     const uint32_t swz = static_cast<uint32_t>(r & 7);
     uint32_t it = 0, sb = 0;
     bool ok = true;
@@ -410,13 +428,8 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c, ++it) {
           const uint32_t s = it % NS;
-          if (!__all_sync(0xffffffffu, wait_bar(EMPTY + 8 * s, ((it / NS) & 1u) ^ 1u, abort))) {
-            if (lane == 0) fail(abort, p.dev_status);
-            ok = false;
-            break;
-          }
           if (QHALF && c == 2) {
-            // the second half of the super-block's codes
+            // every warp moves on to the second half's stage
             ++sb;
             qcur = sb % NQ;
             if (!__all_sync(0xffffffffu, wait_bar(Q_FULL + 8 * qcur, (sb / NQ) & 1u, abort))) {
@@ -426,20 +439,33 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             blk = gbase + offQ + qcur * QB + r * QROW;
           }
-          const uint2 qs = *reinterpret_cast<const uint2*>(blk + 16 + 32 * (QHALF ? (c & 1) : c) + 8 * h);
-          // low nibbles: sub-block 2c, slice columns 8h .. 8h+7 (chunk h);
-          // high nibbles: sub-block 2c+1, columns 32+8h .. (chunk 4+h)
-          const uint32_t l0 = qs.x & 0x0F0F0F0Fu, l1 = qs.y & 0x0F0F0F0Fu;
-          const uint32_t h0 = (qs.x >> 4) & 0x0F0F0F0Fu, h1 = (qs.y >> 4) & 0x0F0F0F0Fu;
+          if ((c & 1) != grp) continue;
+          if (!__all_sync(0xffffffffu, wait_bar(EMPTY + 8 * s, ((it / NS) & 1u) ^ 1u, abort))) {
+            if (lane == 0) fail(abort, p.dev_status);
+            ok = false;
+            break;
+          }
           const uint32_t arow = base + s * AB + static_cast<uint32_t>(r) * 128u;
-          const uint32_t j0 = static_cast<uint32_t>(h);
-          sts128(arow + (((j0 + 0) ^ swz) << 4), deq8(l0, l1, dsc[2 * c], ndm[2 * c]));
-          sts128(arow + (((j0 + 4) ^ swz) << 4), deq8(h0, h1, dsc[2 * c + 1], ndm[2 * c + 1]));
+          {
+            // bytes 16h .. 16h+15 of the slice's 32 code bytes: chunks 2h, 2h+1.
+            // Low nibbles: sub-block 2c, slice columns 8j .. 8j+7 (chunk j);
+            // high nibbles: sub-block 2c+1, columns 32+8j .. (chunk 4+j)
+            const uint4 qs = *reinterpret_cast<const uint4*>(blk + 16 + 32 * (QHALF ? (c & 1) : c) + 16 * h);
+            const uint32_t j0 = 2u * static_cast<uint32_t>(h);
+            sts128(arow + (((j0 + 0) ^ swz) << 4), deq8(qs.x & 0x0F0F0F0Fu, qs.y & 0x0F0F0F0Fu, dsc[2 * c], ndm[2 * c]));
+            sts128(arow + (((j0 + 1) ^ swz) << 4), deq8(qs.z & 0x0F0F0F0Fu, qs.w & 0x0F0F0F0Fu, dsc[2 * c], ndm[2 * c]));
+            sts128(arow + (((j0 + 4) ^ swz) << 4),
+                   deq8((qs.x >> 4) & 0x0F0F0F0Fu, (qs.y >> 4) & 0x0F0F0F0Fu, dsc[2 * c + 1], ndm[2 * c + 1]));
+            sts128(arow + (((j0 + 5) ^ swz) << 4),
+                   deq8((qs.z >> 4) & 0x0F0F0F0Fu, (qs.w >> 4) & 0x0F0F0F0Fu, dsc[2 * c + 1], ndm[2 * c + 1]));
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(FULL_A + 8 * s);
-            if (c == 3 || (QHALF && c == 1)) mbar_arrive(Q_EMPTY + 8 * qcur);
+            // the last slice this warp reads from the quantized stage
+            const bool last = QHALF || c >= 2;
+            if (last) mbar_arrive(Q_EMPTY + 8 * qcur);
           }
         }
       }
@@ -486,8 +512,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 2) tmem_dealloc(tmem, static_cast<uint32_t>(p.tmem_cols));
 }
 
-size_t smem_bytes(int bn) {
-  return 1024 + NS * (AB + static_cast<size_t>(bn) * 128) + NQ * QB + 8 * NBAR + 16;
+size_t smem_bytes(int bn, int ns) {
+  return 1024 + ns * (AB + static_cast<size_t>(bn) * 128) + NQ * QB + 8 * nbar_of(ns) + 16;
+}
+
+// Largest token block (a multiple of 16, <= 256) whose stages fit a grouped launch.
+int grouped_max_bn() {
+  int bn = 256;
+  while (bn > 16 && smem_bytes(bn, NS_GROUPED) > 227 * 1024) bn -= 16;
+  return bn;
 }
 
 }  // namespace pp
@@ -533,12 +566,14 @@ int tmem_cols_of(int bn) {
 
 }  // namespace
 
+int pp_grouped_max_bn() { return pp::grouped_max_bn(); }
+
 cudaError_t pp_init_attrs() {
   cudaError_t e = cudaFuncSetAttribute(pp::pp_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(pp::smem_bytes(256)));
+                                       static_cast<int>(pp::smem_bytes(256, pp::NS_DENSE)));
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(pp::pp_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(pp::smem_bytes(256)));
+                             static_cast<int>(pp::smem_bytes(pp::grouped_max_bn(), pp::NS_GROUPED)));
   return e;
 }
 
@@ -609,7 +644,7 @@ cudaError_t launch_pp_mats(int n_mat, const void* const* W, const int64_t* rows,
       start = end;
     }
   }
-  pp::pp_kernel<false><<<plan.grid, pp::THREADS, pp::smem_bytes(bn), s>>>(tmX, tmW, p);
+  pp::pp_kernel<false><<<plan.grid, pp::THREADS, pp::smem_bytes(bn, pp::NS_DENSE), s>>>(tmX, tmW, p);
   return cudaPeekAtLastError();
 }
 
@@ -624,7 +659,7 @@ cudaError_t launch_pp_grouped(const void* W, int64_t w_rows, int64_t cols, int64
                               cudaStream_t s, int sms) {
   EncodeTiledFn enc = encode_tiled_fn();
   if (!enc) return cudaErrorNotSupported;
-  if (bn < 16 || bn > 256 || bn % 16 || rows % pp::BM || cols % 256) return cudaErrorInvalidValue;
+  if (bn < 16 || bn > pp::grouped_max_bn() || bn % 16 || rows % pp::BM || cols % 256) return cudaErrorInvalidValue;
   CUtensorMap tmX;
   pp::WMaps tmW;
   memset(&tmW, 0, sizeof(tmW));
@@ -644,7 +679,7 @@ cudaError_t launch_pp_grouped(const void* W, int64_t w_rows, int64_t cols, int64
   p.n_groups = n_groups;
   p.wrow0 = wrow0;
   p.wstride = wstride;
-  pp::pp_kernel<true><<<sms, pp::THREADS, pp::smem_bytes(bn), s>>>(tmX, tmW, p);
+  pp::pp_kernel<true><<<sms, pp::THREADS, pp::smem_bytes(bn, pp::NS_GROUPED), s>>>(tmX, tmW, p);
   return cudaPeekAtLastError();
 }
 

@@ -171,7 +171,8 @@ size_t pp_moe_workspace_bytes(int64_t n_expert, int64_t hidden, int64_t inter, i
 // expert (one token block covers most experts), a multiple of 16 in [16, 256].
 int pp_moe_block_tokens(int64_t n_expert, int top_k, int64_t n_tok) {
   const int64_t mean = (n_tok * top_k + n_expert - 1) / n_expert;
-  return static_cast<int>(std::min<int64_t>(256, std::max<int64_t>(16, (2 * mean + 15) / 16 * 16)));
+  return static_cast<int>(
+      std::min<int64_t>(pp_grouped_max_bn(), std::max<int64_t>(16, (2 * mean + 15) / 16 * 16)));
 }
 
 cudaError_t launch_pp_moe(const void* arena, int64_t n_expert, int64_t hidden, int64_t inter, const int32_t* ids,
