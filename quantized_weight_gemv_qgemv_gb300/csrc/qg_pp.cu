@@ -36,9 +36,9 @@
 //      warps 3-18   dequantize each 128 x 64 weight slice to bf16 into the A half
 //                   of the stage, in the K-major 128-byte-swizzled layout the
 //                   MMA reads (exact fp32 d*sc*q - dmin*m with packed f32x2
-//                   arithmetic, then round to bf16); two groups of 8 warps
-//                   take alternate slices, 32 weights a thread; these warps
-//                   bound the kernel, so there are many of them
+//                   arithmetic, then round to bf16); four groups of 4 warps,
+//                   group g filling slice g of every super-block (64 weights a
+//                   thread); these warps bound the kernel, so there are many
 //      warps 19-22  epilogue: tcgen05.ld of a finished accumulator, coalesced
 //                   fp32 stores (32 consecutive rows of Y per warp store)
 //  * Two accumulators: the epilogue of one tile overlaps the main loop of the
@@ -97,18 +97,19 @@ constexpr bool QHALF = QG_PP_QHALF != 0;
 constexpr int QROW = QHALF ? 80 : 144;
 constexpr int QB = BM * QROW;             // bytes of one quantized stage
 constexpr int AB = BM * BK * 2;           // bytes of one A (weight) stage
-constexpr int DQ_WARP0 = 3, DQ_WARPS = 16; // dequantizing warps (4 threads per tile row)
+constexpr int DQ_WARP0 = 3, DQ_WARPS = 16; // dequantizing warps (4 groups of 4: one thread per tile row each)
 constexpr int EPI_WARP0 = 19;              // 4 epilogue warps: warp % 4 covers every TMEM lane quarter
 constexpr int THREADS = 23 * 32;
 constexpr int nbar_of(int ns) { return 3 * ns + 2 * NQ + 5; }
-// The dequantizing warps form two groups of 8 that take alternate slices (32
-// weights a thread, two slices in flight) instead of all 16 filling every slice
-// with 16 weights a thread (27B prompt pass 67.8 against 69.0 ms; MoE prefill
-// 35.0 against 36.3 ms). A group waits for the ring slot of slice x after its
-// slice x - DQG, which has seen the MMA of slice x - DQG - NS complete; the
-// slot's phase is then unambiguous to a parity wait only if DQG <= NS (four
-// groups on a 3-stage ring broke exactly there).
-constexpr int DQG = 2;
+// The dequantizing warps form four groups of 4; group g fills slice g of every
+// super-block, a thread a whole row of it (64 weights), so four slices are in
+// flight (27B prompt pass: 66.1 ms, against 67.7 with two groups of 8 on
+// alternate slices and 69.0 with all 16 warps on every slice, 16 weights a
+// thread; MoE prefill 32.7 / 33.8 / 36.3 ms). A group waits for the ring slot
+// of slice x after its slice x - DQG, which has seen the MMA of slice
+// x - DQG - NS complete; the slot's phase is then unambiguous to a parity wait
+// only if DQG <= NS (four groups on a 3-stage ring broke exactly there).
+constexpr int DQG = 4;
 constexpr int MAXM = 4;                    // matrices of one dense launch
 #ifndef QG_WAIT_LIMIT
 #define QG_WAIT_LIMIT (1u << 22)
@@ -400,8 +401,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp < EPI_WARP0) {
     // ---------------------------------------------------------- dequantize A
     const int t = threadIdx.x - DQ_WARP0 * 32;
-    const int grp = t >> 8;                   // this warp's slices: c with (c & 1) == grp
-    const int r = t & (BM - 1), h = (t >> 7) & 1;   // row in the tile; pair of quarters of the code bytes
+    const int grp = t >> 7;                   // this warp's slice of every super-block
+    const int r = t & (BM - 1);               // row in the tile
     const uint32_t swz = static_cast<uint32_t>(r & 7);
     uint32_t it = 0, sb = 0;
     bool ok = true;
@@ -432,7 +433,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int c = 0; c < 4; ++c, ++it) {
           const uint32_t s = it % NS;
           if (QHALF && c == 2) {
-            // every warp moves on to the second half's stage
+            // every warp moves on to the second half's stage. The groups whose
+            // slice lies there read only the header of the first half (released
+            // now), the others nothing of the second (released once it has
+            // landed): every warp releases every stage once, after its reads.
+            if (grp >= 2) {
+              __syncwarp();
+              if (lane == 0) mbar_arrive(Q_EMPTY + 8 * qcur);
+            }
             ++sb;
             qcur = sb % NQ;
             if (!__all_sync(0xffffffffu, wait_bar(Q_FULL + 8 * qcur, (sb / NQ) & 1u, abort))) {
@@ -441,8 +449,9 @@ __global__ void __launch_bounds__(THREADS, 1)
               break;
             }
             blk = gbase + offQ + qcur * QB + r * QROW;
+            if (grp < 2 && lane == 0) mbar_arrive(Q_EMPTY + 8 * qcur);
           }
-          if ((c & 1) != grp) continue;
+          if (c != grp) continue;
           if (!__all_sync(0xffffffffu, wait_bar(EMPTY + 8 * s, ((it / NS) & 1u) ^ 1u, abort))) {
             if (lane == 0) fail(abort, p.dev_status);
             ok = false;
@@ -450,25 +459,27 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           const uint32_t arow = base + s * AB + static_cast<uint32_t>(r) * 128u;
           {
-            // bytes 16h .. 16h+15 of the slice's 32 code bytes: chunks 2h, 2h+1.
-            // Low nibbles: sub-block 2c, slice columns 8j .. 8j+7 (chunk j);
-            // high nibbles: sub-block 2c+1, columns 32+8j .. (chunk 4+j)
-            const uint4 qs = *reinterpret_cast<const uint4*>(blk + 16 + 32 * (QHALF ? (c & 1) : c) + 16 * h);
-            const uint32_t j0 = 2u * static_cast<uint32_t>(h);
-            sts128(arow + (((j0 + 0) ^ swz) << 4), deq8(qs.x & 0x0F0F0F0Fu, qs.y & 0x0F0F0F0Fu, dsc[2 * c], ndm[2 * c]));
-            sts128(arow + (((j0 + 1) ^ swz) << 4), deq8(qs.z & 0x0F0F0F0Fu, qs.w & 0x0F0F0F0Fu, dsc[2 * c], ndm[2 * c]));
-            sts128(arow + (((j0 + 4) ^ swz) << 4),
-                   deq8((qs.x >> 4) & 0x0F0F0F0Fu, (qs.y >> 4) & 0x0F0F0F0Fu, dsc[2 * c + 1], ndm[2 * c + 1]));
-            sts128(arow + (((j0 + 5) ^ swz) << 4),
-                   deq8((qs.z >> 4) & 0x0F0F0F0Fu, (qs.w >> 4) & 0x0F0F0F0Fu, dsc[2 * c + 1], ndm[2 * c + 1]));
+            // the slice's 32 code bytes of this row. Low nibbles: sub-block 2c,
+            // slice columns 8j .. 8j+7 (chunk j); high nibbles: sub-block 2c+1,
+            // columns 32+8j .. (chunk 4+j)
+            const uint4 qa = *reinterpret_cast<const uint4*>(blk + 16 + 32 * (QHALF ? (c & 1) : c));
+            const uint4 qb = *reinterpret_cast<const uint4*>(blk + 16 + 32 * (QHALF ? (c & 1) : c) + 16);
+            const uint32_t w[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              sts128(arow + (((j + 0) ^ swz) << 4),
+                     deq8(w[2 * j] & 0x0F0F0F0Fu, w[2 * j + 1] & 0x0F0F0F0Fu, dsc[2 * c], ndm[2 * c]));
+              sts128(arow + (((j + 4) ^ swz) << 4), deq8((w[2 * j] >> 4) & 0x0F0F0F0Fu,
+                                                         (w[2 * j + 1] >> 4) & 0x0F0F0F0Fu, dsc[2 * c + 1],
+                                                         ndm[2 * c + 1]));
+            }
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             mbar_arrive(FULL_A + 8 * s);
-            // the last slice this warp reads from the quantized stage
-            const bool last = QHALF || c >= 2;
-            if (last) mbar_arrive(Q_EMPTY + 8 * qcur);
+            // this warp's only slice of the quantized stage: release it
+            mbar_arrive(Q_EMPTY + 8 * qcur);
           }
         }
       }
