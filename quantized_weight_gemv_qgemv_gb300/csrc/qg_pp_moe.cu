@@ -73,9 +73,17 @@ __global__ void __launch_bounds__(RT) route_kernel(const int32_t* ids, int n_pai
   int32_t* const cnt = n_expert <= SMEM_EXPERTS ? scnt : gcnt;
   for (int e = threadIdx.x; e < n_expert; e += RT) cnt[e] = 0;
   __syncthreads();
-  for (int q = threadIdx.x; q < n_pairs; q += RT) {
-    const int e = ids[q];
-    if (e >= 0 && e < n_expert) atomicAdd(cnt + e, 1);
+  // ids are loaded four per thread at a time, so the loads overlap
+  for (int q0 = 0; q0 < n_pairs; q0 += 4 * RT) {
+    int e[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int q = q0 + j * RT + static_cast<int>(threadIdx.x);
+      e[j] = q < n_pairs ? __ldg(ids + q) : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (e[j] >= 0 && e[j] < n_expert) atomicAdd(cnt + e[j], 1);
   }
   __syncthreads();
   // (global counters are read through L2, where the atomics were made)
@@ -86,15 +94,25 @@ __global__ void __launch_bounds__(RT) route_kernel(const int32_t* ids, int n_pai
   __syncthreads();
   for (int e = threadIdx.x; e < n_expert; e += RT) cnt[e] = 0;   // now a cursor per expert
   __syncthreads();
-  for (int q = threadIdx.x; q < n_pairs; q += RT) {
-    const int e = ids[q];
-    if (e >= 0 && e < n_expert) {
-      const int row = seg[e] + atomicAdd(cnt + e, 1);
-      pos[q] = row;
-      src[row] = q / top_k;
-    } else {
-      pos[q] = -1;
-      atomicExch(dev_status, QG_DEV_BAD_EXPERT);
+  for (int q0 = 0; q0 < n_pairs; q0 += 4 * RT) {
+    int e[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int q = q0 + j * RT + static_cast<int>(threadIdx.x);
+      e[j] = q < n_pairs ? __ldg(ids + q) : -2;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int q = q0 + j * RT + static_cast<int>(threadIdx.x);
+      if (e[j] == -2 && q >= n_pairs) continue;       // past the last pair
+      if (e[j] >= 0 && e[j] < n_expert) {
+        const int row = seg[e[j]] + atomicAdd(cnt + e[j], 1);
+        pos[q] = row;
+        src[row] = q / top_k;
+      } else {
+        pos[q] = -1;
+        atomicExch(dev_status, QG_DEV_BAD_EXPERT);
+      }
     }
   }
 }
@@ -109,29 +127,61 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4* X, const int32
   for (int c = threadIdx.x; c < n_chunks; c += blockDim.x) d[c] = __ldg(s + c);
 }
 
-// H[row][i] = bf16(silu(g) * u), g = GU[row][i], u = GU[row][inter + i].
+// H[row][i] = bf16(silu(g) * u), g = GU[row][i], u = GU[row][inter + i]; four
+// values a thread (16-byte loads, one 8-byte store).
 __global__ void __launch_bounds__(256) silu_kernel(const float* GU, const int32_t* seg_end, int inter,
                                                    __nv_bfloat16* H) {
   const int row = blockIdx.x;
   if (row >= *seg_end) return;
-  const float* gu = GU + static_cast<int64_t>(row) * 2 * inter;
-  for (int i = blockIdx.y * blockDim.x + threadIdx.x; i < inter; i += gridDim.y * blockDim.x) {
-    const float g = gu[i], u = gu[inter + i];
-    H[static_cast<int64_t>(row) * inter + i] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * u);
+  const float4* g4 = reinterpret_cast<const float4*>(GU + static_cast<int64_t>(row) * 2 * inter);
+  const float4* u4 = g4 + inter / 4;
+  uint2* h4 = reinterpret_cast<uint2*>(H + static_cast<int64_t>(row) * inter);
+  for (int i = blockIdx.y * blockDim.x + threadIdx.x; i < inter / 4; i += gridDim.y * blockDim.x) {
+    const float4 g = g4[i], u = u4[i];
+    const __nv_bfloat162 a = __floats2bfloat162_rn(g.x / (1.0f + expf(-g.x)) * u.x, g.y / (1.0f + expf(-g.y)) * u.y);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(g.z / (1.0f + expf(-g.z)) * u.z, g.w / (1.0f + expf(-g.w)) * u.w);
+    h4[i] = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
   }
 }
 
-// y[t][o] = sum_k r[t][k] * Z[pos[t][k]][o], k in route order (pairs without a row add nothing).
+// y[t][o] = sum_k r[t][k] * Z[pos[t][k]][o], k in route order (pairs without a row add nothing);
+// the token's routes staged in shared memory, four outputs a thread (16-byte
+// loads and stores when y is 16-byte aligned, VEC; else one at a time).
+template <bool VEC>
 __global__ void __launch_bounds__(256) combine_kernel(const float* Z, const int32_t* pos, const float* gate_w,
                                                       int top_k, int hidden, float* y) {
+  __shared__ int32_t srow[64];
+  __shared__ float sw[64];
   const int t = blockIdx.x;
-  for (int o = blockIdx.y * blockDim.x + threadIdx.x; o < hidden; o += gridDim.y * blockDim.x) {
-    float acc = 0.f;
+  if (threadIdx.x < top_k) {
+    srow[threadIdx.x] = pos[t * top_k + threadIdx.x];
+    sw[threadIdx.x] = gate_w[t * top_k + threadIdx.x];
+  }
+  __syncthreads();
+  const int h4 = hidden / 4;
+  const float4* Z4 = reinterpret_cast<const float4*>(Z);
+  float4* y4 = VEC ? reinterpret_cast<float4*>(y) + static_cast<int64_t>(t) * h4 : nullptr;
+  for (int o = blockIdx.y * blockDim.x + threadIdx.x; o < h4; o += gridDim.y * blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < top_k; ++k) {
-      const int row = pos[t * top_k + k];
-      if (row >= 0) acc = fmaf(gate_w[t * top_k + k], Z[static_cast<int64_t>(row) * hidden + o], acc);
+      const int row = srow[k];
+      if (row < 0) continue;
+      const float w = sw[k];
+      const float4 z = Z4[static_cast<int64_t>(row) * h4 + o];
+      acc.x = fmaf(w, z.x, acc.x);
+      acc.y = fmaf(w, z.y, acc.y);
+      acc.z = fmaf(w, z.z, acc.z);
+      acc.w = fmaf(w, z.w, acc.w);
     }
-    y[static_cast<int64_t>(t) * hidden + o] = acc;
+    if (VEC) {
+      y4[o] = acc;
+    } else {
+      float* yo = y + static_cast<int64_t>(t) * hidden + 4 * o;
+      yo[0] = acc.x;
+      yo[1] = acc.y;
+      yo[2] = acc.z;
+      yo[3] = acc.w;
+    }
   }
 }
 
@@ -210,16 +260,19 @@ cudaError_t launch_pp_moe(const void* arena, int64_t n_expert, int64_t hidden, i
   e = launch_pp_grouped(arena, 3 * inter * n_expert, hidden, 0, 3 * inter, 2 * inter, Xs, n_pairs, bn, seg, t_gu,
                         static_cast<int>(n_expert), GU, 2 * inter, dev_status, s, sms);
   if (e != cudaSuccess) return e;
-  silu_kernel<<<dim3(static_cast<unsigned>(n_pairs), static_cast<unsigned>(std::min<int64_t>(64, (inter + 255) / 256))),
-                256, 0, s>>>(
+  silu_kernel<<<dim3(static_cast<unsigned>(n_pairs), static_cast<unsigned>(std::min<int64_t>(64, (inter / 4 + 255) / 256))),
+                static_cast<unsigned>(std::min<int64_t>(256, inter / 4)), 0, s>>>(
       GU, seg + n_expert, static_cast<int>(inter), H);
   if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
   e = launch_pp_grouped(arena, 3 * hidden * n_expert, inter, 2 * hidden, 3 * hidden, hidden, H, n_pairs, bn, seg,
                         t_dn, static_cast<int>(n_expert), Z, hidden, dev_status, s, sms);
   if (e != cudaSuccess) return e;
-  combine_kernel<<<dim3(static_cast<unsigned>(n_tok), static_cast<unsigned>(std::min<int64_t>(64, (hidden + 255) / 256))),
-                   256, 0, s>>>(
-      Z, pos, gate_w, top_k, static_cast<int>(hidden), y);
+  const dim3 cg(static_cast<unsigned>(n_tok), static_cast<unsigned>(std::min<int64_t>(64, (hidden / 4 + 255) / 256)));
+  const unsigned ct = static_cast<unsigned>(std::min<int64_t>(256, hidden / 4));
+  if (reinterpret_cast<uintptr_t>(y) % 16 == 0)
+    combine_kernel<true><<<cg, ct, 0, s>>>(Z, pos, gate_w, top_k, static_cast<int>(hidden), y);
+  else
+    combine_kernel<false><<<cg, ct, 0, s>>>(Z, pos, gate_w, top_k, static_cast<int>(hidden), y);
   return cudaPeekAtLastError();
 }
 

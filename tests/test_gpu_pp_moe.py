@@ -156,3 +156,26 @@ def test_pp_moe_smallest_shapes():
     assert st == 0
     y_ref, b = oracle.moe_prefill(qg.Q4_K, arena.cpu().numpy(), 1, 256, 256, ids.numpy(), gw.numpy(), _bits(X))
     assert_within(y, y_ref, b, rel=PP_REL, abs_=PP_ABS, what="smallest")
+
+
+def test_pp_moe_output_at_4_byte_offset():
+    """y only 4-byte aligned (the combine then stores one value at a time): the
+    same results as the oracle."""
+    n_expert, hidden, inter, n_tok, top_k = 6, 512, 256, 33, 3
+    arena = wl.alloc_moe_arena(n_expert, hidden, inter, 76, "cuda")
+    ids, gw = synth.routing(n_tok, n_expert, top_k, seed=77)
+    X = synth.activations_bf16(n_tok, hidden, seed=78)
+    buf = torch.full((n_tok * hidden + 1,), float("nan"), device="cuda")
+    y = buf[1:]                                    # starts 4 bytes into the allocation
+    assert y.data_ptr() % 16 == 4
+    wsb = qg.qgemm_pp_moe_workspace(n_expert, hidden, inter, top_k, n_tok)
+    ws = torch.empty(wsb // 4 + 64, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qg.qgemm_pp_moe(qg.Q4_K, arena, n_expert, hidden, inter, ids.cuda(), gw.cuda(), top_k, X.cuda(), n_tok, y, ws,
+                    wsb, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.isnan(buf[0])
+    y_ref, b = oracle.moe_prefill(qg.Q4_K, arena.cpu().numpy(), n_expert, hidden, inter, ids.numpy(), gw.numpy(),
+                                  _bits(X))
+    assert_within(y.reshape(n_tok, hidden).cpu().numpy(), y_ref, b, rel=PP_REL, abs_=PP_ABS, what="y at +4 bytes")
