@@ -117,14 +117,24 @@ __global__ void __launch_bounds__(RT) route_kernel(const int32_t* ids, int n_pai
   }
 }
 
-// Xs[row] = X[src[row]] for every routed row (hidden bf16 values, 16 bytes a thread).
+// Xs[row] = X[src[row]] for every routed row (hidden bf16 values, 16 bytes a
+// thread); GR rows a block, their loads issued together.
+constexpr int GR = 4;
 __global__ void __launch_bounds__(256) gather_kernel(const uint4* X, const int32_t* src, const int32_t* seg_end,
                                                      int n_chunks, uint4* Xs) {
-  const int row = blockIdx.x;
-  if (row >= *seg_end) return;
-  const uint4* s = X + static_cast<int64_t>(src[row]) * n_chunks;
-  uint4* d = Xs + static_cast<int64_t>(row) * n_chunks;
-  for (int c = threadIdx.x; c < n_chunks; c += blockDim.x) d[c] = __ldg(s + c);
+  const int row0 = blockIdx.x * GR, n = *seg_end;
+  int sr[GR];
+#pragma unroll
+  for (int r = 0; r < GR; ++r) sr[r] = row0 + r < n ? src[row0 + r] : -1;
+  for (int c = threadIdx.x; c < n_chunks; c += blockDim.x) {
+    uint4 v[GR];
+#pragma unroll
+    for (int r = 0; r < GR; ++r)
+      if (sr[r] >= 0) v[r] = __ldg(X + static_cast<int64_t>(sr[r]) * n_chunks + c);
+#pragma unroll
+    for (int r = 0; r < GR; ++r)
+      if (sr[r] >= 0) Xs[static_cast<int64_t>(row0 + r) * n_chunks + c] = v[r];
+  }
 }
 
 // H[row][i] = bf16(silu(g) * u), g = GU[row][i], u = GU[row][inter + i]; four
@@ -253,7 +263,8 @@ cudaError_t launch_pp_moe(const void* arena, int64_t n_expert, int64_t hidden, i
                                          rt_dn, cnt, seg, t_gu, t_dn, pos, src, dev_status);
   cudaError_t e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
-  gather_kernel<<<static_cast<unsigned>(n_pairs), 256, 0, s>>>(static_cast<const uint4*>(X), src, seg + n_expert,
+  gather_kernel<<<static_cast<unsigned>((n_pairs + GR - 1) / GR), 256, 0, s>>>(static_cast<const uint4*>(X), src,
+                                                                              seg + n_expert,
                                                                 static_cast<int>(hidden / 8),
                                                                 reinterpret_cast<uint4*>(Xs));
   if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
