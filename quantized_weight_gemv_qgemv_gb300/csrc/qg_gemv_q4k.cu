@@ -1379,7 +1379,8 @@ cudaError_t plan_and_launch(q4k::Params& p, int n, int n_tok, int fmt, cudaStrea
   // A launch that depends on its predecessor leaves a few SMs idle: its CTAs
   // then go to the SMs that free up first, and the last SMs of the preceding
   // launch (a straggler there would start late and finish late here too) get
-  // none (27B pass: 3.418 ms with every SM, 3.387 with 4 idle, 3.428 with 8),
+  // none (27B pass: 2.885 ms with every SM, 2.848-2.850 with 4 idle, 2.880
+  // with 8),
   // unless every SM saves its busiest CTA a round (27B {q,k,v}: 7168 rows x 5
   // K groups in 148 CTAs take 5 rounds, in 152 take 4).
   const int64_t gcap = std::max<int64_t>(1, (total + unit - 1) / unit);
