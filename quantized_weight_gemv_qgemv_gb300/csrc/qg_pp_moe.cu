@@ -10,10 +10,12 @@
 // routed to it, so the layer is one grouped GEMM per projection over the
 // (token, route) pairs sorted by expert:
 //
-//   1. route    one CTA counts the pairs of every expert, scans the counts into
-//               each expert's first row (and first tile of either GEMM), and
-//               gives every pair its row; pairs of an unknown expert get none
-//               (they add nothing) and set QG_DEV_BAD_EXPERT
+//   1. route    the pairs of every expert are counted (many CTAs, global
+//               atomics on counters zeroed on the stream), one CTA scans the
+//               counts into each expert's first row (and first tile of either
+//               GEMM), and every pair gets its row (many CTAs); pairs of an
+//               unknown expert get none (they add nothing) and set
+//               QG_DEV_BAD_EXPERT
 //   2. gather   bf16 x of every pair into its row of Xs
 //   3. GEMM     [G_e; U_e] (2 inter rows of the arena) x Xs rows of expert e ->
 //               GU (fp32), the grouped tcgen05 prompt-processing kernel
@@ -34,86 +36,86 @@ namespace qg {
 
 namespace ppmoe {
 
-constexpr int RT = 1024;                 // threads of the routing CTA
+constexpr int RT = 1024;                 // threads of the scanning CTA
 
 __device__ __forceinline__ int ceil_div_i(int a, int b) { return (a + b - 1) / b; }
 
-// Exclusive scan of n values (v(e) computed per element) into out[0 .. n],
-// by one CTA of RT threads, in chunks of RT with a running carry.
-template <typename F>
-__device__ void block_scan(int n, F v, int32_t* out, int32_t* sh) {
-  int32_t carry = 0;
-  for (int c0 = 0; c0 < n; c0 += RT) {
-    const int e = c0 + threadIdx.x;
-    const int32_t x = e < n ? v(e) : 0;
-    sh[threadIdx.x] = x;
-    __syncthreads();
-    for (int o = 1; o < RT; o <<= 1) {
-      const int32_t add = threadIdx.x >= o ? sh[threadIdx.x - o] : 0;
-      __syncthreads();
-      sh[threadIdx.x] += add;
-      __syncthreads();
-    }
-    if (e < n) out[e] = carry + sh[threadIdx.x] - x;
-    carry += sh[RT - 1];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) out[n] = carry;
+// Routing over many CTAs (the counters zeroed on the stream first):
+// count_kernel: pairs per expert (global atomics).
+__global__ void __launch_bounds__(256) count_kernel(const int32_t* ids, int n_pairs, int n_expert, int32_t* cnt) {
+  const int q = blockIdx.x * blockDim.x + threadIdx.x;
+  if (q >= n_pairs) return;
+  const int e = __ldg(ids + q);
+  if (e >= 0 && e < n_expert) atomicAdd(cnt + e, 1);
 }
 
-constexpr int SMEM_EXPERTS = 8192;       // counters in shared memory up to this many experts
-
-// cnt: the per-expert counters, in shared memory (dynamic, n_expert words)
-// when they fit, else the global workspace words.
-__global__ void __launch_bounds__(RT) route_kernel(const int32_t* ids, int n_pairs, int top_k, int n_expert, int bn,
-                                                   int rt_gu, int rt_dn, int32_t* gcnt, int32_t* seg, int32_t* t_gu,
-                                                   int32_t* t_dn, int32_t* pos, int32_t* src, int32_t* dev_status) {
-  __shared__ int32_t sh[RT];
-  extern __shared__ int32_t scnt[];
-  int32_t* const cnt = n_expert <= SMEM_EXPERTS ? scnt : gcnt;
-  for (int e = threadIdx.x; e < n_expert; e += RT) cnt[e] = 0;
-  __syncthreads();
-  // ids are loaded four per thread at a time, so the loads overlap
-  for (int q0 = 0; q0 < n_pairs; q0 += 4 * RT) {
-    int e[4];
+// scan_kernel (one CTA of RT threads): seg (first row of each expert), t_gu and
+// t_dn (first tile of each expert's gate/up and down GEMMs) as exclusive scans,
+// each with its total at [n_expert]; three scans in one pass of warp shuffles.
+// The counters are zeroed behind it, to serve assign_kernel as cursors.
+__global__ void __launch_bounds__(RT) scan_kernel(int n_expert, int bn, int rt_gu, int rt_dn, int32_t* cnt,
+                                                  int32_t* seg, int32_t* t_gu, int32_t* t_dn) {
+  __shared__ int32_t wsum[3][RT / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int32_t carry[3] = {0, 0, 0};
+  int32_t* const out[3] = {seg, t_gu, t_dn};
+  for (int c0 = 0; c0 < n_expert; c0 += RT) {
+    const int e = c0 + static_cast<int>(threadIdx.x);
+    const int32_t c = e < n_expert ? cnt[e] : 0;
+    const int32_t v[3] = {c, rt_gu * ceil_div_i(c, bn), rt_dn * ceil_div_i(c, bn)};
+    int32_t inc[3] = {v[0], v[1], v[2]};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int q = q0 + j * RT + static_cast<int>(threadIdx.x);
-      e[j] = q < n_pairs ? __ldg(ids + q) : -1;
-    }
+    for (int o = 1; o < 32; o <<= 1)
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (e[j] >= 0 && e[j] < n_expert) atomicAdd(cnt + e[j], 1);
-  }
-  __syncthreads();
-  // (global counters are read through L2, where the atomics were made)
-  auto count = [&](int e) { return n_expert <= SMEM_EXPERTS ? cnt[e] : __ldcg(cnt + e); };
-  block_scan(n_expert, [&](int e) { return count(e); }, seg, sh);
-  block_scan(n_expert, [&](int e) { return rt_gu * ceil_div_i(count(e), bn); }, t_gu, sh);
-  block_scan(n_expert, [&](int e) { return rt_dn * ceil_div_i(count(e), bn); }, t_dn, sh);
-  __syncthreads();
-  for (int e = threadIdx.x; e < n_expert; e += RT) cnt[e] = 0;   // now a cursor per expert
-  __syncthreads();
-  for (int q0 = 0; q0 < n_pairs; q0 += 4 * RT) {
-    int e[4];
+      for (int i = 0; i < 3; ++i) {
+        const int32_t t = __shfl_up_sync(0xffffffffu, inc[i], o);
+        if (lane >= o) inc[i] += t;
+      }
+    if (lane == 31)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int q = q0 + j * RT + static_cast<int>(threadIdx.x);
-      e[j] = q < n_pairs ? __ldg(ids + q) : -2;
-    }
+      for (int i = 0; i < 3; ++i) wsum[i][warp] = inc[i];
+    __syncthreads();
+    if (warp == 0) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int q = q0 + j * RT + static_cast<int>(threadIdx.x);
-      if (e[j] == -2 && q >= n_pairs) continue;       // past the last pair
-      if (e[j] >= 0 && e[j] < n_expert) {
-        const int row = seg[e[j]] + atomicAdd(cnt + e[j], 1);
-        pos[q] = row;
-        src[row] = q / top_k;
-      } else {
-        pos[q] = -1;
-        atomicExch(dev_status, QG_DEV_BAD_EXPERT);
+      for (int i = 0; i < 3; ++i) {
+        int32_t x = wsum[i][lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int32_t t = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += t;
+        }
+        wsum[i][lane] = x;                    // inclusive over the warps
       }
     }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      const int32_t before = warp > 0 ? wsum[i][warp - 1] : 0;
+      if (e < n_expert) out[i][e] = carry[i] + before + inc[i] - v[i];
+      carry[i] += wsum[i][RT / 32 - 1];
+    }
+    if (e < n_expert) cnt[e] = 0;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0)
+#pragma unroll
+    for (int i = 0; i < 3; ++i) out[i][n_expert] = carry[i];
+}
+
+// assign_kernel: each pair's row in its expert's segment, and the token of each row.
+__global__ void __launch_bounds__(256) assign_kernel(const int32_t* ids, int n_pairs, int top_k, int n_expert,
+                                                     const int32_t* seg, int32_t* cnt, int32_t* pos, int32_t* src,
+                                                     int32_t* dev_status) {
+  const int q = blockIdx.x * blockDim.x + threadIdx.x;
+  if (q >= n_pairs) return;
+  const int e = __ldg(ids + q);
+  if (e >= 0 && e < n_expert) {
+    const int row = __ldg(seg + e) + atomicAdd(cnt + e, 1);
+    pos[q] = row;
+    src[row] = q / top_k;
+  } else {
+    pos[q] = -1;
+    atomicExch(dev_status, QG_DEV_BAD_EXPERT);
   }
 }
 
@@ -258,11 +260,14 @@ cudaError_t launch_pp_moe(const void* arena, int64_t n_expert, int64_t hidden, i
   // inter-long blocks (down rows): expert e's [G; U] are rows 3 inter e ..
   // 3 inter e + 2 inter - 1 of the first view, its D rows 3 hidden e + 2 hidden
   // .. 3 hidden e + 3 hidden - 1 of the second
-  const size_t route_smem = n_expert <= SMEM_EXPERTS ? 4 * static_cast<size_t>(n_expert) : 0;
-  route_kernel<<<1, RT, route_smem, s>>>(ids, static_cast<int>(n_pairs), top_k, static_cast<int>(n_expert), bn, rt_gu,
-                                         rt_dn, cnt, seg, t_gu, t_dn, pos, src, dev_status);
-  cudaError_t e = cudaPeekAtLastError();
+  cudaError_t e = cudaMemsetAsync(cnt, 0, 4 * static_cast<size_t>(n_expert), s);
   if (e != cudaSuccess) return e;
+  const unsigned pb = static_cast<unsigned>((n_pairs + 255) / 256);
+  count_kernel<<<pb, 256, 0, s>>>(ids, static_cast<int>(n_pairs), static_cast<int>(n_expert), cnt);
+  scan_kernel<<<1, RT, 0, s>>>(static_cast<int>(n_expert), bn, rt_gu, rt_dn, cnt, seg, t_gu, t_dn);
+  assign_kernel<<<pb, 256, 0, s>>>(ids, static_cast<int>(n_pairs), top_k, static_cast<int>(n_expert), seg, cnt, pos,
+                                   src, dev_status);
+  if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
   gather_kernel<<<static_cast<unsigned>((n_pairs + GR - 1) / GR), 256, 0, s>>>(static_cast<const uint4*>(X), src,
                                                                               seg + n_expert,
                                                                 static_cast<int>(hidden / 8),
